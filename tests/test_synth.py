@@ -1,0 +1,77 @@
+"""Generators: determinism, exact shapes of the structured workloads, and R-MAT sanity.
+
+The R-MAT check compares with the gMAGNUS page, section IV-A, Table III (scale 15,
+A.nnz/A.n = 4, B.nnz/B.n = 8: C.nnz/C.n = 477.6).  PaRMAT's internals are not on the
+page, so this is a loose statistical band, not a parity pin.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def test_counter_generator_is_deterministic_and_splittable():
+    a = synth.draws(0, 1, 0, 1000)
+    b = np.concatenate([synth.draws(0, 1, 0, 400), synth.draws(0, 1, 400, 600)])
+    assert np.array_equal(a, b)
+    assert not np.array_equal(a, synth.draws(0, 2, 0, 1000))
+    assert not np.array_equal(a, synth.draws(1, 1, 0, 1000))
+    u = synth.to_unit(synth.draws(3, 1, 0, 200000))
+    assert 0.0 <= u.min() and u.max() < 1.0 and abs(u.mean() - 0.5) < 0.005
+
+
+def test_splitmix64_reference_value():
+    # splitmix64 seeded with 0: the first output is 0xE220A8397B1DCDAF (published
+    # test vector of the algorithm).  key(0, 0) + 1*gamma reproduces that state only for
+    # the raw sequence, so check the output function directly.
+    z = np.array([0x9E3779B97F4A7C15], dtype=np.uint64)
+    assert int(synth._fin(z)[0]) == 0xE220A8397B1DCDAF
+
+
+def test_uniform_rows():
+    A = synth.config(1)
+    A.check()
+    assert A.rows == 2048 and A.nnz == 2048 * 8
+    for i in range(0, 2048, 97):
+        cols, vals = A.row(i)
+        assert len(np.unique(cols)) == 8 and np.all(np.diff(cols) > 0)
+        assert np.all((vals >= -1) & (vals < 1))
+
+
+def test_banded_shape():
+    A = synth.banded(1000, 3)
+    A.check()
+    assert A.nnz == 7 * 1000 - 12
+    cols, _ = A.row(500)
+    assert np.array_equal(cols, np.arange(497, 504))
+
+
+def test_rmat_shape_and_skew():
+    A = synth.rmat(12, 8, seed=0)
+    A.check()
+    assert A.rows == 4096
+    deg = np.diff(A.row_ptr)
+    assert deg[:64].mean() > 10 * deg[-2048:].mean()   # heavy rows sit at low indices
+    rows = np.repeat(np.arange(A.rows), deg)
+    key = rows * A.cols + A.col
+    assert len(np.unique(key)) == A.nnz               # duplicates merged
+    assert A.val.min() >= 0 and A.val.max() < 1
+
+
+def test_rmat_table3_band():
+    A = synth.rmat(15, 4, seed=1)
+    B = synth.rmat(15, 8, seed=2)
+    C, _ = oracle.spgemm(A, B, threads=4)
+    ratio = C.nnz / (1 << 15)
+    assert abs(ratio - 477.6) / 477.6 < 0.10
+
+
+def test_mcl_column_stochastic():
+    M = synth.mcl_matrix(10, 8)
+    M.check()
+    s = np.zeros(M.cols)
+    np.add.at(s, M.col, M.val)
+    assert np.allclose(s, 1.0, rtol=0, atol=1e-12)
+    diag = [i in set(M.row(i)[0].tolist()) for i in range(M.rows)]
+    assert all(diag)
