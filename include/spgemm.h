@@ -1,0 +1,180 @@
+/*
+ * spgemm.h -- C ABI of libspgemm_gb300.so: single-GPU sparse general matrix-matrix product
+ * C = A * B on CSR matrices (int64 row pointers, int32 column indices, fp64 values), for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method is the gMAGNUS pipeline ("gMAGNUS: Fast SpGEMM on GPUs for Irregular Matrices
+ * via Hierarchical Multisplit", arXiv 2607.22866v1):
+ *   - per-row intermediate-product (IP) count and light/heavy partition (section III-A,
+ *     Algorithm 3, setup phase);
+ *   - light rows: Gustavson row-wise accumulation in shared-memory hash maps, or in a
+ *     shortened dense accumulator when the row's column span is narrow (section II-B,
+ *     section III-E; bin ladder after "Ocean: Fast Estimation-Based SpGEMM on GPU",
+ *     section 4, kernel configurations);
+ *   - heavy rows: masked CSR-to-CSC of A, outer-product expansion into an intermediate
+ *     matrix C^ (section III-B, Algorithm 4), hierarchical histogram + multisplit by column
+ *     range into C^_reord (section III-C, Algorithm 5), chunk accumulation in shared memory
+ *     (section III-E) written straight to the final CSR positions;
+ *   - an exact symbolic phase that sizes C.row_ptr through a device scan, then a numeric
+ *     phase (section II-B, Algorithm 1 and the symbolic/numeric split).
+ *
+ * Conventions for every entry point:
+ *   - Return value: SPGEMM_OK (0) or one of the negative codes below; spgemm_strerror()
+ *     names it and spgemm_last_error() gives a one-line detail for the calling thread.
+ *   - "device" pointers point into the current CUDA device's global memory; "host" pointers
+ *     into ordinary process memory.  The library never frees a pointer it did not allocate.
+ *   - All GPU work is ordered on the stream given to spgemm_create (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  Calls return once the work is enqueued,
+ *     except where a host result is returned (noted below), which synchronises that stream.
+ *   - A handle is not thread-safe: use one handle per host thread.
+ *   - Failure of a device-side check (hash probe limit, inconsistent input) is reported as
+ *     SPGEMM_ERR_DEVICE at the next synchronising call; kernels never trap.
+ */
+#ifndef SPGEMM_GB300_H
+#define SPGEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------ */
+#define SPGEMM_OK 0
+#define SPGEMM_ERR_INVALID_ARG (-1)  /* null pointer, negative size, shape mismatch        */
+#define SPGEMM_ERR_INVALID_CSR (-2)  /* optional validation: row_ptr / col_idx malformed    */
+#define SPGEMM_ERR_BAD_STATE (-3)    /* call out of order (numeric before symbolic, ...)    */
+#define SPGEMM_ERR_OUT_OF_MEMORY (-4)/* workspace allocation failed                          */
+#define SPGEMM_ERR_OVERFLOW (-5)     /* a size does not fit the index types (C.cols > 2^31-1) */
+#define SPGEMM_ERR_DEVICE (-6)       /* a kernel reported an internal check failure          */
+#define SPGEMM_ERR_CUDA (-7)         /* a CUDA runtime call failed (detail in last_error)    */
+
+/* ---- option flags (spgemm_options.flags) ------------------------------------------ */
+#define SPGEMM_FLAG_ALL_HEAVY 1       /* route every non-empty row through the heavy path   */
+#define SPGEMM_FLAG_ALL_LIGHT 2       /* route every row through the light path (needs IP <= tau) */
+#define SPGEMM_FLAG_NO_DENSE_LIGHT 4  /* light rows never use the shortened dense accumulator */
+#define SPGEMM_FLAG_VALIDATE 8        /* check A and B (row_ptr monotone, columns in range)  */
+#define SPGEMM_FLAG_RECOMPUTE 16      /* never keep C^_reord between symbolic and numeric    */
+#define SPGEMM_FLAG_TIMING 32         /* record device time per phase (CUDA events, no syncs) */
+
+/* A CSR matrix in device memory, borrowed by the library (never written or freed). */
+typedef struct {
+  int64_t rows, cols, nnz;
+  const int64_t* row_ptr; /* device, rows+1 entries, row_ptr[0] = 0, non-decreasing, row_ptr[rows] = nnz */
+  const int32_t* col_idx; /* device, nnz entries, 0 <= col < cols; rows need not be sorted; repeats are separate terms */
+  const double* vals;     /* device, nnz entries */
+} spgemm_csr;
+
+/* Planner overrides; a zero field means "derive from the device".  Used by tests (to force
+ * several multisplit levels and both paths on tiny inputs) and for tuning. */
+typedef struct {
+  int64_t tau;               /* heavy threshold: rows (and chunks) with more IP are heavy */
+  int64_t chunk_width;       /* dense accumulator width W of the last level (power of two) */
+  int64_t chunks_max;        /* most chunks one multisplit level may create (power of two) */
+  int64_t heavy_batch_elems; /* most heavy intermediate products expanded at once          */
+  int64_t smem_bytes;        /* shared-memory budget s_LM per thread block                 */
+  int32_t flags;             /* SPGEMM_FLAG_* */
+  int32_t reserved;
+} spgemm_options;
+
+#define SPGEMM_MAX_LEVELS 8
+
+/* Parameters of the gMAGNUS planner (gMAGNUS page, section III-D, Eq. (4)-(7)). */
+typedef struct {
+  int64_t s_lm;              /* shared-memory bytes per block the accumulators may use      */
+  int64_t tau;               /* heavy threshold, Eq. (4): s_LM / (alpha * (s_col + s_val)), alpha = 2 */
+  int64_t dense_numeric;     /* n_denseNumeric = s_LM / (s_val + s_bitmap), bitmap = 1/8 byte */
+  int64_t chunk_width;       /* W: dense_numeric floored to a power of two (or override)    */
+  int64_t chunks_required;   /* ceil(C.cols / W) rounded up to a power of two                */
+  int64_t chunks_max;        /* Eq. (6) for this build's multisplit kernel, floored to pow2  */
+  int32_t levels;            /* Eq. (7): ceil(log2(required) / log2(max)), 1 if required <= max */
+  int32_t reserved;
+  int64_t v_chunks[SPGEMM_MAX_LEVELS]; /* chunks per row per level: max, ..., required / max^(levels-1) */
+  int64_t group_elems_op;    /* flattened elements per outer-product thread block            */
+  int64_t group_elems_ms;    /* flattened elements per histogram / multisplit thread block   */
+  int64_t group_rows;        /* n_groupRows = ceil((group_elems_ms - 1) / tau) + 1           */
+} spgemm_plan;
+
+/* Counters of one product, filled after spgemm_create / spgemm_symbolic. */
+typedef struct {
+  int64_t m, k, n;
+  int64_t ip_total;          /* intermediate products of all rows                      */
+  int64_t ip_heavy;          /* of heavy rows                                           */
+  int64_t rows_heavy, rows_light, rows_empty;
+  int64_t rows_dense_light;  /* light rows on the shortened dense accumulator           */
+  int64_t c_nnz;             /* -1 before spgemm_symbolic                               */
+  int64_t heavy_batches;     /* expansions of heavy rows per phase                      */
+  int64_t levels_run;        /* multisplit levels executed (<= plan.levels)             */
+  int64_t final_chunks;      /* C^_reord rows accumulated                               */
+  int64_t chunks_dense;      /* of which on the dense accumulator                       */
+  int64_t chat_bytes;        /* bytes of C^ col+val per batch buffer (largest batch)    */
+  int64_t c_nnz_heavy;       /* entries of C in heavy rows (after spgemm_symbolic)      */
+  int32_t resident;          /* 1: C^_reord kept from symbolic to numeric               */
+  int32_t reserved;
+} spgemm_stats;
+
+typedef struct spgemm_ctx* spgemm_handle;
+
+/* Planner alone (host only, no GPU).  c_cols = C.cols; s_lm = shared-memory bytes per block
+ * (opt-in maximum on the device); ov may be NULL.  Fills *out.  gMAGNUS page, section
+ * III-D.  Returns SPGEMM_ERR_INVALID_ARG for c_cols < 0, s_lm < 4096, or overrides that are
+ * not powers of two. */
+int spgemm_plan_params(int64_t c_cols, int64_t s_lm, const spgemm_options* ov, spgemm_plan* out);
+
+/* Start a product C = A * B with A m-by-k and B k-by-n.  Borrows A and B (device CSR), which
+ * must stay valid and unchanged until spgemm_destroy.  Runs the setup phase (gMAGNUS page,
+ * Algorithm 3, setup part: planner, IP per row, partition and binning) and synchronises the
+ * stream once to read the bin sizes.  On success *h owns its device workspace.  stream is a
+ * cudaStream_t.  Errors: INVALID_ARG (null pointers, A.cols != k, B.rows != k, negative or
+ * inconsistent sizes), OVERFLOW (n > 2^31-1), INVALID_CSR (with SPGEMM_FLAG_VALIDATE),
+ * OUT_OF_MEMORY, CUDA. */
+int spgemm_create(spgemm_handle* h, int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
+                  const spgemm_csr* B, void* stream);
+int spgemm_create_ex(spgemm_handle* h, int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
+                     const spgemm_csr* B, void* stream, const spgemm_options* opt);
+
+/* Symbolic phase: writes C.row_ptr (device, m+1 int64, caller-owned) and *c_nnz (host).
+ * Row i of C holds every column that receives at least one product, including sums that are
+ * exactly zero.  Synchronises the stream.  May be called once per handle. */
+int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz);
+
+/* Numeric phase: writes C.col_idx (device, c_nnz int32) and C.vals (device, c_nnz fp64),
+ * caller-owned, each row sorted by column, at the positions of the row_ptr from
+ * spgemm_symbolic (which must still hold those values).  May be called more than once. */
+int spgemm_numeric(spgemm_handle h, int32_t* c_col_idx, double* c_vals);
+
+/* Numeric phase for rows [row_begin, row_end) only, written at offset 0 = row_ptr[row_begin]
+ * of the given arrays (which need row_ptr[row_end] - row_ptr[row_begin] entries).  Lets a
+ * caller stream a C too large for the device in row blocks. */
+int spgemm_numeric_rows(spgemm_handle h, int64_t row_begin, int64_t row_end, int32_t* c_col_idx,
+                        double* c_vals);
+
+int spgemm_get_stats(spgemm_handle h, spgemm_stats* out);
+int spgemm_get_plan(spgemm_handle h, spgemm_plan* out);
+
+/* Cumulative device time (milliseconds, CUDA events recorded on the handle's stream around
+ * every timed region) and number of timed regions per slot, since create:
+ *   0 setup, 1 light symbolic, 2 masked CSR-to-CSC + slice offsets, 3 outer-product kernel,
+ *   4 histogram kernel, 5 multisplit kernel, 6 multisplit bookkeeping (partition, offsets),
+ *   7 heavy chunk symbolic, 8 chunk offsets, 9 C.row_ptr scan, 10 light numeric,
+ *   11 heavy chunk numeric.
+ * Only recorded when the handle was created with SPGEMM_FLAG_TIMING or the environment
+ * variable SPGEMM_TIMING=1.  Synchronises the stream.  t and launches (may be NULL) receive
+ * min(count, 12) entries. */
+int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_t count);
+
+/* Number of kernels this library has launched in the process so far (all handles). */
+long long spgemm_kernel_launches(void);
+
+/* Release the workspace (stream-ordered on the handle's stream) and the handle.  NULL is ok. */
+int spgemm_destroy(spgemm_handle h);
+
+const char* spgemm_strerror(int code);
+/* Detail of the last failure on the calling host thread ("" if none). */
+const char* spgemm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPGEMM_GB300_H */

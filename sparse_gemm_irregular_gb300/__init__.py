@@ -1,0 +1,123 @@
+"""Single-GPU SpGEMM C = A * B on CSR matrices for NVIDIA GB300 (sm_103a).
+
+The product runs in the hand-written CUDA kernels of libspgemm_gb300.so (C ABI in
+include/spgemm.h).  This package only marshals arguments: ``DeviceCSR`` keeps a CSR matrix in
+PyTorch device tensors, and ``multiply`` drives create / symbolic / numeric / destroy.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+from . import binding
+from .binding import (SpgemmError, load, options, spgemm_create, spgemm_destroy, spgemm_get_phase_times,
+                      spgemm_get_plan, spgemm_get_stats, spgemm_kernel_launches, spgemm_last_error, spgemm_numeric,
+                      spgemm_numeric_rows, spgemm_plan_params, spgemm_strerror, spgemm_symbolic)
+
+__all__ = [
+    "DeviceCSR", "multiply", "Product", "SpgemmError", "load", "options", "spgemm_create",
+    "spgemm_destroy", "spgemm_get_phase_times", "spgemm_get_plan", "spgemm_get_stats",
+    "spgemm_kernel_launches",
+    "spgemm_last_error", "spgemm_numeric", "spgemm_numeric_rows", "spgemm_plan_params",
+    "spgemm_strerror", "spgemm_symbolic",
+]
+
+
+@dataclass
+class DeviceCSR:
+    """CSR matrix in device memory: row_ptr int64 (rows+1), col int32 (nnz), val float64 (nnz)."""
+    rows: int
+    cols: int
+    row_ptr: "object"
+    col: "object"
+    val: "object"
+
+    @property
+    def nnz(self) -> int:
+        return int(self.col.numel())
+
+    @staticmethod
+    def from_host(m, device="cuda", pin: bool = False) -> "DeviceCSR":
+        """Upload a host CSR (anything with rows, cols, row_ptr, col, val numpy arrays)."""
+        import torch
+        def up(a, dt):
+            t = torch.from_numpy(a).to(dt)
+            if pin:
+                t = t.pin_memory()
+            return t.to(device, non_blocking=pin)
+        return DeviceCSR(m.rows, m.cols, up(m.row_ptr, torch.int64), up(m.col, torch.int32),
+                         up(m.val, torch.float64))
+
+    def desc(self) -> binding.spgemm_csr:
+        d = binding.spgemm_csr()
+        d.rows, d.cols, d.nnz = self.rows, self.cols, self.nnz
+        d.row_ptr = self.row_ptr.data_ptr()
+        d.col_idx = self.col.data_ptr() if self.nnz else 0
+        d.vals = self.val.data_ptr() if self.nnz else 0
+        return d
+
+    def to_host(self):
+        """(row_ptr, col, val) as numpy arrays."""
+        return self.row_ptr.cpu().numpy(), self.col.cpu().numpy(), self.val.cpu().numpy()
+
+
+class Product:
+    """One product C = A * B: the handle plus the caller-owned C arrays."""
+
+    def __init__(self, A: DeviceCSR, B: DeviceCSR, stream=None, opts=None):
+        import torch
+        self.A, self.B = A, B
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self._da, self._db = A.desc(), B.desc()  # kept alive: the library borrows the pointers
+        self.h = spgemm_create(A.rows, A.cols, B.cols, self._da, self._db, self.stream.cuda_stream, opts)
+        self.row_ptr = None
+        self.nnz = None
+
+    def symbolic(self):
+        import torch
+        self.row_ptr = torch.empty(self.A.rows + 1, dtype=torch.int64, device=self.A.row_ptr.device)
+        self.nnz = spgemm_symbolic(self.h, self.row_ptr.data_ptr())
+        return self.row_ptr, self.nnz
+
+    def numeric(self, col=None, val=None):
+        import torch
+        dev = self.A.row_ptr.device
+        if col is None:
+            col = torch.empty(max(self.nnz, 1), dtype=torch.int32, device=dev)
+        if val is None:
+            val = torch.empty(max(self.nnz, 1), dtype=torch.float64, device=dev)
+        spgemm_numeric(self.h, col.data_ptr(), val.data_ptr())
+        return col[:self.nnz], val[:self.nnz]
+
+    def numeric_rows(self, row_begin: int, row_end: int, col, val):
+        spgemm_numeric_rows(self.h, row_begin, row_end, col.data_ptr(), val.data_ptr())
+
+    def stats(self):
+        return spgemm_get_stats(self.h)
+
+    def plan(self):
+        return spgemm_get_plan(self.h)
+
+    def phase_times(self):
+        return spgemm_get_phase_times(self.h)
+
+    def close(self):
+        if self.h is not None:
+            spgemm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def multiply(A: DeviceCSR, B: DeviceCSR, stream=None, opts=None) -> DeviceCSR:
+    """C = A * B, all on the device; returns C as a DeviceCSR."""
+    p = Product(A, B, stream, opts)
+    try:
+        row_ptr, _ = p.symbolic()
+        col, val = p.numeric()
+    finally:
+        p.close()
+    return DeviceCSR(A.rows, B.cols, row_ptr, col, val)

@@ -1,0 +1,829 @@
+// C ABI and orchestration of the gMAGNUS pipeline (gMAGNUS page, Algorithm 3).
+//
+//   create    : planner, IP per row + bins (light ladder / heavy), one synchronisation.
+//   symbolic  : light rows (hash / shortened dense symbolic), heavy batches (CSC -> outer
+//               product -> levels of histogram + partition + multisplit -> chunk symbolic),
+//               scan of C.row_ptr, one synchronisation for nnz(C).
+//   numeric   : light rows (accumulate + sort + write), heavy batches (chunk accumulate +
+//               sorted write at the final positions).  The expansion is kept from symbolic
+//               to numeric when the whole heavy part fits one batch ("resident"), otherwise
+//               it is recomputed batch by batch (the device cannot hold C^ of every heavy row
+//               of the largest products).
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <memory>
+#include <string>
+
+#include "internal.h"
+
+static thread_local std::string g_last_error;
+static std::atomic<long long> g_launches{0};
+
+namespace sg {
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
+void set_last_error(const std::string& s) { g_last_error = s; }
+
+int check_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return SPGEMM_OK;
+  set_last_error(std::string(what) + ": " + cudaGetErrorString(e));
+  return SPGEMM_ERR_CUDA;
+}
+
+void* ws_alloc(spgemm_ctx* h, size_t bytes) {
+  void* p = nullptr;
+  if (bytes == 0) bytes = 16;
+  if (cudaMallocAsync(&p, bytes, h->st) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  h->allocs.push_back(p);
+  return p;
+}
+
+void ws_free(spgemm_ctx* h, void* p) {
+  if (!p) return;
+  auto it = std::find(h->allocs.begin(), h->allocs.end(), p);
+  if (it != h->allocs.end()) h->allocs.erase(it);
+  cudaFreeAsync(p, h->st);
+}
+
+Ladder make_ladder(int64_t tau) {
+  Ladder L;
+  int64_t u = 32;
+  while (u < tau && u <= 4096 && L.n < kMaxLadder - 1) {
+    L.upper[L.n++] = u;
+    u *= 2;
+  }
+  L.upper[L.n++] = tau;
+  for (int i = 0; i < L.n; ++i) {
+    const int64_t up = L.upper[i];
+    L.slots[i] = 2 * up;
+    L.tpr[i] = up <= 256 ? 32 : (up <= 512 ? 256 : (up <= 1024 ? 512 : 1024));
+  }
+  return L;
+}
+
+}  // namespace sg
+
+using namespace sg;
+
+#define SG_TRY(expr)                 \
+  do {                               \
+    int _rc = (expr);                \
+    if (_rc != SPGEMM_OK) return _rc; \
+  } while (0)
+
+#define SG_ALLOC(ptr, type, count)                                                     \
+  do {                                                                                 \
+    ptr = static_cast<type*>(ws_alloc(h, sizeof(type) * static_cast<size_t>(count))); \
+    if (!ptr) {                                                                        \
+      set_last_error("device workspace allocation failed (" #ptr ")");                \
+      return SPGEMM_ERR_OUT_OF_MEMORY;                                                 \
+    }                                                                                  \
+  } while (0)
+
+namespace {
+
+// Scan scratch that grows on demand.
+int64_t* scan_scratch(spgemm_ctx* h, int64_t n) {
+  const int64_t need = scan_scratch_elems(n);
+  if (need > h->scan_cap) {
+    ws_free(h, h->d_scan);
+    h->d_scan = static_cast<int64_t*>(ws_alloc(h, sizeof(int64_t) * need));
+    h->scan_cap = h->d_scan ? need : 0;
+  }
+  return h->d_scan;
+}
+
+int scan(spgemm_ctx* h, const int64_t* in, int64_t* out, int64_t n) {
+  int64_t* sc = scan_scratch(h, n);
+  if (!sc) {
+    set_last_error("scan scratch allocation failed");
+    return SPGEMM_ERR_OUT_OF_MEMORY;
+  }
+  scan_excl_i64(in, out, n, sc, h->st);
+  return SPGEMM_OK;
+}
+
+int sync_and_check(spgemm_ctx* h, const char* where) {
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), where));
+  SG_TRY(check_cuda(cudaGetLastError(), where));
+  uint32_t err = 0;
+  SG_TRY(check_cuda(cudaMemcpy(&err, h->d_err, sizeof(err), cudaMemcpyDeviceToHost), where));
+  if (err) {
+    char buf[160];
+    snprintf(buf, sizeof(buf), "%s: device check failed (flags 0x%x)", where, err);
+    set_last_error(buf);
+    return (err & kErrCsr) ? SPGEMM_ERR_INVALID_CSR : SPGEMM_ERR_DEVICE;
+  }
+  return SPGEMM_OK;
+}
+
+// Device time per phase: a pair of events around each timed region, read out (and the
+// stream synchronised) only by spgemm_get_phase_times, so timing adds no synchronisation.
+struct PhaseTimer {
+  spgemm_ctx* h;
+  int slot;
+  cudaEvent_t a{};
+  PhaseTimer(spgemm_ctx* hh, int s) : h(hh), slot(s) {
+    if (!h->timing) return;
+    cudaEventCreate(&a);
+    cudaEventRecord(a, h->st);
+  }
+  ~PhaseTimer() {
+    if (!h->timing) return;
+    cudaEvent_t b;
+    cudaEventCreate(&b);
+    cudaEventRecord(b, h->st);
+    h->timed[slot].push_back({a, b});
+  }
+};
+
+void drain_timers(spgemm_ctx* h) {
+  if (!h->timing) return;
+  cudaStreamSynchronize(h->st);
+  for (int s = 0; s < kPhaseSlots; ++s) {
+    for (auto& pr : h->timed[s]) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess) h->phase_ms[s] += ms;
+      h->phase_n[s] += 1;
+      cudaEventDestroy(pr.first);
+      cudaEventDestroy(pr.second);
+    }
+    h->timed[s].clear();
+  }
+}
+
+int valid_csr_desc(const spgemm_csr* M, int64_t rows, int64_t cols) {
+  if (!M) return 0;
+  if (M->rows != rows || M->cols != cols || M->nnz < 0) return 0;
+  if (!M->row_ptr) return 0;
+  if (M->nnz > 0 && (!M->col_idx || !M->vals)) return 0;
+  return 1;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Heavy batch: expansion (MaskedCsr2Csc + OuterProduct of Algorithm 3).
+int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr) {
+  std::unique_ptr<PhaseTimer> tcsc(new PhaseTimer(h, 2));
+  const int64_t R = hb.h1 - hb.h0;
+  const int32_t* rows = h->d_heavy + hb.h0;
+  const int64_t kc = h->k;
+  int32_t* colcnt;
+  int64_t *colptr, *slice_off;
+  SG_ALLOC(colcnt, int32_t, kc);
+  SG_ALLOC(colptr, int64_t, kc + 1);
+  SG_ALLOC(slice_off, int64_t, kc + 1);
+  cudaMemsetAsync(colcnt, 0, sizeof(int32_t) * kc, h->st);
+  launch_csc_count(h->A, rows, R, colcnt, h->st);
+  launch_slice_sizes(colcnt, h->B, kc, colptr, slice_off, h->st);
+  SG_TRY(scan(h, colptr, colptr, kc));
+  SG_TRY(scan(h, slice_off, slice_off, kc));
+  // nnz of the masked A: sum of the heavy rows' lengths; bounded by nnz(A)
+  int64_t nnzh = 0;
+  SG_TRY(check_cuda(cudaMemcpyAsync(&nnzh, colptr + kc, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy masked nnz"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "masked csc"));
+  int32_t* csc_row;
+  double* csc_val;
+  int64_t* cursor;
+  SG_ALLOC(csc_row, int32_t, nnzh);
+  SG_ALLOC(csc_val, double, nnzh);
+  SG_ALLOC(cursor, int64_t, std::max<int64_t>(kc, R));
+  launch_copy_i64(colptr, cursor, kc, h->st);
+  launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, h->st);
+  // C^ row pointers: heavy IP prefix of the batch; the cursor starts at each row's first slot
+  launch_offset_copy(h->d_heavy_pre + hb.h0, R + 1, h->heavy_pre[hb.h0], c_rowptr, h->st);
+  launch_copy_i64(c_rowptr, cursor, R, h->st);
+  tcsc.reset();
+  {
+    PhaseTimer t(h, 3);
+    launch_outer_product(colptr, csc_row, csc_val, slice_off, kc, hb.elems, h->B, cursor, h->d_chat_col,
+                         vals ? h->d_chat_val : nullptr, vals, h->d_err, h->st);
+  }
+  ws_free(h, colcnt);
+  ws_free(h, colptr);
+  ws_free(h, slice_off);
+  ws_free(h, csc_row);
+  ws_free(h, csc_val);
+  ws_free(h, cursor);
+  return SPGEMM_OK;
+}
+
+// Heavy batch: hierarchical multisplit (the reorder loop of Algorithm 3).  The symbolic pass records
+// the level structure (which needs the heavy-chunk counts on the host); the numeric pass of a
+// recomputed batch replays it without synchronising.
+int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const int64_t* c_rowptr) {
+  const spgemm_plan& P = h->plan;
+  const int64_t R = hb.h1 - hb.h0;
+  const int64_t cap = h->batch_cap;
+  if (record) hb.lv.clear();
+  if (P.chunks_required == 1) {
+    // one chunk per row: the rows of C^ are the final chunks
+    if (record) {
+      hb.nfinal = R;
+      SG_ALLOC(hb.f_start, int64_t, R);
+      SG_ALLOC(hb.f_cnt, int64_t, R);
+      SG_ALLOC(hb.f_row, int32_t, R);
+      SG_ALLOC(hb.f_base, int32_t, R);
+      launch_final_desc(c_rowptr, 0, R, 0, nullptr, nullptr, hb.f_start, hb.f_cnt, hb.f_row, hb.f_base, h->st);
+    }
+    return SPGEMM_OK;
+  }
+  // level inputs
+  int64_t nin = R;
+  const int64_t* in_ptr = c_rowptr;
+  int64_t in_half = 0;  // which half of the C^ buffer holds the input
+  int32_t* in_row = nullptr;
+  int32_t* in_base = nullptr;
+  int64_t in_width = P.chunk_width * P.chunks_required;  // padded column range of a C^ row
+  int64_t* prev_ptr = nullptr;
+  int64_t total_in = hb.elems;
+  std::vector<void*> to_free;
+  if (record) {
+    // descriptor capacity: level l writes at most nin_l * v_l final chunks, and the next
+    // level's input holds only heavy chunks (more than tau elements each)
+    int64_t capd = 0, rows = R;
+    for (int l = 0; l < P.levels; ++l) {
+      capd += rows * P.v_chunks[l];
+      rows = std::min<int64_t>(rows * P.v_chunks[l], hb.elems / (P.tau + 1));
+    }
+    hb.nfinal = 0;
+    SG_ALLOC(hb.f_start, int64_t, capd);
+    SG_ALLOC(hb.f_cnt, int64_t, capd);
+    SG_ALLOC(hb.f_row, int32_t, capd);
+    SG_ALLOC(hb.f_base, int32_t, capd);
+  }
+  for (int l = 0; l < P.levels; ++l) {
+    const int64_t v = P.v_chunks[l];
+    const int64_t width = in_width / v;
+    const int shift = ilog2_i64(width);
+    const bool last = (l == P.levels - 1);
+    const int64_t nout = nin * v;
+    LevelInfo li;
+    if (record) {
+      li.nin = nin;
+      li.v = v;
+      li.width = width;
+      li.desc0 = hb.nfinal;
+    } else {
+      li = hb.lv[l];
+    }
+    unsigned long long* counts;
+    int32_t *xmap = nullptr, *out_row, *out_base;
+    int64_t* rptr;
+    SG_ALLOC(counts, unsigned long long, nout);
+    SG_ALLOC(rptr, int64_t, nout + 1);
+    SG_ALLOC(out_row, int32_t, nout);
+    SG_ALLOC(out_base, int32_t, nout);
+    cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
+    const int32_t* in_col = h->d_chat_col + in_half * cap;
+    const double* in_val = h->d_chat_val ? h->d_chat_val + in_half * cap : nullptr;
+    {
+      PhaseTimer t(h, 4);
+      launch_histogram(in_ptr, nin, total_in, in_col, shift, v, P.group_rows, counts, h->d_err, h->st);
+    }
+    if (!last) {
+      // ThreshPartition of the chunks: heavy (count > tau) first, stable
+      uint8_t* pbin;
+      int32_t* plist;
+      int64_t* pcnt;
+      const int64_t nblk = bin_blocks(nout);
+      SG_ALLOC(pbin, uint8_t, nout);
+      SG_ALLOC(plist, int32_t, nout);
+      SG_ALLOC(pcnt, int64_t, 2 * nblk + 1);
+      SG_ALLOC(xmap, int32_t, nout);
+      launch_chunk_partition(counts, nout, P.tau, pbin, h->st);
+      launch_bin_count(pbin, nout, 2, pcnt, h->st);
+      SG_TRY(scan(h, pcnt, pcnt, 2 * nblk));
+      launch_bin_scatter(pbin, nout, 2, pcnt, plist, h->st);
+      launch_invert(plist, nout, xmap, h->st);
+      if (record) {
+        int64_t nh = 0;
+        SG_TRY(check_cuda(cudaMemcpyAsync(&nh, pcnt + nblk, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                          "copy heavy chunk count"));
+        SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "level partition"));
+        li.nheavy = nh;
+      }
+      ws_free(h, pbin);
+      ws_free(h, plist);
+      ws_free(h, pcnt);
+    } else {
+      li.nheavy = 0;
+    }
+    {
+      PhaseTimer t(h, 6);
+      launch_reord_meta(counts, nin, v, xmap, in_row, in_base, width, rptr, out_row, out_base, h->st);
+      SG_TRY(scan(h, rptr, rptr, nout));
+    }
+    // cursor for the multisplit reservations: starts at each C^_reord row's first slot
+    unsigned long long* cursor;
+    SG_ALLOC(cursor, unsigned long long, nout);
+    launch_copy_i64(rptr, reinterpret_cast<int64_t*>(cursor), nout, h->st);
+    const int64_t out_half = 1 - in_half;
+    {
+      PhaseTimer t(h, 5);
+      launch_multisplit(in_ptr, nin, total_in, in_col, in_val, shift, v, P.group_rows, xmap, cursor,
+                        h->d_chat_col + out_half * cap, vals ? h->d_chat_val + out_half * cap : nullptr, vals,
+                        h->d_err, h->st);
+    }
+    ws_free(h, cursor);
+    ws_free(h, counts);
+    if (xmap) ws_free(h, xmap);
+    // light outputs of this level (all outputs at the last level) are final chunks
+    if (record) {
+      const int64_t q0 = last ? 0 : li.nheavy;
+      launch_final_desc(rptr, q0, nout, out_half * cap, out_row, out_base, hb.f_start + hb.nfinal,
+                        hb.f_cnt + hb.nfinal, hb.f_row + hb.nfinal, hb.f_base + hb.nfinal, h->st);
+      hb.nfinal += nout - q0;
+      li.elem_base = out_half * cap;
+      hb.lv.push_back(li);
+    }
+    // next level: the heavy chunks (stored first) of this level's output
+    if (in_row) ws_free(h, in_row);
+    if (in_base) ws_free(h, in_base);
+    if (prev_ptr) ws_free(h, prev_ptr);
+    if (last || li.nheavy == 0) {
+      ws_free(h, rptr);
+      ws_free(h, out_row);
+      ws_free(h, out_base);
+      break;
+    }
+    int64_t heavy_elems = 0;
+    if (record) {
+      SG_TRY(check_cuda(cudaMemcpyAsync(&heavy_elems, rptr + li.nheavy, sizeof(int64_t), cudaMemcpyDeviceToHost,
+                                        h->st), "copy heavy chunk elements"));
+      SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "level input"));
+      hb.lv.back().next_elems = heavy_elems;
+    } else {
+      heavy_elems = li.next_elems;
+    }
+    nin = li.nheavy;
+    in_ptr = rptr;
+    prev_ptr = rptr;
+    in_row = out_row;
+    in_base = out_base;
+    in_half = out_half;
+    in_width = width;
+    total_in = heavy_elems;
+  }
+  return SPGEMM_OK;
+}
+
+// Accumulator bins of the final chunks (stable order), then their symbolic counts and the
+// offsets of every chunk inside its row of C.
+int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
+  const int64_t nf = hb.nfinal;
+  const int64_t R = hb.h1 - hb.h0;
+  const int nb = h->nbins;
+  SG_ALLOC(hb.f_nnz, int64_t, nf);
+  SG_ALLOC(hb.f_out, int64_t, nf);
+  SG_ALLOC(hb.f_list, int32_t, nf);
+  cudaMemsetAsync(hb.f_nnz, 0, sizeof(int64_t) * nf, h->st);
+  {
+    uint8_t* fbin;
+    int64_t* fcnt;
+    int64_t* starts;
+    const int64_t nblk = bin_blocks(nf);
+    SG_ALLOC(fbin, uint8_t, nf);
+    SG_ALLOC(fcnt, int64_t, nb * nblk + 1);
+    SG_ALLOC(starts, int64_t, nb + 1);
+    launch_chunk_classify(hb.f_cnt, nf, h->rule, fbin, h->st);
+    launch_bin_count(fbin, nf, nb, fcnt, h->st);
+    SG_TRY(scan(h, fcnt, fcnt, nb * nblk));
+    launch_bin_scatter(fbin, nf, nb, fcnt, hb.f_list, h->st);
+    launch_bin_starts(fcnt, nblk, nb, starts, h->st);
+    hb.f_bin_start.assign(nb + 1, 0);
+    SG_TRY(check_cuda(cudaMemcpyAsync(hb.f_bin_start.data(), starts, sizeof(int64_t) * (nb + 1),
+                                      cudaMemcpyDeviceToHost, h->st), "copy chunk bins"));
+    SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "chunk bins"));
+    ws_free(h, fbin);
+    ws_free(h, fcnt);
+    ws_free(h, starts);
+  }
+  {
+    PhaseTimer t(h, 7);
+    ChunkSet cs{};
+    cs.start = hb.f_start;
+    cs.cnt = hb.f_cnt;
+    cs.row = hb.f_row;
+    cs.base = hb.f_base;
+    cs.nnz = hb.f_nnz;
+    cs.heavy_rows = h->d_heavy + hb.h0;
+    cs.col = h->d_chat_col;
+    cs.val = nullptr;
+    Sink sk{};
+    sk.row_begin = 0;
+    sk.row_end = h->m;
+    for (int L = 0; L < h->lad.n; ++L) {
+      const int b = 2 * L;
+      launch_chunks(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+                    h->lad.slots[L], h->lad.tpr[L], false, 0, false, sk, h->d_err, h->st);
+    }
+    const int bd = 2 * h->lad.n;
+    launch_chunks(cs, hb.f_list + hb.f_bin_start[bd], hb.f_bin_start[bd + 1] - hb.f_bin_start[bd], 0, 1024,
+                  true, h->plan.chunk_width, false, sk, h->d_err, h->st);
+  }
+  // offsets of the chunks inside their rows
+  PhaseTimer toff(h, 8);
+  const int64_t nfin = h->plan.chunks_required;
+  const int shift_fin = ilog2_i64(h->plan.chunk_width);
+  int64_t* grid;
+  SG_ALLOC(grid, int64_t, R * nfin + 1);
+  cudaMemsetAsync(grid, 0, sizeof(int64_t) * (R * nfin + 1), h->st);
+  launch_grid_fill(hb.f_row, hb.f_base, hb.f_nnz, nf, shift_fin, nfin, grid, h->st);
+  SG_TRY(scan(h, grid, grid, R * nfin));
+  launch_grid_finish(grid, hb.f_row, hb.f_base, nf, shift_fin, nfin, hb.f_out, h->st);
+  launch_row_totals(grid, R, nfin, h->d_heavy + hb.h0, row_nnz, h->st);
+  SG_TRY(check_cuda(cudaMemcpyAsync(&hb.nnz_c, grid + R * nfin, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy heavy nnz"));
+  ws_free(h, grid);
+  return SPGEMM_OK;
+}
+
+int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
+  PhaseTimer t(h, 11);
+  ChunkSet cs{};
+  cs.start = hb.f_start;
+  cs.cnt = hb.f_cnt;
+  cs.row = hb.f_row;
+  cs.base = hb.f_base;
+  cs.nnz = hb.f_nnz;
+  cs.out = hb.f_out;
+  cs.heavy_rows = h->d_heavy + hb.h0;
+  cs.col = h->d_chat_col;
+  cs.val = h->d_chat_val;
+  for (int L = 0; L < h->lad.n; ++L) {
+    const int b = 2 * L;
+    launch_chunks(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b], h->lad.slots[L],
+                  h->lad.tpr[L], false, 0, true, sk, h->d_err, h->st);
+  }
+  const int bd = 2 * h->lad.n;
+  launch_chunks(cs, hb.f_list + hb.f_bin_start[bd], hb.f_bin_start[bd + 1] - hb.f_bin_start[bd], 0, 1024, true,
+                h->plan.chunk_width, true, sk, h->d_err, h->st);
+  return SPGEMM_OK;
+}
+
+int ensure_chat(spgemm_ctx* h, bool vals) {
+  if (!h->d_chat_col) SG_ALLOC(h->d_chat_col, int32_t, 2 * h->batch_cap);
+  if (vals && !h->d_chat_val) SG_ALLOC(h->d_chat_val, double, 2 * h->batch_cap);
+  return SPGEMM_OK;
+}
+
+void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
+  for (int L = 0; L < h->lad.n; ++L) {
+    for (int d = 0; d < 2; ++d) {
+      const int b = 2 * L + d;
+      RowJob job;
+      job.rows = h->d_rows + h->bin_start[b];
+      job.count = h->bin_start[b + 1] - h->bin_start[b];
+      job.slots = h->lad.slots[L];
+      job.tpr = h->lad.tpr[L];
+      job.dense = d == 1;
+      launch_light(h->A, h->B, h->d_span_lo, job, numeric, sk, h->d_err, h->st);
+    }
+  }
+}
+
+int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
+  if (h->state < 2) {
+    set_last_error("numeric called before symbolic");
+    return SPGEMM_ERR_BAD_STATE;
+  }
+  Sink sk{};
+  sk.row_ptr = h->c_row_ptr;
+  sk.c_col = c_col;
+  sk.c_val = c_val;
+  sk.row_begin = rb;
+  sk.row_end = re;
+  {
+    PhaseTimer t(h, 10);
+    light_pass(h, true, sk);
+  }
+  for (auto& hb : h->batches) {
+    if (hb.row_hi < rb || hb.row_lo >= re) continue;
+    if (!h->resident) {
+      SG_TRY(ensure_chat(h, true));
+      int64_t* crp;
+      SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
+      SG_TRY(heavy_expand(h, hb, true, crp));
+      SG_TRY(heavy_levels(h, hb, true, false, crp));
+      SG_TRY(heavy_chunk_numeric(h, hb, sk));
+      ws_free(h, crp);
+    } else {
+      SG_TRY(heavy_chunk_numeric(h, hb, sk));
+    }
+  }
+  return sync_and_check(h, "numeric");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------------
+extern "C" {
+
+int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
+                     const spgemm_csr* B, void* stream, const spgemm_options* opt) {
+  g_last_error.clear();
+  if (!out) return SPGEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (m < 0 || k < 0 || n < 0 || !valid_csr_desc(A, m, k) || !valid_csr_desc(B, k, n)) {
+    set_last_error("invalid shapes or CSR descriptors");
+    return SPGEMM_ERR_INVALID_ARG;
+  }
+  if (n > 0x7fffffffLL || k > 0x7fffffffLL || m > 0x7fffffffLL) {
+    set_last_error("dimensions beyond int32 indices");
+    return SPGEMM_ERR_OVERFLOW;
+  }
+  spgemm_ctx* h = new spgemm_ctx();
+  h->m = m;
+  h->k = k;
+  h->n = n;
+  h->A = *A;
+  h->B = *B;
+  h->st = static_cast<cudaStream_t>(stream);
+  if (opt) h->opt = *opt;
+  const char* tenv = getenv("SPGEMM_TIMING");
+  h->timing = (tenv && tenv[0] == '1') || (h->opt.flags & SPGEMM_FLAG_TIMING);
+  int rc = SPGEMM_OK;
+  auto fail = [&](int code) {
+    spgemm_destroy(h);
+    return code;
+  };
+  int dev = 0, sms = 0, optin = 0, l2 = 0;
+  if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice")) != SPGEMM_OK) return fail(rc);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  h->device = dev;
+  h->sms = sms;
+  h->smem_optin = optin;
+  h->l2_bytes = l2;
+  const int64_t s_lm = h->opt.smem_bytes ? h->opt.smem_bytes : optin - kSmemReserve;
+  if (s_lm + kSmemReserve > optin) {
+    set_last_error("smem_bytes exceeds the device's shared memory per block");
+    return fail(SPGEMM_ERR_INVALID_ARG);
+  }
+  if ((rc = plan_params(n, s_lm, &h->opt, &h->plan)) != SPGEMM_OK) {
+    set_last_error("planner rejected the options");
+    return fail(rc);
+  }
+  h->lad = make_ladder(h->plan.tau);
+  h->rule.n = h->lad.n;
+  for (int i = 0; i < h->lad.n; ++i) {
+    h->rule.upper[i] = h->lad.upper[i];
+    h->rule.slots[i] = h->lad.slots[i];
+  }
+  h->rule.tau = h->plan.tau;
+  h->rule.all_heavy = (h->opt.flags & SPGEMM_FLAG_ALL_HEAVY) ? 1 : 0;
+  h->rule.all_light = (h->opt.flags & SPGEMM_FLAG_ALL_LIGHT) ? 1 : 0;
+  h->rule.no_dense = (h->opt.flags & SPGEMM_FLAG_NO_DENSE_LIGHT) ? 1 : 0;
+  h->nbins = 2 * h->lad.n + 1;
+
+  PhaseTimer* tsetup = new PhaseTimer(h, 0);
+  h->d_err = static_cast<uint32_t*>(ws_alloc(h, sizeof(uint32_t)));
+  if (!h->d_err) {
+    delete tsetup;
+    return fail(SPGEMM_ERR_OUT_OF_MEMORY);
+  }
+  cudaMemsetAsync(h->d_err, 0, sizeof(uint32_t), h->st);
+  auto body = [&]() -> int {
+    if (h->opt.flags & SPGEMM_FLAG_VALIDATE) {
+      launch_validate(h->A, h->d_err, h->st);
+      launch_validate(h->B, h->d_err, h->st);
+      SG_TRY(sync_and_check(h, "input validation"));
+    }
+    const int64_t mm = std::max<int64_t>(m, 1);
+    SG_ALLOC(h->d_ip, int64_t, mm);
+    SG_ALLOC(h->d_span_lo, int32_t, mm);
+    SG_ALLOC(h->d_bin, uint8_t, mm);
+    SG_ALLOC(h->d_rows, int32_t, mm);
+    int32_t *bmin, *bmax;
+    SG_ALLOC(bmin, int32_t, std::max<int64_t>(k, 1));
+    SG_ALLOC(bmax, int32_t, std::max<int64_t>(k, 1));
+    launch_brow_minmax(h->B, bmin, bmax, h->st);
+    launch_row_ip(h->A, h->B, bmin, bmax, h->rule, h->d_ip, h->d_span_lo, h->d_bin, h->st);
+    const int nb = h->nbins;
+    const int64_t nblk = bin_blocks(m);
+    int64_t* starts;
+    SG_ALLOC(h->d_binoff, int64_t, nb * nblk + 1);
+    SG_ALLOC(starts, int64_t, nb + 1);
+    cudaMemsetAsync(h->d_binoff, 0, sizeof(int64_t) * (nb * nblk + 1), h->st);
+    launch_bin_count(h->d_bin, m, nb, h->d_binoff, h->st);
+    SG_TRY(scan(h, h->d_binoff, h->d_binoff, nb * nblk));
+    launch_bin_scatter(h->d_bin, m, nb, h->d_binoff, h->d_rows, h->st);
+    launch_bin_starts(h->d_binoff, nblk, nb, starts, h->st);
+    h->bin_start.assign(nb + 1, 0);
+    SG_TRY(check_cuda(cudaMemcpyAsync(h->bin_start.data(), starts, sizeof(int64_t) * (nb + 1),
+                                      cudaMemcpyDeviceToHost, h->st), "copy bin starts"));
+    SG_TRY(sync_and_check(h, "setup"));
+    ws_free(h, bmin);
+    ws_free(h, bmax);
+    ws_free(h, starts);
+    // heavy rows and their IP prefix
+    const int hb = 2 * h->lad.n;
+    h->nheavy = h->bin_start[hb + 1] - h->bin_start[hb];
+    h->d_heavy = h->d_rows + h->bin_start[hb];
+    // statistics
+    std::vector<int64_t> hip(1, 0);
+    h->stats.m = m;
+    h->stats.k = k;
+    h->stats.n = n;
+    h->stats.c_nnz = -1;
+    h->stats.rows_heavy = h->nheavy;
+    h->stats.rows_light = h->bin_start[hb] - h->bin_start[0];
+    h->stats.rows_empty = m - h->bin_start[nb];
+    for (int L = 0; L < h->lad.n; ++L)
+      h->stats.rows_dense_light += h->bin_start[2 * L + 2] - h->bin_start[2 * L + 1];
+    {
+      // total IP (for the statistics): scan of IP per row
+      int64_t* tmp;
+      SG_ALLOC(tmp, int64_t, m + 1);
+      SG_TRY(scan(h, h->d_ip, tmp, m));
+      SG_TRY(check_cuda(cudaMemcpyAsync(&h->stats.ip_total, tmp + m, sizeof(int64_t), cudaMemcpyDeviceToHost,
+                                        h->st), "copy ip total"));
+      SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "ip total"));
+      ws_free(h, tmp);
+    }
+    if (h->nheavy > 0) {
+      SG_ALLOC(h->d_heavy_pre, int64_t, h->nheavy + 1);
+      launch_gather_ip(h->d_heavy, h->nheavy, h->d_ip, h->d_heavy_pre, h->st);
+      SG_TRY(scan(h, h->d_heavy_pre, h->d_heavy_pre, h->nheavy));
+      h->heavy_pre.resize(h->nheavy + 1);
+      std::vector<int32_t> hrows(h->nheavy);
+      SG_TRY(check_cuda(cudaMemcpyAsync(h->heavy_pre.data(), h->d_heavy_pre, sizeof(int64_t) * (h->nheavy + 1),
+                                        cudaMemcpyDeviceToHost, h->st), "copy heavy prefix"));
+      SG_TRY(check_cuda(cudaMemcpyAsync(hrows.data(), h->d_heavy, sizeof(int32_t) * h->nheavy,
+                                        cudaMemcpyDeviceToHost, h->st), "copy heavy rows"));
+      SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "heavy prefix"));
+      h->stats.ip_heavy = h->heavy_pre[h->nheavy];
+      // batches of heavy rows whose C^ fits the budget
+      int64_t cap = h->opt.heavy_batch_elems;
+      if (!cap) {
+        size_t fr = 0, tot = 0;
+        cudaMemGetInfo(&fr, &tot);
+        cap = static_cast<int64_t>(static_cast<double>(fr) * 0.35 / 24.0);
+      }
+      int64_t i = 0, maxb = 0;
+      while (i < h->nheavy) {
+        HeavyBatch b;
+        b.h0 = i;
+        int64_t j = i + 1;
+        while (j < h->nheavy && h->heavy_pre[j + 1] - h->heavy_pre[i] <= cap) ++j;
+        b.h1 = j;
+        b.elems = h->heavy_pre[j] - h->heavy_pre[i];
+        b.row_lo = hrows[i];
+        b.row_hi = hrows[j - 1];
+        maxb = std::max(maxb, b.elems);
+        h->batches.push_back(b);
+        i = j;
+      }
+      h->batch_cap = maxb;
+      h->resident = h->batches.size() == 1 && !(h->opt.flags & SPGEMM_FLAG_RECOMPUTE);
+      h->stats.heavy_batches = static_cast<int64_t>(h->batches.size());
+      h->stats.chat_bytes = maxb * 12;
+      h->stats.resident = h->resident ? 1 : 0;
+    }
+    return SPGEMM_OK;
+  };
+  rc = body();
+  delete tsetup;
+  if (rc != SPGEMM_OK) return fail(rc);
+  h->state = 1;
+  *out = h;
+  return SPGEMM_OK;
+}
+
+int spgemm_create(spgemm_handle* h, int64_t m, int64_t k, int64_t n, const spgemm_csr* A, const spgemm_csr* B,
+                  void* stream) {
+  return spgemm_create_ex(h, m, k, n, A, B, stream, nullptr);
+}
+
+int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
+  g_last_error.clear();
+  if (!h || !c_row_ptr || !c_nnz) return SPGEMM_ERR_INVALID_ARG;
+  if (h->state != 1) {
+    set_last_error("symbolic must follow create, once");
+    return SPGEMM_ERR_BAD_STATE;
+  }
+  cudaMemsetAsync(c_row_ptr, 0, sizeof(int64_t) * (h->m + 1), h->st);
+  Sink sk{};
+  sk.row_nnz = c_row_ptr;
+  sk.row_begin = 0;
+  sk.row_end = h->m;
+  {
+    PhaseTimer t(h, 1);
+    light_pass(h, false, sk);
+  }
+  int64_t levels = 0, finals = 0, dense = 0;
+  for (auto& hb : h->batches) {
+    const bool vals = h->resident;
+    SG_TRY(ensure_chat(h, vals));
+    int64_t* crp;
+    SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
+    SG_TRY(heavy_expand(h, hb, vals, crp));
+    SG_TRY(heavy_levels(h, hb, vals, true, crp));
+    SG_TRY(heavy_chunk_symbolic(h, hb, c_row_ptr));
+    ws_free(h, crp);
+    levels = std::max<int64_t>(levels, static_cast<int64_t>(hb.lv.size()));
+    finals += hb.nfinal;
+    dense += hb.f_bin_start[2 * h->lad.n + 1] - hb.f_bin_start[2 * h->lad.n];
+  }
+  h->stats.levels_run = levels;
+  h->stats.final_chunks = finals;
+  h->stats.chunks_dense = dense;
+  {
+    PhaseTimer t(h, 9);
+    SG_TRY(scan(h, c_row_ptr, c_row_ptr, h->m));
+  }
+  int64_t nnz = 0;
+  SG_TRY(check_cuda(cudaMemcpyAsync(&nnz, c_row_ptr + h->m, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy nnz"));
+  SG_TRY(sync_and_check(h, "symbolic"));
+  *c_nnz = nnz;
+  h->stats.c_nnz = nnz;
+  h->stats.c_nnz_heavy = 0;
+  for (auto& hb : h->batches) h->stats.c_nnz_heavy += hb.nnz_c;
+  h->c_row_ptr = c_row_ptr;
+  h->state = 2;
+  return SPGEMM_OK;
+}
+
+int spgemm_numeric(spgemm_handle h, int32_t* c_col_idx, double* c_vals) {
+  g_last_error.clear();
+  if (!h) return SPGEMM_ERR_INVALID_ARG;
+  if (h->stats.c_nnz > 0 && (!c_col_idx || !c_vals)) return SPGEMM_ERR_INVALID_ARG;
+  return numeric_window(h, 0, h->m, c_col_idx, c_vals);
+}
+
+int spgemm_numeric_rows(spgemm_handle h, int64_t row_begin, int64_t row_end, int32_t* c_col_idx,
+                        double* c_vals) {
+  g_last_error.clear();
+  if (!h) return SPGEMM_ERR_INVALID_ARG;
+  if (row_begin < 0 || row_end > h->m || row_begin > row_end) {
+    set_last_error("row range outside [0, m]");
+    return SPGEMM_ERR_INVALID_ARG;
+  }
+  if (row_begin == row_end) return SPGEMM_OK;
+  if (!c_col_idx || !c_vals) return SPGEMM_ERR_INVALID_ARG;
+  return numeric_window(h, row_begin, row_end, c_col_idx, c_vals);
+}
+
+int spgemm_get_stats(spgemm_handle h, spgemm_stats* out) {
+  if (!h || !out) return SPGEMM_ERR_INVALID_ARG;
+  *out = h->stats;
+  return SPGEMM_OK;
+}
+
+int spgemm_get_plan(spgemm_handle h, spgemm_plan* out) {
+  if (!h || !out) return SPGEMM_ERR_INVALID_ARG;
+  *out = h->plan;
+  return SPGEMM_OK;
+}
+
+int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_t count) {
+  if (!h || !t || count < 0) return SPGEMM_ERR_INVALID_ARG;
+  drain_timers(h);
+  for (int i = 0; i < count && i < kPhaseSlots; ++i) {
+    t[i] = h->phase_ms[i];
+    if (launches) launches[i] = h->phase_n[i];
+  }
+  return SPGEMM_OK;
+}
+
+long long spgemm_kernel_launches(void) { return launch_count(); }
+
+int spgemm_destroy(spgemm_handle h) {
+  if (!h) return SPGEMM_OK;
+  drain_timers(h);
+  for (void* p : h->allocs) cudaFreeAsync(p, h->st);
+  h->allocs.clear();
+  cudaStreamSynchronize(h->st);
+  delete h;
+  return SPGEMM_OK;
+}
+
+const char* spgemm_strerror(int code) {
+  switch (code) {
+    case SPGEMM_OK: return "ok";
+    case SPGEMM_ERR_INVALID_ARG: return "invalid argument";
+    case SPGEMM_ERR_INVALID_CSR: return "malformed CSR input";
+    case SPGEMM_ERR_BAD_STATE: return "call out of order";
+    case SPGEMM_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case SPGEMM_ERR_OVERFLOW: return "size exceeds the index types";
+    case SPGEMM_ERR_DEVICE: return "device-side check failed";
+    case SPGEMM_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+const char* spgemm_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

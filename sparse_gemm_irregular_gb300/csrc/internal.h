@@ -1,0 +1,234 @@
+// Internal declarations of the SpGEMM library: handle, plan constants, kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/spgemm.h"
+#include "common.cuh"
+
+namespace sg {
+
+// ---- tile sizes shared by the planner and the kernels ---------------------------------
+constexpr int64_t kMsTile = 4096;          // elements per histogram / multisplit block
+constexpr int kMsThreads = 512;            // threads per multisplit block (8 elements each)
+constexpr int64_t kMsSmemBudget = 65536;   // bytes of shared memory per multisplit block (Eq. 6)
+constexpr int64_t kMsMaxBins = 2048;       // group_rows * chunks bins held by one block
+constexpr int64_t kOpTile = 2048;          // elements per outer-product block
+constexpr int kOpThreads = 256;
+constexpr int kSmemReserve = 7168;         // bytes kept back from s_LM for per-block staging
+constexpr int kMaxLadder = 16;             // light bin ladder levels
+constexpr int kScanTile = 4096;            // elements per scan block (512 threads x 8)
+constexpr int kPhaseSlots = 12;            // timed regions, see spgemm_get_phase_times
+
+// Light-row / chunk bin ladder derived from tau (hash tables at load factor 1/2).
+struct Ladder {
+  int n = 0;                       // levels
+  int64_t upper[kMaxLadder];       // level L takes IP (or chunk size) in (upper[L-1], upper[L]]
+  int64_t slots[kMaxLadder];       // hash slots = 2 * upper (shortened dense: span <= slots)
+  int tpr[kMaxLadder];             // threads per row: 32 = one warp per row, else one block
+};
+
+// Parameters of the row classifier, passed by value to kernels.
+struct BinRule {
+  int n;                 // ladder levels
+  int64_t upper[kMaxLadder];
+  int64_t slots[kMaxLadder];
+  int64_t tau;
+  int all_heavy, all_light, no_dense;
+};
+
+// Bin numbering: level L hash = 2L, level L dense = 2L+1, heavy = 2n, empty = 255.
+constexpr uint8_t kBinEmpty = 255;
+
+// ---- launch accounting --------------------------------------------------------------------
+void note_launch();        // every kernel launch of the library calls this once
+long long launch_count();
+
+// ---- host planner ----------------------------------------------------------------------
+int plan_params(int64_t c_cols, int64_t s_lm, const spgemm_options* ov, spgemm_plan* out);
+Ladder make_ladder(int64_t tau);
+
+// ---- scans (k_scan.cu) ------------------------------------------------------------------
+// out[i] = sum_{j<i} in[j] for i in [0, n]; out has n+1 entries; in may equal out.
+// `scratch` holds scan_scratch_elems(n) int64.
+int64_t scan_scratch_elems(int64_t n);
+void scan_excl_i64(const int64_t* in, int64_t* out, int64_t n, int64_t* scratch, cudaStream_t s);
+
+// ---- setup kernels (k_setup.cu) --------------------------------------------------------
+void launch_brow_minmax(const spgemm_csr& B, int32_t* bmin, int32_t* bmax, cudaStream_t s);
+void launch_row_ip(const spgemm_csr& A, const spgemm_csr& B, const int32_t* bmin,
+                   const int32_t* bmax, const BinRule& rule, int64_t* ip, int32_t* span_lo,
+                   uint8_t* bin, cudaStream_t s);
+// Stable multisplit of items [0, n) by bin id (bins [0, nbins); kBinEmpty skipped).
+// cnt: nbins * ceil(n / 1024) + 1 int64 (scanned in place into offsets).
+int64_t bin_blocks(int64_t n);
+void launch_bin_count(const uint8_t* bin, int64_t n, int nbins, int64_t* cnt, cudaStream_t s);
+void launch_bin_scatter(const uint8_t* bin, int64_t n, int nbins, const int64_t* off,
+                        int32_t* out, cudaStream_t s);
+void launch_bin_starts(const int64_t* off, int64_t nblk, int nbins, int64_t* starts, cudaStream_t s);
+void launch_validate(const spgemm_csr& M, uint32_t* err, cudaStream_t s);
+
+// ---- light rows and chunk accumulators (k_accum.cu) ------------------------------------
+// Source of one accumulation: a light row of A*B, or a final chunk of C^_reord.
+struct RowJob {
+  const int32_t* rows;   // bin list (global row ids)
+  int64_t count;
+  int64_t slots;         // hash slots (or maximal dense span)
+  int tpr;               // threads per row (32 or block size)
+  bool dense;
+};
+struct ChunkSet {        // final chunks of one heavy batch
+  const int64_t* start;  // element offset in the C^ buffers
+  const int64_t* cnt;    // elements
+  const int32_t* row;    // batch-local heavy row
+  const int32_t* base;   // first column covered
+  int64_t* nnz;          // out (symbolic)
+  const int64_t* out;    // in (numeric): offset of the chunk inside its C row
+  const int32_t* heavy_rows;  // batch-local row -> global row
+  const int32_t* col;    // C^ buffers (both halves)
+  const double* val;
+};
+struct Sink {            // where results go
+  int64_t* row_nnz;      // symbolic: count per global row (C.row_ptr before the scan)
+  const int64_t* row_ptr;// numeric: C.row_ptr
+  int32_t* c_col;
+  double* c_val;
+  int64_t row_begin, row_end;  // numeric row window; output index 0 = row_ptr[row_begin]
+};
+void launch_light(const spgemm_csr& A, const spgemm_csr& B, const int32_t* span_lo,
+                  const RowJob& job, bool numeric, const Sink& sink, uint32_t* err,
+                  cudaStream_t s);
+void launch_chunks(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t slots, int tpr,
+                   bool dense, int64_t dense_width, bool numeric, const Sink& sink,
+                   uint32_t* err, cudaStream_t s);
+size_t light_smem_bytes(int64_t slots, int tpr, bool dense, bool numeric);
+
+// ---- heavy pipeline (k_heavy.cu) ---------------------------------------------------------
+void launch_gather_ip(const int32_t* heavy_rows, int64_t nrows, const int64_t* ip, int64_t* out,
+                      cudaStream_t s);
+void launch_csc_count(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows,
+                      int32_t* colcnt, cudaStream_t s);
+void launch_slice_sizes(const int32_t* colcnt, const spgemm_csr& B, int64_t kcols,
+                        int64_t* colptr_sizes, int64_t* slice_sizes, cudaStream_t s);
+void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows,
+                        int64_t* cursor, int32_t* csc_row, double* csc_val, cudaStream_t s);
+void launch_copy_i64(const int64_t* src, int64_t* dst, int64_t n, cudaStream_t s);
+void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
+                          const int64_t* slice_off, int64_t kcols, int64_t total,
+                          const spgemm_csr& B, int64_t* row_cursor, int32_t* chat_col,
+                          double* chat_val, bool with_vals, uint32_t* err, cudaStream_t s);
+void launch_histogram(const int64_t* row_ptr, int64_t nrows, int64_t total, const int32_t* col,
+                      int shift, int64_t nchunks, int64_t group_rows,
+                      unsigned long long* counts, uint32_t* err, cudaStream_t s);
+void launch_chunk_partition(const unsigned long long* counts, int64_t n, int64_t tau,
+                            uint8_t* bin, cudaStream_t s);
+void launch_reord_meta(const unsigned long long* counts, int64_t nrows_in, int64_t nchunks,
+                       const int32_t* xmap, const int32_t* in_row, const int32_t* in_base,
+                       int64_t width, int64_t* reord_cnt, int32_t* out_row, int32_t* out_base,
+                       cudaStream_t s);
+void launch_multisplit(const int64_t* row_ptr, int64_t nrows, int64_t total,
+                       const int32_t* in_col, const double* in_val, int shift, int64_t nchunks,
+                       int64_t group_rows, const int32_t* xmap, unsigned long long* reord_cursor,
+                       int32_t* out_col, double* out_val, bool with_vals, uint32_t* err,
+                       cudaStream_t s);
+void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t elem_base,
+                       const int32_t* row, const int32_t* base, int64_t* f_start, int64_t* f_cnt,
+                       int32_t* f_row, int32_t* f_base, cudaStream_t s);
+void launch_chunk_classify(const int64_t* f_cnt, int64_t n, const BinRule& rule, uint8_t* bin,
+                           cudaStream_t s);
+void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s);
+void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s);
+void launch_grid_fill(const int32_t* f_row, const int32_t* f_base, const int64_t* f_nnz, int64_t n,
+                      int shift_fin, int64_t nfin, int64_t* grid, cudaStream_t s);
+void launch_grid_finish(const int64_t* grid_scanned, const int32_t* f_row, const int32_t* f_base,
+                        int64_t n, int shift_fin, int64_t nfin, int64_t* f_out, cudaStream_t s);
+void launch_row_totals(const int64_t* grid_scanned, int64_t nrows, int64_t nfin,
+                       const int32_t* heavy_rows, int64_t* row_nnz, cudaStream_t s);
+
+}  // namespace sg
+
+// ---- the handle ---------------------------------------------------------------------------
+struct LevelInfo {
+  int64_t nin = 0;       // input rows of the level
+  int64_t v = 0;         // chunks per input row
+  int64_t width = 0;     // columns per output chunk
+  int64_t nheavy = 0;    // output chunks passed to the next level (heavy ones, stored first)
+  int64_t desc0 = 0;     // first final-chunk descriptor written by this level
+  int64_t elem_base = 0; // offset of the level's output half in the C^ buffer
+  int64_t next_elems = 0;// elements of the heavy chunks (the next level's input)
+};
+
+struct HeavyBatch {
+  int64_t h0 = 0, h1 = 0;       // range of the heavy-row list
+  int64_t row_lo = 0, row_hi = 0;  // smallest and largest global row of the batch
+  int64_t elems = 0;            // intermediate products of the batch
+  std::vector<LevelInfo> lv;    // recorded by the symbolic phase, replayed by the numeric one
+  int64_t nfinal = 0;           // final chunks (C^_reord rows that are accumulated)
+  int64_t* f_start = nullptr;
+  int64_t* f_cnt = nullptr;
+  int32_t* f_row = nullptr;
+  int32_t* f_base = nullptr;
+  int64_t* f_nnz = nullptr;
+  int64_t* f_out = nullptr;
+  int32_t* f_list = nullptr;    // chunk ids ordered by accumulator bin
+  std::vector<int64_t> f_bin_start;  // host, per chunk bin (size nbins + 1)
+  int64_t nnz_c = 0;            // entries of C in the batch's rows (read after the symbolic sync)
+};
+
+struct spgemm_ctx {
+  int64_t m = 0, k = 0, n = 0;
+  spgemm_csr A{}, B{};
+  cudaStream_t st = nullptr;
+  int device = 0, sms = 0;
+  int64_t smem_optin = 0, l2_bytes = 0;
+  spgemm_options opt{};
+  spgemm_plan plan{};
+  sg::Ladder lad;
+  sg::BinRule rule{};
+  int nbins = 0;                // 2 * ladder levels + 1 (heavy)
+  spgemm_stats stats{};
+  int state = 0;                // 1 after create, 2 after symbolic
+  int64_t* c_row_ptr = nullptr; // remembered from symbolic
+
+  // workspace (device)
+  std::vector<void*> allocs;
+  uint32_t* d_err = nullptr;
+  int64_t* d_scan = nullptr;    // scan scratch
+  int64_t scan_cap = 0;
+  int64_t* d_ip = nullptr;
+  int32_t* d_span_lo = nullptr;
+  uint8_t* d_bin = nullptr;
+  int32_t* d_rows = nullptr;    // concatenated stable bin lists
+  int64_t* d_binoff = nullptr;
+  std::vector<int64_t> bin_start;  // host copy (nbins + 1)
+
+  // heavy rows
+  int64_t nheavy = 0;
+  const int32_t* d_heavy = nullptr;   // into d_rows
+  int64_t* d_heavy_pre = nullptr;     // exclusive prefix of heavy IP (nheavy + 1)
+  std::vector<int64_t> heavy_pre;     // host copy
+  std::vector<HeavyBatch> batches;
+  int64_t batch_cap = 0;              // elements per C^ buffer
+  int32_t* d_chat_col = nullptr;      // 2 * batch_cap (ping-pong halves)
+  double* d_chat_val = nullptr;
+  bool resident = false;
+  bool chat_has_vals = false;
+
+  // phase timing (slots: see spgemm_get_phase_times)
+  bool timing = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[sg::kPhaseSlots];
+  double phase_ms[sg::kPhaseSlots] = {0};
+  int64_t phase_n[sg::kPhaseSlots] = {0};
+};
+
+namespace sg {
+// api.cu helpers used by the heavy orchestration
+void* ws_alloc(spgemm_ctx* h, size_t bytes);
+void ws_free(spgemm_ctx* h, void* p);
+int check_cuda(cudaError_t e, const char* what);
+void set_last_error(const std::string& s);
+}  // namespace sg

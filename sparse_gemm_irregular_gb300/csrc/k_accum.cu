@@ -1,0 +1,469 @@
+// Shared-memory accumulators (gMAGNUS page, sections II-B and III-E):
+//   * light rows of C: Gustavson expansion of row i (every A[i,k] scales row k of B), summed
+//     in a hash map (modulo hashing, linear probing, load factor 1/2) or, when the row's
+//     column span is narrow, in a shortened dense array over that span;
+//   * final chunks of C^_reord: a flat list of (local column, value) pairs, summed in a hash
+//     map (light chunks) or in a dense array of the chunk width plus a bitmap (heavy chunks).
+// Symbolic phase: count the distinct columns.  Numeric phase: accumulate, then produce the
+// row (or chunk) sorted by column -- a bitonic sort of the compacted hash entries, or a scan
+// over the dense bitmap -- and write it at its final CSR position.
+//
+// One group of threads owns one row or chunk: a warp (several per block) for small bins, a
+// whole block for large ones (bin ladder after the Ocean page, section 4: each larger kernel
+// doubles the threads and the accumulator).
+#include "internal.h"
+
+namespace sg {
+
+constexpr int kWarpGroupsPerBlock = 8;
+constexpr int kMaxBatch = 256;  // A entries staged per expansion step
+
+struct AccParams {
+  // row source
+  const int64_t* arp;
+  const int32_t* acol;
+  const double* aval;
+  const int64_t* brp;
+  const int32_t* bcol;
+  const double* bval;
+  const int32_t* span_lo;
+  // chunk source
+  ChunkSet cs;
+  // common
+  const int32_t* list;
+  int64_t count;
+  int64_t slots;       // hash slots, or dense width
+  Sink sink;
+  uint32_t* err;
+  int has_vals;        // chunk source carries values
+};
+
+template <bool WARP>
+struct Group {
+  int lane, size;
+  __device__ __forceinline__ void sync() const {
+    if (WARP) __syncwarp(); else __syncthreads();
+  }
+};
+
+// Inclusive scan over the group; `tmp` is 33 int64 of shared memory (block groups only).
+template <bool WARP>
+__device__ __forceinline__ int64_t group_scan(const Group<WARP>& g, int64_t v, int64_t* tmp,
+                                              int64_t* total) {
+  if (WARP) {
+    int64_t x = warp_incl_scan(v);
+    *total = __shfl_sync(0xffffffffu, x, 31);
+    return x;
+  } else {
+    return block_incl_scan(v, tmp, total);
+  }
+}
+
+// Shared-memory layout of one group.
+struct Smem {
+  double* av;        // [batch] A values of the staged entries
+  int64_t* bstart;   // [batch] first B index of the staged entries
+  int64_t* incl;     // [batch] inclusive prefix of their B row lengths
+  int64_t* tmp;      // [33] scan scratch
+  double* vals;      // [slots] (numeric)
+  int32_t* keys;     // [slots] hash keys, or dense bitmap words
+};
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+__host__ __device__ inline int batch_of(int size) { return size < kMaxBatch ? size : kMaxBatch; }
+
+__host__ __device__ inline size_t group_bytes(int64_t slots, int size, bool dense, bool numeric,
+                                              bool rows) {
+  size_t b = align16(33 * sizeof(int64_t));
+  if (rows) b += align16(batch_of(size) * (sizeof(double) + 2 * sizeof(int64_t)));
+  if (numeric) b += align16(static_cast<size_t>(slots) * sizeof(double));
+  b += dense ? align16(((slots + 31) / 32) * sizeof(int32_t))
+             : align16(static_cast<size_t>(slots) * sizeof(int32_t));
+  return b;
+}
+
+__device__ __forceinline__ Smem carve(char* p, int64_t slots, int size, bool dense, bool numeric,
+                                      bool rows) {
+  Smem s;
+  s.tmp = reinterpret_cast<int64_t*>(p);
+  p += align16(33 * sizeof(int64_t));
+  if (rows) {
+    const int nb = batch_of(size);
+    s.av = reinterpret_cast<double*>(p);
+    s.bstart = reinterpret_cast<int64_t*>(p + nb * sizeof(double));
+    s.incl = reinterpret_cast<int64_t*>(p + nb * (sizeof(double) + sizeof(int64_t)));
+    p += align16(nb * (sizeof(double) + 2 * sizeof(int64_t)));
+  } else {
+    s.av = nullptr;
+    s.bstart = nullptr;
+    s.incl = nullptr;
+  }
+  if (numeric) {
+    s.vals = reinterpret_cast<double*>(p);
+    p += align16(static_cast<size_t>(slots) * sizeof(double));
+  } else {
+    s.vals = nullptr;
+  }
+  s.keys = reinterpret_cast<int32_t*>(p);
+  return s;
+}
+
+// ---- accumulators ------------------------------------------------------------------------
+template <bool NUMERIC>
+__device__ __forceinline__ bool hash_insert(const Smem& s, uint32_t slots, int32_t col, double v,
+                                            uint32_t* err) {
+  uint32_t slot = hash_slot(col, slots);
+  for (uint32_t probe = 0; probe < slots; ++probe) {
+    int32_t k = *reinterpret_cast<volatile int32_t*>(&s.keys[slot]);
+    if (k == col) {
+      if (NUMERIC) atomicAdd(&s.vals[slot], v);
+      return false;
+    }
+    if (k == kEmptyKey) {
+      const int32_t old = atomicCAS(&s.keys[slot], kEmptyKey, col);
+      if (old == kEmptyKey || old == col) {
+        if (NUMERIC) atomicAdd(&s.vals[slot], v);
+        return old == kEmptyKey;
+      }
+    }
+    slot = (slot + 1 == slots) ? 0 : slot + 1;
+  }
+  set_error(err, kErrHashFull);
+  return false;
+}
+
+template <bool NUMERIC>
+__device__ __forceinline__ bool dense_insert(const Smem& s, uint32_t width, int32_t idx, double v,
+                                             uint32_t* err) {
+  if (static_cast<uint32_t>(idx) >= width) {
+    set_error(err, kErrBounds);
+    return false;
+  }
+  const uint32_t bit = 1u << (idx & 31);
+  const uint32_t old = atomicOr(reinterpret_cast<uint32_t*>(&s.keys[idx >> 5]), bit);
+  if (NUMERIC) atomicAdd(&s.vals[idx], v);
+  return (old & bit) == 0;
+}
+
+template <bool WARP, bool NUMERIC, bool DENSE>
+__device__ __forceinline__ void acc_clear(const Group<WARP>& g, const Smem& s, int64_t slots) {
+  if (DENSE) {
+    const int64_t words = (slots + 31) / 32;
+    for (int64_t w = g.lane; w < words; w += g.size) s.keys[w] = 0;
+    if (NUMERIC)
+      for (int64_t j = g.lane; j < slots; j += g.size) s.vals[j] = 0.0;
+  } else {
+    for (int64_t j = g.lane; j < slots; j += g.size) s.keys[j] = kEmptyKey;
+    if (NUMERIC)
+      for (int64_t j = g.lane; j < slots; j += g.size) s.vals[j] = 0.0;
+  }
+}
+
+// ---- sources -----------------------------------------------------------------------------
+// Expand row `row` of A*B into the accumulator; returns this thread's count of new columns.
+template <bool WARP, bool NUMERIC, bool DENSE>
+__device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& s,
+                                              const AccParams& p, int64_t row, int32_t base,
+                                              uint32_t slots) {
+  int64_t fresh = 0;
+  const int64_t a0 = p.arp[row], a1 = p.arp[row + 1];
+  const int nb = batch_of(g.size);
+  for (int64_t eb = a0; eb < a1; eb += nb) {
+    const int nent = static_cast<int>(min(static_cast<int64_t>(nb), a1 - eb));
+    int64_t len = 0;
+    if (g.lane < nent) {
+      const int64_t e = eb + g.lane;
+      const int32_t k = p.acol[e];
+      const int64_t b0 = p.brp[k];
+      len = p.brp[k + 1] - b0;
+      s.av[g.lane] = NUMERIC ? p.aval[e] : 0.0;
+      s.bstart[g.lane] = b0;
+    }
+    int64_t total;
+    const int64_t incl = group_scan<WARP>(g, g.lane < nb ? len : 0, s.tmp, &total);
+    if (g.lane < nent) s.incl[g.lane] = incl;
+    g.sync();
+    int j = 0;
+    for (int64_t f = g.lane; f < total; f += g.size) {
+      // staged entry j holds flattened positions [incl[j-1], incl[j])
+      if (s.incl[j] <= f) {
+        int lo = j, hi = nent - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s.incl[mid] <= f) lo = mid + 1; else hi = mid;
+        }
+        j = lo;
+      }
+      const int64_t before = j > 0 ? s.incl[j - 1] : 0;
+      const int64_t q = s.bstart[j] + (f - before);
+      const int32_t col = p.bcol[q];
+      const double v = NUMERIC ? s.av[j] * p.bval[q] : 0.0;
+      if (DENSE) fresh += dense_insert<NUMERIC>(s, slots, col - base, v, p.err);
+      else fresh += hash_insert<NUMERIC>(s, slots, col, v, p.err);
+    }
+    g.sync();
+  }
+  return fresh;
+}
+
+template <bool WARP, bool NUMERIC, bool DENSE>
+__device__ __forceinline__ int64_t expand_chunk(const Group<WARP>& g, const Smem& s,
+                                                const AccParams& p, int64_t start, int64_t cnt,
+                                                uint32_t slots) {
+  int64_t fresh = 0;
+  const int32_t* col = p.cs.col + start;
+  const double* val = p.cs.val + start;
+  for (int64_t f = g.lane; f < cnt; f += g.size) {
+    const int32_t c = col[f];
+    const double v = (NUMERIC && p.has_vals) ? val[f] : 0.0;
+    if (DENSE) fresh += dense_insert<NUMERIC>(s, slots, c, v, p.err);
+    else fresh += hash_insert<NUMERIC>(s, slots, c, v, p.err);
+  }
+  return fresh;
+}
+
+// ---- outputs -----------------------------------------------------------------------------
+// Sorted write of a hash table holding `n` entries: compact in place (rounds over the
+// slots; every entry moves to a lower or equal slot), bitonic sort of the first 2^ceil(log2 n)
+// slots, then a coalesced write.
+template <bool WARP>
+__device__ void hash_emit(const Group<WARP>& g, const Smem& s, int64_t slots, int64_t n,
+                          int64_t expected, int32_t col_base, int32_t* c_col, double* c_val,
+                          uint32_t* err) {
+  int64_t written = 0;
+  for (int64_t r0 = 0; r0 < slots; r0 += g.size) {
+    const int64_t slot = r0 + g.lane;
+    int32_t k = kEmptyKey;
+    double v = 0.0;
+    if (slot < slots) {
+      k = s.keys[slot];
+      v = s.vals[slot];
+    }
+    const int64_t occ = (k != kEmptyKey) ? 1 : 0;
+    int64_t total;
+    const int64_t incl = group_scan<WARP>(g, occ, s.tmp, &total);
+    g.sync();
+    if (occ) {
+      const int64_t pos = written + incl - 1;
+      s.keys[pos] = k;
+      s.vals[pos] = v;
+    }
+    written += total;
+    g.sync();
+  }
+  int64_t P = 1;
+  while (P < n) P <<= 1;
+  if (P > slots) {  // only after a probe failure (table overfilled): give up on this row
+    if (g.lane == 0) set_error(err, kErrHashFull);
+    return;
+  }
+  for (int64_t j = n + g.lane; j < P; j += g.size) s.keys[j] = kPadKey;
+  g.sync();
+  for (int64_t kk = 2; kk <= P; kk <<= 1) {
+    for (int64_t jj = kk >> 1; jj > 0; jj >>= 1) {
+      for (int64_t i = g.lane; i < P; i += g.size) {
+        const int64_t ixj = i ^ jj;
+        if (ixj > i) {
+          const int32_t ki = s.keys[i], kx = s.keys[ixj];
+          const bool up = (i & kk) == 0;
+          if ((ki > kx) == up) {
+            s.keys[i] = kx;
+            s.keys[ixj] = ki;
+            const double t = s.vals[i];
+            s.vals[i] = s.vals[ixj];
+            s.vals[ixj] = t;
+          }
+        }
+      }
+      g.sync();
+    }
+  }
+  if (n != expected && g.lane == 0) set_error(err, kErrRowOverflow);
+  const int64_t m = n < expected ? n : expected;
+  for (int64_t i = g.lane; i < m; i += g.size) {
+    c_col[i] = s.keys[i] + col_base;
+    c_val[i] = s.vals[i];
+  }
+}
+
+// Ordered write of a dense accumulator: scan over the bitmap words.
+template <bool WARP>
+__device__ void dense_emit(const Group<WARP>& g, const Smem& s, int64_t width, int64_t expected,
+                           int32_t col_base, int32_t* c_col, double* c_val, uint32_t* err) {
+  const int64_t words = (width + 31) / 32;
+  int64_t written = 0;
+  for (int64_t w0 = 0; w0 < words; w0 += g.size) {
+    const int64_t w = w0 + g.lane;
+    const uint32_t bits = w < words ? static_cast<uint32_t>(s.keys[w]) : 0u;
+    const int64_t c = __popc(bits);
+    int64_t total;
+    const int64_t incl = group_scan<WARP>(g, c, s.tmp, &total);
+    int64_t pos = written + incl - c;
+    uint32_t b = bits;
+    while (b) {
+      const int bit = __ffs(b) - 1;
+      b &= b - 1;
+      const int64_t idx = w * 32 + bit;
+      if (pos < expected) {
+        c_col[pos] = static_cast<int32_t>(idx) + col_base;
+        c_val[pos] = s.vals[idx];
+      }
+      ++pos;
+    }
+    written += total;
+  }
+  if (written != expected && g.lane == 0) set_error(err, kErrRowOverflow);
+}
+
+// ---- the kernel --------------------------------------------------------------------------
+template <bool WARP, bool NUMERIC, bool DENSE, bool CHUNK>
+__global__ void k_accum(AccParams p) {
+  extern __shared__ __align__(16) char smem_raw[];
+  Group<WARP> g;
+  int64_t item;
+  char* region = smem_raw;
+  const size_t gb = group_bytes(p.slots, WARP ? 32 : blockDim.x, DENSE, NUMERIC, !CHUNK);
+  if (WARP) {
+    const int w = threadIdx.x >> 5;
+    g.lane = threadIdx.x & 31;
+    g.size = 32;
+    item = static_cast<int64_t>(blockIdx.x) * kWarpGroupsPerBlock + w;
+    region += gb * w;
+  } else {
+    g.lane = threadIdx.x;
+    g.size = blockDim.x;
+    item = blockIdx.x;
+  }
+  if (item >= p.count) return;  // uniform per group
+  const Smem s = carve(region, p.slots, g.size, DENSE, NUMERIC, !CHUNK);
+  const uint32_t slots = static_cast<uint32_t>(p.slots);
+
+  // identify the work item and its output
+  int64_t grow;             // global row of C
+  int32_t col_base = 0;     // column added on output
+  int32_t acc_base = 0;     // dense accumulator origin (light dense rows)
+  int64_t q = 0, cstart = 0, ccnt = 0;
+  if (CHUNK) {
+    q = p.list[item];
+    cstart = p.cs.start[q];
+    ccnt = p.cs.cnt[q];
+    grow = p.cs.heavy_rows[p.cs.row[q]];
+    col_base = p.cs.base[q];
+  } else {
+    grow = p.list[item];
+    if (DENSE) acc_base = p.span_lo[grow];
+  }
+  if (NUMERIC && (grow < p.sink.row_begin || grow >= p.sink.row_end)) return;
+
+  acc_clear<WARP, NUMERIC, DENSE>(g, s, p.slots);
+  g.sync();
+  int64_t fresh;
+  if (CHUNK) fresh = expand_chunk<WARP, NUMERIC, DENSE>(g, s, p, cstart, ccnt, slots);
+  else fresh = expand_row<WARP, NUMERIC, DENSE>(g, s, p, grow, acc_base, slots);
+  g.sync();
+  int64_t n;
+  group_scan<WARP>(g, fresh, s.tmp, &n);
+  if (!NUMERIC) {
+    if (g.lane == 0) {
+      if (CHUNK) p.cs.nnz[q] = n;
+      else p.sink.row_nnz[grow] = n;
+    }
+    return;
+  }
+  const int64_t rp0 = p.sink.row_ptr[grow];
+  const int64_t win = p.sink.row_ptr[p.sink.row_begin];
+  int64_t out, expected;
+  if (CHUNK) {
+    out = rp0 + p.cs.out[q] - win;
+    expected = p.cs.nnz[q];  // counted by the symbolic phase
+  } else {
+    out = rp0 - win;
+    expected = p.sink.row_ptr[grow + 1] - rp0;
+  }
+  g.sync();
+  if (DENSE) {
+    const int32_t base = CHUNK ? col_base : acc_base;
+    dense_emit<WARP>(g, s, p.slots, expected, base, p.sink.c_col + out, p.sink.c_val + out, p.err);
+  } else {
+    hash_emit<WARP>(g, s, p.slots, n, expected, col_base, p.sink.c_col + out, p.sink.c_val + out,
+                    p.err);
+  }
+}
+
+size_t light_smem_bytes(int64_t slots, int tpr, bool dense, bool numeric) {
+  const size_t gb = group_bytes(slots, tpr, dense, numeric, true);
+  return tpr == 32 ? gb * kWarpGroupsPerBlock : gb;
+}
+
+template <bool WARP, bool NUMERIC, bool DENSE, bool CHUNK>
+static void launch_one(const AccParams& p, int tpr, cudaStream_t s) {
+  const size_t gb = group_bytes(p.slots, WARP ? 32 : tpr, DENSE, NUMERIC, !CHUNK);
+  const size_t smem = WARP ? gb * kWarpGroupsPerBlock : gb;
+  auto kern = k_accum<WARP, NUMERIC, DENSE, CHUNK>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const int64_t blocks = WARP ? ceil_div(p.count, kWarpGroupsPerBlock) : p.count;
+  const int threads = WARP ? 32 * kWarpGroupsPerBlock : tpr;
+  note_launch();
+  kern<<<static_cast<unsigned>(blocks), threads, smem, s>>>(p);
+}
+
+template <bool CHUNK>
+static void dispatch(const AccParams& p, int tpr, bool dense, bool numeric, cudaStream_t s) {
+  const bool warp = tpr == 32;
+  if (warp) {
+    if (numeric) {
+      if (dense) launch_one<true, true, true, CHUNK>(p, tpr, s);
+      else launch_one<true, true, false, CHUNK>(p, tpr, s);
+    } else {
+      if (dense) launch_one<true, false, true, CHUNK>(p, tpr, s);
+      else launch_one<true, false, false, CHUNK>(p, tpr, s);
+    }
+  } else {
+    if (numeric) {
+      if (dense) launch_one<false, true, true, CHUNK>(p, tpr, s);
+      else launch_one<false, true, false, CHUNK>(p, tpr, s);
+    } else {
+      if (dense) launch_one<false, false, true, CHUNK>(p, tpr, s);
+      else launch_one<false, false, false, CHUNK>(p, tpr, s);
+    }
+  }
+}
+
+void launch_light(const spgemm_csr& A, const spgemm_csr& B, const int32_t* span_lo,
+                  const RowJob& job, bool numeric, const Sink& sink, uint32_t* err,
+                  cudaStream_t s) {
+  if (job.count == 0) return;
+  AccParams p{};
+  p.arp = A.row_ptr;
+  p.acol = A.col_idx;
+  p.aval = A.vals;
+  p.brp = B.row_ptr;
+  p.bcol = B.col_idx;
+  p.bval = B.vals;
+  p.span_lo = span_lo;
+  p.list = job.rows;
+  p.count = job.count;
+  p.slots = job.slots;
+  p.sink = sink;
+  p.err = err;
+  p.has_vals = 1;
+  dispatch<false>(p, job.tpr, job.dense, numeric, s);
+}
+
+void launch_chunks(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t slots, int tpr,
+                   bool dense, int64_t dense_width, bool numeric, const Sink& sink,
+                   uint32_t* err, cudaStream_t s) {
+  if (count == 0) return;
+  AccParams p{};
+  p.cs = cs;
+  p.list = list;
+  p.count = count;
+  p.slots = dense ? dense_width : slots;
+  p.sink = sink;
+  p.err = err;
+  p.has_vals = cs.val != nullptr;
+  dispatch<true>(p, tpr, dense, numeric, s);
+}
+
+}  // namespace sg

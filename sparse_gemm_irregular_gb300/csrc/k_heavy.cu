@@ -1,0 +1,554 @@
+// Heavy rows (gMAGNUS page, sections III-A to III-C, Algorithms 3-5):
+//   MaskedCsr2Csc   -> csc_count / csc_scatter: A[x_heavy,:] transposed by a counting sort.
+//   sliceOffsets    -> slice_sizes + scan: |column k of A~_CSC| * |row k of B|.
+//   OuterProduct    -> outer_product: flattened static partition of all slice elements,
+//                      one atomic reservation per (A~ entry, block) on the C^ row cursor,
+//                      coalesced copy of (partial) B rows scaled by the A value.
+//   Histogram       -> histogram: per (C^ row, chunk) counts, warp-aggregated with
+//                      __match_any_sync into a block histogram, one global atomic per bin.
+//   ThreshPartition -> chunk_partition + the stable bin scatter: heavy chunks first.
+//   Multisplit      -> multisplit: block histogram, global reservation per bin, block scan,
+//                      permute in shared memory, coalesced write with the column shifted into
+//                      the chunk's local range.
+// plus the bookkeeping that turns the final chunks into offsets inside the rows of C.
+#include "internal.h"
+
+namespace sg {
+
+// ---- small helpers --------------------------------------------------------------------------
+__global__ void k_gather_ip(const int32_t* __restrict__ rows, int64_t n, const int64_t* __restrict__ ip,
+                            int64_t* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = ip[rows[i]];
+}
+void launch_gather_ip(const int32_t* heavy_rows, int64_t nrows, const int64_t* ip, int64_t* out,
+                      cudaStream_t s) {
+  if (nrows == 0) return;
+  note_launch();
+  k_gather_ip<<<static_cast<unsigned>(ceil_div(nrows, 256)), 256, 0, s>>>(heavy_rows, nrows, ip, out);
+}
+
+__global__ void k_copy_i64(const int64_t* __restrict__ a, int64_t* __restrict__ b, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) b[i] = a[i];
+}
+void launch_copy_i64(const int64_t* src, int64_t* dst, int64_t n, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_copy_i64<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(src, dst, n);
+}
+
+__global__ void k_offset_copy(const int64_t* __restrict__ a, int64_t n, int64_t delta, int64_t* __restrict__ b) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) b[i] = a[i] - delta;
+}
+void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_offset_copy<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(src, n, delta, dst);
+}
+
+// ---- masked CSR -> CSC of the heavy rows of A ------------------------------------------------
+__global__ void k_csc_count(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
+                            const int32_t* __restrict__ rows, int64_t nrows, int32_t* __restrict__ cnt) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (w >= nrows) return;
+  const int64_t r = rows[w];
+  for (int64_t e = arp[r] + lane_id(); e < arp[r + 1]; e += 32) atomicAdd(&cnt[acol[e]], 1);
+}
+void launch_csc_count(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows, int32_t* colcnt,
+                      cudaStream_t s) {
+  if (nrows == 0) return;
+  note_launch();
+  k_csc_count<<<static_cast<unsigned>(ceil_div(nrows * 32, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx,
+                                                                               heavy_rows, nrows, colcnt);
+}
+
+__global__ void k_slice_sizes(const int32_t* __restrict__ cnt, const int64_t* __restrict__ brp,
+                              int64_t kcols, int64_t* __restrict__ colsz, int64_t* __restrict__ slsz) {
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k < kcols) {
+    const int64_t c = cnt[k];
+    colsz[k] = c;
+    slsz[k] = c * (brp[k + 1] - brp[k]);
+  }
+}
+void launch_slice_sizes(const int32_t* colcnt, const spgemm_csr& B, int64_t kcols, int64_t* colptr_sizes,
+                        int64_t* slice_sizes, cudaStream_t s) {
+  if (kcols == 0) return;
+  note_launch();
+  k_slice_sizes<<<static_cast<unsigned>(ceil_div(kcols, 256)), 256, 0, s>>>(colcnt, B.row_ptr, kcols,
+                                                                            colptr_sizes, slice_sizes);
+}
+
+__global__ void k_csc_scatter(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
+                              const double* __restrict__ aval, const int32_t* __restrict__ rows,
+                              int64_t nrows, unsigned long long* __restrict__ cursor,
+                              int32_t* __restrict__ crow, double* __restrict__ cval) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (w >= nrows) return;
+  const int64_t r = rows[w];
+  for (int64_t e = arp[r] + lane_id(); e < arp[r + 1]; e += 32) {
+    const unsigned long long pos = atomicAdd(&cursor[acol[e]], 1ull);
+    crow[pos] = static_cast<int32_t>(w);  // batch-local heavy row (x_map)
+    cval[pos] = aval[e];
+  }
+}
+void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows, int64_t* cursor,
+                        int32_t* csc_row, double* csc_val, cudaStream_t s) {
+  if (nrows == 0) return;
+  note_launch();
+  k_csc_scatter<<<static_cast<unsigned>(ceil_div(nrows * 32, 256)), 256, 0, s>>>(
+      A.row_ptr, A.col_idx, A.vals, heavy_rows, nrows, reinterpret_cast<unsigned long long*>(cursor),
+      csc_row, csc_val);
+}
+
+// ---- outer product (Algorithm 4) ---------------------------------------------------------------
+struct OpSmem {
+  int64_t s0, s1, a_first, nent;
+};
+
+template <bool VALS>
+__global__ void __launch_bounds__(kOpThreads) k_outer_product(
+    const int64_t* __restrict__ colptr, const int32_t* __restrict__ crow, const double* __restrict__ cval,
+    const int64_t* __restrict__ slice_off, int64_t kcols, int64_t total, const int64_t* __restrict__ brp,
+    const int32_t* __restrict__ bcol, const double* __restrict__ bval, unsigned long long* __restrict__ cursor,
+    int32_t* __restrict__ out_col, double* __restrict__ out_val, uint32_t* err) {
+  extern __shared__ __align__(16) char smem_raw[];
+  __shared__ OpSmem hdr;
+  int64_t* dst_delta = reinterpret_cast<int64_t*>(smem_raw);
+  int64_t* src_delta = dst_delta + kOpTile;
+  double* a_val = reinterpret_cast<double*>(src_delta + kOpTile);
+  int32_t* seg_start = reinterpret_cast<int32_t*>(a_val + kOpTile);
+
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kOpTile;
+  const int64_t g1 = min(total, g0 + kOpTile);
+  if (threadIdx.x == 0) {
+    // GroupRange + Search: the slices holding the first and the last element of this block
+    const int64_t s0 = upper_bound_minus1(slice_off, 0, kcols + 1, g0);
+    const int64_t s1 = upper_bound_minus1(slice_off, s0, kcols + 1, g1 - 1);
+    const int64_t len0 = brp[s0 + 1] - brp[s0];
+    const int64_t len1 = brp[s1 + 1] - brp[s1];
+    // ARange (GetAEntry, Eq. 3): first and last entry of A~_CSC touched by this block
+    const int64_t a_first = colptr[s0] + (g0 - slice_off[s0]) / len0;
+    const int64_t a_last = colptr[s1] + (g1 - 1 - slice_off[s1]) / len1;
+    hdr.s0 = s0;
+    hdr.s1 = s1;
+    hdr.a_first = a_first;
+    hdr.nent = a_last - a_first + 1;
+  }
+  __syncthreads();
+  const int64_t s0 = hdr.s0, s1 = hdr.s1, a_first = hdr.a_first, nent = hdr.nent;
+  if (nent > kOpTile || nent <= 0) {  // impossible for consistent offsets
+    if (threadIdx.x == 0) set_error(err, kErrBounds);
+    return;
+  }
+  // Step 2: reserve space in the C^ rows, one atomic per (entry, block) (GetExcess trims the
+  // partial B rows at both ends of the block's range).
+  for (int64_t e = threadIdx.x; e < nent; e += blockDim.x) {
+    const int64_t a = a_first + e;
+    const int64_t s = upper_bound_minus1(colptr, s0, s1 + 1, a);
+    const int64_t b0 = brp[s];
+    const int64_t len = brp[s + 1] - b0;
+    const int64_t F = slice_off[s] + (a - colptr[s]) * len;
+    const int64_t lo = max(F, g0), hi = min(F + len, g1);
+    const int64_t cnt = hi > lo ? hi - lo : 0;
+    const int64_t clo = lo < g1 ? lo : g1;
+    int64_t base = 0;
+    if (cnt > 0) base = static_cast<int64_t>(atomicAdd(&cursor[crow[a]], static_cast<unsigned long long>(cnt)));
+    seg_start[e] = static_cast<int32_t>(clo - g0);
+    dst_delta[e] = base - (clo - g0);
+    src_delta[e] = b0 + (clo - F) - (clo - g0);
+    a_val[e] = VALS ? cval[a] : 0.0;
+  }
+  __syncthreads();
+  // Step 3: populate C^, consecutive threads -> consecutive elements of a B row
+  const int32_t n = static_cast<int32_t>(g1 - g0);
+  int32_t p = threadIdx.x;
+  if (p >= n) return;
+  int32_t e;
+  {
+    int32_t lo = 0, hi = static_cast<int32_t>(nent) - 1;
+    while (lo < hi) {  // last entry with seg_start <= p
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (seg_start[mid] <= p) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+  }
+  for (; p < n; p += blockDim.x) {
+    while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
+    const int64_t src = src_delta[e] + p;
+    const int64_t dst = dst_delta[e] + p;
+    out_col[dst] = bcol[src];
+    if (VALS) out_val[dst] = a_val[e] * bval[src];
+  }
+}
+
+void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
+                          const int64_t* slice_off, int64_t kcols, int64_t total, const spgemm_csr& B,
+                          int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
+                          uint32_t* err, cudaStream_t s) {
+  if (total == 0) return;
+  const size_t smem = kOpTile * (8 + 8 + 8 + 4);
+  const unsigned grid = static_cast<unsigned>(ceil_div(total, kOpTile));
+  auto* ull = reinterpret_cast<unsigned long long*>(row_cursor);
+  if (with_vals) {
+    cudaFuncSetAttribute(k_outer_product<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    note_launch();
+    k_outer_product<true><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, kcols, total,
+                                                         B.row_ptr, B.col_idx, B.vals, ull, chat_col,
+                                                         chat_val, err);
+  } else {
+    cudaFuncSetAttribute(k_outer_product<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    note_launch();
+    k_outer_product<false><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, kcols, total,
+                                                          B.row_ptr, B.col_idx, B.vals, ull, chat_col,
+                                                          nullptr, err);
+  }
+}
+
+// ---- histogram and multisplit (Algorithm 5) -----------------------------------------------------
+constexpr int kMsItems = static_cast<int>(kMsTile) / kMsThreads;  // 8 per thread
+
+// Row window of one block: rows [r0, r0 + nr) intersect elements [e0, e1).
+struct MsHdr {
+  int64_t r0, r_last;
+};
+
+__device__ __forceinline__ int find_local_row(const int64_t* rstart, int nr, int64_t pos) {
+  int lo = 0, hi = nr - 1;  // last local row with rstart <= pos
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rstart[mid] <= pos) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kMsThreads) k_histogram(const int64_t* __restrict__ rp, int64_t nrows,
+                                                         int64_t total, const int32_t* __restrict__ col,
+                                                         int shift, int64_t v, int64_t gr,
+                                                         unsigned long long* __restrict__ counts, uint32_t* err) {
+  extern __shared__ __align__(16) char smem_raw[];
+  __shared__ MsHdr hdr;
+  int64_t* rstart = reinterpret_cast<int64_t*>(smem_raw);  // gr + 1
+  unsigned* hist = reinterpret_cast<unsigned*>(rstart + gr + 1);  // gr * v
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kMsTile;
+  const int64_t g1 = min(total, g0 + kMsTile);
+  if (threadIdx.x == 0) {
+    hdr.r0 = upper_bound_minus1(rp, 0, nrows + 1, g0);
+    hdr.r_last = upper_bound_minus1(rp, hdr.r0, nrows + 1, g1 - 1);
+  }
+  __syncthreads();
+  const int64_t rfirst = hdr.r0, rlast = hdr.r_last;
+  for (int64_t w0 = rfirst; w0 <= rlast; w0 += gr) {  // windows of at most gr rows
+    const int nr = static_cast<int>(min(gr, rlast - w0 + 1));
+    const int64_t e0 = max(g0, rp[w0]);
+    const int64_t e1 = min(g1, rp[w0 + nr]);
+    for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
+    for (int64_t i = threadIdx.x; i < nr * v; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMsItems; ++j) {
+      const int64_t p = e0 + j * kMsThreads + threadIdx.x;
+      int bin = -1;
+      if (p < e1) {
+        const int r = find_local_row(rstart, nr, p);
+        const int64_t c = static_cast<int64_t>(col[p]) >> shift;
+        if (c < v) bin = static_cast<int>(r * v + c);
+        else set_error(err, kErrBounds);
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[bin], __popc(peers));
+    }
+    __syncthreads();
+    for (int64_t b = threadIdx.x; b < nr * v; b += blockDim.x) {
+      const unsigned h = hist[b];
+      if (h) atomicAdd(&counts[(w0 + b / v) * v + (b % v)], static_cast<unsigned long long>(h));
+    }
+    __syncthreads();
+  }
+}
+
+void launch_histogram(const int64_t* row_ptr, int64_t nrows, int64_t total, const int32_t* col, int shift,
+                      int64_t nchunks, int64_t group_rows, unsigned long long* counts, uint32_t* err,
+                      cudaStream_t s) {
+  if (total == 0) return;
+  const size_t smem = (group_rows + 1) * 8 + group_rows * nchunks * 4;
+  cudaFuncSetAttribute(k_histogram, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  note_launch();
+  k_histogram<<<static_cast<unsigned>(ceil_div(total, kMsTile)), kMsThreads, smem, s>>>(
+      row_ptr, nrows, total, col, shift, nchunks, group_rows, counts, err);
+}
+
+template <bool VALS>
+__global__ void __launch_bounds__(kMsThreads) k_multisplit(
+    const int64_t* __restrict__ rp, int64_t nrows, int64_t total, const int32_t* __restrict__ in_col,
+    const double* __restrict__ in_val, int shift, int64_t v, int64_t gr, const int32_t* __restrict__ xmap,
+    unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col, double* __restrict__ out_val,
+    uint32_t* err) {
+  extern __shared__ __align__(16) char smem_raw[];
+  __shared__ MsHdr hdr;
+  __shared__ unsigned scan_tmp[33];
+  double* val_buf = reinterpret_cast<double*>(smem_raw);                       // kMsTile
+  unsigned long long* goff = reinterpret_cast<unsigned long long*>(val_buf + kMsTile);  // gr*v
+  int64_t* rstart = reinterpret_cast<int64_t*>(goff + gr * v);                 // gr + 1
+  int32_t* col_buf = reinterpret_cast<int32_t*>(rstart + gr + 1);             // kMsTile
+  unsigned* hist = reinterpret_cast<unsigned*>(col_buf + kMsTile);             // gr*v (count, then cursor)
+  unsigned* loff = hist + gr * v;                                              // gr*v + 1
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kMsTile;
+  const int64_t g1 = min(total, g0 + kMsTile);
+  if (threadIdx.x == 0) {
+    hdr.r0 = upper_bound_minus1(rp, 0, nrows + 1, g0);
+    hdr.r_last = upper_bound_minus1(rp, hdr.r0, nrows + 1, g1 - 1);
+  }
+  __syncthreads();
+  const int64_t rfirst = hdr.r0, rlast = hdr.r_last;
+  const int64_t wmask = (int64_t(1) << shift) - 1;
+  for (int64_t w0 = rfirst; w0 <= rlast; w0 += gr) {
+    const int nr = static_cast<int>(min(gr, rlast - w0 + 1));
+    const int64_t e0 = max(g0, rp[w0]);
+    const int64_t e1 = min(g1, rp[w0 + nr]);
+    const int nbins = static_cast<int>(nr * v);
+    for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
+    for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    // load the tile into registers and build the local histogram
+    int32_t c_reg[kMsItems];
+    double v_reg[kMsItems];
+    int bin_reg[kMsItems];
+#pragma unroll
+    for (int j = 0; j < kMsItems; ++j) {
+      const int64_t p = e0 + j * kMsThreads + threadIdx.x;
+      int bin = -1;
+      c_reg[j] = 0;
+      v_reg[j] = 0.0;
+      if (p < e1) {
+        c_reg[j] = in_col[p];
+        if (VALS) v_reg[j] = in_val[p];
+        const int r = find_local_row(rstart, nr, p);
+        const int64_t c = static_cast<int64_t>(c_reg[j]) >> shift;
+        if (c < v) bin = static_cast<int>(r * v + c);
+        else set_error(err, kErrBounds);
+      }
+      bin_reg[j] = bin;
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[bin], __popc(peers));
+    }
+    __syncthreads();
+    // local offsets (exclusive scan of the histogram) and global reservations
+    {
+      const int per = (nbins + kMsThreads - 1) / kMsThreads;
+      const int b0 = threadIdx.x * per;
+      unsigned local = 0;
+      for (int b = b0; b < min(nbins, b0 + per); ++b) local += hist[b];
+      unsigned tot;
+      const unsigned incl = block_incl_scan(local, scan_tmp, &tot);
+      unsigned run = incl - local;
+      for (int b = b0; b < min(nbins, b0 + per); ++b) {
+        const unsigned h = hist[b];
+        loff[b] = run;
+        if (h) {
+          const int64_t gchunk = (w0 + b / v) * v + (b % v);
+          const int64_t q = xmap ? xmap[gchunk] : gchunk;
+          goff[b] = atomicAdd(&cursor[q], static_cast<unsigned long long>(h));
+        }
+        hist[b] = run;  // becomes the permute cursor
+        run += h;
+      }
+      if (threadIdx.x == 0) loff[nbins] = tot;
+    }
+    __syncthreads();
+    // permute into shared memory, grouped by (row, chunk)
+#pragma unroll
+    for (int j = 0; j < kMsItems; ++j) {
+      const int bin = bin_reg[j];
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      const int leader = __ffs(peers) - 1;
+      unsigned base = 0;
+      if (bin >= 0 && static_cast<int>(lane_id()) == leader) base = atomicAdd(&hist[bin], __popc(peers));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (bin >= 0) {
+        const unsigned pos = base + __popc(peers & lanemask_lt());
+        col_buf[pos] = c_reg[j];
+        if (VALS) val_buf[pos] = v_reg[j];
+      }
+    }
+    __syncthreads();
+    // coalesced write: runs of one local chunk go to consecutive global positions
+    const int cnt = static_cast<int>(e1 - e0);
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      const int32_t c = col_buf[i];
+      int r = 0;
+      {
+        int lo = 0, hi = nr - 1;  // last row whose first bin starts at or before i
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (static_cast<int>(loff[mid * v]) <= i) lo = mid; else hi = mid - 1;
+        }
+        r = lo;
+      }
+      const int b = static_cast<int>(r * v + (static_cast<int64_t>(c) >> shift));
+      const int64_t dst = static_cast<int64_t>(goff[b]) + (i - static_cast<int>(loff[b]));
+      out_col[dst] = static_cast<int32_t>(c & wmask);
+      if (VALS) out_val[dst] = val_buf[i];
+    }
+    __syncthreads();
+  }
+}
+
+void launch_multisplit(const int64_t* row_ptr, int64_t nrows, int64_t total, const int32_t* in_col,
+                       const double* in_val, int shift, int64_t nchunks, int64_t group_rows,
+                       const int32_t* xmap, unsigned long long* reord_cursor, int32_t* out_col,
+                       double* out_val, bool with_vals, uint32_t* err, cudaStream_t s) {
+  if (total == 0) return;
+  const int64_t bins = group_rows * nchunks;
+  const size_t smem = kMsTile * 8 + bins * 8 + (group_rows + 1) * 8 + kMsTile * 4 + bins * 4 + (bins + 1) * 4;
+  const unsigned grid = static_cast<unsigned>(ceil_div(total, kMsTile));
+  if (with_vals) {
+    cudaFuncSetAttribute(k_multisplit<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    note_launch();
+    k_multisplit<true><<<grid, kMsThreads, smem, s>>>(row_ptr, nrows, total, in_col, in_val, shift, nchunks,
+                                                      group_rows, xmap, reord_cursor, out_col, out_val, err);
+  } else {
+    cudaFuncSetAttribute(k_multisplit<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    note_launch();
+    k_multisplit<false><<<grid, kMsThreads, smem, s>>>(row_ptr, nrows, total, in_col, nullptr, shift, nchunks,
+                                                       group_rows, xmap, reord_cursor, out_col, nullptr, err);
+  }
+}
+
+// ---- chunk partition, metadata and final chunk descriptors ---------------------------------------
+__global__ void k_chunk_partition(const unsigned long long* __restrict__ counts, int64_t n, int64_t tau,
+                                  uint8_t* __restrict__ bin) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) bin[i] = counts[i] > static_cast<unsigned long long>(tau) ? 0 : 1;
+}
+void launch_chunk_partition(const unsigned long long* counts, int64_t n, int64_t tau, uint8_t* bin,
+                            cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_chunk_partition<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(counts, n, tau, bin);
+}
+
+__global__ void k_invert(const int32_t* __restrict__ list, int64_t n, int32_t* __restrict__ xmap) {
+  const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (q < n) xmap[list[q]] = static_cast<int32_t>(q);
+}
+void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_invert<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(list, n, xmap);
+}
+
+__global__ void k_reord_meta(const unsigned long long* __restrict__ counts, int64_t nin, int64_t v,
+                             const int32_t* __restrict__ xmap, const int32_t* __restrict__ in_row,
+                             const int32_t* __restrict__ in_base, int64_t width, int64_t* __restrict__ rcnt,
+                             int32_t* __restrict__ out_row, int32_t* __restrict__ out_base) {
+  const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (id >= nin * v) return;
+  const int64_t p = id / v, c = id % v;
+  const int64_t q = xmap ? xmap[id] : id;
+  rcnt[q] = static_cast<int64_t>(counts[id]);
+  out_row[q] = in_row ? in_row[p] : static_cast<int32_t>(p);
+  out_base[q] = (in_base ? in_base[p] : 0) + static_cast<int32_t>(c * width);
+}
+void launch_reord_meta(const unsigned long long* counts, int64_t nrows_in, int64_t nchunks, const int32_t* xmap,
+                       const int32_t* in_row, const int32_t* in_base, int64_t width, int64_t* reord_cnt,
+                       int32_t* out_row, int32_t* out_base, cudaStream_t s) {
+  const int64_t n = nrows_in * nchunks;
+  if (n == 0) return;
+  note_launch();
+  k_reord_meta<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(counts, nrows_in, nchunks, xmap, in_row,
+                                                                       in_base, width, reord_cnt, out_row, out_base);
+}
+
+__global__ void k_final_desc(const int64_t* __restrict__ rptr, int64_t q0, int64_t q1, int64_t elem_base,
+                             const int32_t* __restrict__ row, const int32_t* __restrict__ base,
+                             int64_t* __restrict__ fs, int64_t* __restrict__ fc, int32_t* __restrict__ fr,
+                             int32_t* __restrict__ fb) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t q = q0 + i;
+  if (q >= q1) return;
+  fs[i] = elem_base + rptr[q];
+  fc[i] = rptr[q + 1] - rptr[q];
+  fr[i] = row ? row[q] : static_cast<int32_t>(q);
+  fb[i] = base ? base[q] : 0;
+}
+void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t elem_base, const int32_t* row,
+                       const int32_t* base, int64_t* f_start, int64_t* f_cnt, int32_t* f_row, int32_t* f_base,
+                       cudaStream_t s) {
+  if (q1 <= q0) return;
+  note_launch();
+  k_final_desc<<<static_cast<unsigned>(ceil_div(q1 - q0, 256)), 256, 0, s>>>(reord_ptr, q0, q1, elem_base, row,
+                                                                             base, f_start, f_cnt, f_row, f_base);
+}
+
+// Accumulator bin of a final chunk: hash ladder level by size, or the dense accumulator (bin
+// 2 * levels) for chunks above tau, which only occur at the last level (width W).
+__global__ void k_chunk_classify(const int64_t* __restrict__ fc, int64_t n, BinRule r, uint8_t* __restrict__ bin) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int64_t c = fc[i];
+  uint8_t b;
+  if (c == 0) {
+    b = kBinEmpty;
+  } else if (c > r.tau) {
+    b = static_cast<uint8_t>(2 * r.n);
+  } else {
+    int L = 0;
+    while (L < r.n - 1 && c > r.upper[L]) ++L;
+    b = static_cast<uint8_t>(2 * L);
+  }
+  bin[i] = b;
+}
+void launch_chunk_classify(const int64_t* f_cnt, int64_t n, const BinRule& rule, uint8_t* bin, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_chunk_classify<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(f_cnt, n, rule, bin);
+}
+
+// Offsets of the final chunks inside their C rows: a dense grid (row, finest chunk) of
+// chunk sizes, scanned; chunk offset = grid prefix at the chunk - grid prefix at the row start.
+__global__ void k_grid_fill(const int32_t* __restrict__ fr, const int32_t* __restrict__ fb,
+                            const int64_t* __restrict__ fnnz, int64_t n, int shift, int64_t nfin,
+                            int64_t* __restrict__ grid) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) grid[static_cast<int64_t>(fr[i]) * nfin + (fb[i] >> shift)] = fnnz[i];
+}
+void launch_grid_fill(const int32_t* f_row, const int32_t* f_base, const int64_t* f_nnz, int64_t n, int shift_fin,
+                      int64_t nfin, int64_t* grid, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_grid_fill<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(f_row, f_base, f_nnz, n, shift_fin, nfin,
+                                                                      grid);
+}
+__global__ void k_grid_finish(const int64_t* __restrict__ S, const int32_t* __restrict__ fr,
+                              const int32_t* __restrict__ fb, int64_t n, int shift, int64_t nfin,
+                              int64_t* __restrict__ fout) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const int64_t r0 = static_cast<int64_t>(fr[i]) * nfin;
+    fout[i] = S[r0 + (fb[i] >> shift)] - S[r0];
+  }
+}
+void launch_grid_finish(const int64_t* grid_scanned, const int32_t* f_row, const int32_t* f_base, int64_t n,
+                        int shift_fin, int64_t nfin, int64_t* f_out, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_grid_finish<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(grid_scanned, f_row, f_base, n,
+                                                                        shift_fin, nfin, f_out);
+}
+__global__ void k_row_totals(const int64_t* __restrict__ S, int64_t nrows, int64_t nfin,
+                             const int32_t* __restrict__ rows, int64_t* __restrict__ row_nnz) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r < nrows) row_nnz[rows[r]] = S[(r + 1) * nfin] - S[r * nfin];
+}
+void launch_row_totals(const int64_t* grid_scanned, int64_t nrows, int64_t nfin, const int32_t* heavy_rows,
+                       int64_t* row_nnz, cudaStream_t s) {
+  if (nrows == 0) return;
+  note_launch();
+  k_row_totals<<<static_cast<unsigned>(ceil_div(nrows, 256)), 256, 0, s>>>(grid_scanned, nrows, nfin, heavy_rows,
+                                                                           row_nnz);
+}
+
+}  // namespace sg

@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element.
+
+Small and medium inputs are compared in full; the full-size workloads of the benchmark are
+compared on a sample of rows (all the heaviest rows plus a seeded uniform sample) and through
+invariants that hold at any size.  Planner overrides force the rare paths on small inputs:
+every row heavy, several multisplit levels, light chunks at early levels, recomputation across
+many heavy batches."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _helpers import (compare_full, compare_rows, compare_sampled_device, device_invariants,
+                      gpu_product, gpu_product_device, invariants)
+
+pytestmark = pytest.mark.gpu
+
+
+def opts(**kw):
+    import sparse_gemm_irregular_gb300 as sg
+    return sg.options(**kw)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("dup,empty,sort", [(False, False, True), (True, True, False)])
+def test_small_random_default(gpu_lib, seed, dup, empty, sort):
+    A = synth.random_sparse(300, 257, 0.03, seed, duplicates=dup, empty_rows=empty, sort_rows=sort)
+    B = synth.random_sparse(257, 411, 0.05, seed + 50, duplicates=dup, empty_rows=empty, sort_rows=sort)
+    rp, col, val, st = gpu_product(A, B)
+    compare_full(A, B, rp, col, val)
+
+
+FORCED = [
+    # every row heavy, one level of 8 chunks of width 64
+    dict(flags=1, tau=64, chunk_width=64, chunks_max=8),
+    # heavy above 16, two levels (4 x 4 chunks of width 32), light chunks at level 0
+    dict(tau=16, chunk_width=32, chunks_max=4),
+    # four levels of 2 chunks
+    dict(tau=8, chunk_width=32, chunks_max=2),
+    # everything heavy, one chunk per row (W covers all columns)
+    dict(flags=1, tau=32, chunk_width=512),
+    # many heavy batches, recomputed in the numeric phase
+    dict(tau=16, chunk_width=64, chunks_max=4, heavy_batch_elems=700, flags=16),
+    # light rows only, hash accumulators
+    dict(flags=2 | 4, tau=4096),
+]
+
+
+@pytest.mark.parametrize("kw", FORCED)
+@pytest.mark.parametrize("seed", [3, 4])
+def test_forced_paths(gpu_lib, kw, seed):
+    A = synth.random_sparse(200, 180, 0.06, seed, duplicates=True, empty_rows=True, sort_rows=False)
+    B = synth.random_sparse(180, 500, 0.08, seed + 9, duplicates=True, empty_rows=True, sort_rows=False)
+    rp, col, val, st = gpu_product(A, B, opts(**kw))
+    compare_full(A, B, rp, col, val)
+    if kw.get("flags", 0) & 1:
+        assert st.rows_heavy == int((oracle.row_ip(A, B) > 0).sum())
+    if kw.get("chunks_max") == 2:
+        assert st.levels_run >= 2
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(tau=16, chunk_width=32, chunks_max=4),
+                                dict(flags=1, tau=64, chunk_width=64, chunks_max=8)])
+def test_integer_values_exact(gpu_lib, kw):
+    A = synth.random_sparse(150, 160, 0.1, 21, duplicates=True, integer_values=True, sort_rows=False)
+    B = synth.random_sparse(160, 300, 0.1, 22, duplicates=True, integer_values=True, sort_rows=False)
+    rp, col, val, _ = gpu_product(A, B, opts(**kw) if kw else None)
+    orp, ocol, oval, _ = oracle.spgemm_rows(A, B, np.arange(A.rows))
+    assert np.array_equal(rp, orp) and np.array_equal(col, ocol)
+    assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
+
+
+def test_rmat_small_full(gpu_lib):
+    """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
+    row, thousands of light rows in every ladder bin -- compared in full."""
+    A = synth.rmat(14, 16, seed=5)
+    rp, col, val, st = gpu_product(A, A)
+    assert st.rows_heavy > 0 and st.rows_light > 0
+    compare_full(A, A, rp, col, val, threads=16)
+
+
+def test_rmat_small_forced_levels(gpu_lib):
+    A = synth.rmat(13, 16, seed=6)
+    rp, col, val, st = gpu_product(A, A, opts(tau=256, chunk_width=64, chunks_max=4))
+    assert st.levels_run >= 2
+    compare_full(A, A, rp, col, val, threads=16)
+
+
+def test_config1_full(gpu_lib):
+    A = synth.config(1)
+    rp, col, val, _ = gpu_product(A, A)
+    compare_full(A, A, rp, col, val)
+
+
+def test_config2_full(gpu_lib):
+    A = synth.config(2)
+    rp, col, val, st = gpu_product(A, A)
+    assert st.rows_dense_light == A.rows  # the shortened dense path
+    assert rp[-1] == 13 * A.rows - 42
+    compare_full(A, A, rp, col, val, threads=16)
+
+
+def test_banded_ones_closed_form(gpu_lib):
+    A = synth.banded(100_000, 3)
+    A.val = np.ones(A.nnz)
+    rp, col, val, _ = gpu_product(A, A)
+    assert rp[-1] == 13 * A.rows - 42
+    for i in (10, 5000, 99_000):
+        a, b = rp[i], rp[i + 1]
+        assert np.array_equal(col[a:b], np.arange(i - 6, i + 7))
+        assert np.array_equal(val[a:b], 7.0 - np.abs(np.arange(-6, 7)))
+
+
+def sample_rows(A, B, n_top=300, n_uniform=3000, seed=0):
+    ip = oracle.row_ip(A, B)
+    top = np.argsort(ip)[-n_top:]
+    uni = (synth.draws(seed, synth.STREAM_SAMPLE, 0, n_uniform) % np.uint64(A.rows)).astype(np.int64)
+    return np.unique(np.concatenate([top, uni]))
+
+
+def test_config3_full_size_sampled(gpu_lib):
+    A = synth.config(3)
+    p, rp, col, val = gpu_product_device(A, A)
+    st = p.stats()
+    assert st.rows_heavy > 0 and st.resident == 1
+    rowsum, _ = device_invariants(A, A, rp, col, val)
+    compare_sampled_device(A, A, rp, col, val, sample_rows(A, A))
+    p.close()
+
+
+def test_config5_full_size_sampled(gpu_lib):
+    M = synth.config(5)
+    p, rp, col, val = gpu_product_device(M, M)
+    st = p.stats()
+    assert st.rows_heavy > 0
+    _, colsum = device_invariants(M, M, rp, col, val)
+    # C = M M is column-stochastic
+    assert float((colsum - 1.0).abs().max()) <= 1e-9
+    compare_sampled_device(M, M, rp, col, val, sample_rows(M, M, n_top=100, n_uniform=2000))
+    p.close()
+    del rp, col, val
+
+
+def test_identity_and_empty(gpu_lib):
+    from synth import CSR
+    A = synth.random_sparse(64, 64, 0.1, 7)
+    I = CSR(64, 64, np.arange(65, dtype=np.int64), np.arange(64, dtype=np.int32), np.ones(64))
+    rp, col, val, _ = gpu_product(A, I)
+    assert np.array_equal(rp, A.row_ptr) and np.array_equal(col, A.col) and np.array_equal(val, A.val)
+    Z = CSR(10, 64, np.zeros(11, np.int64), np.zeros(0, np.int32), np.zeros(0))
+    rp, col, val, _ = gpu_product(Z, A)
+    assert np.all(rp == 0) and len(col) == 0
+
+
+def test_numeric_rows_window(gpu_lib):
+    import torch
+    import sparse_gemm_irregular_gb300 as sg
+    A = synth.rmat(12, 16, seed=8)
+    dA = sg.DeviceCSR.from_host(A)
+    p = sg.Product(dA, dA, opts=opts(tau=512, chunk_width=256))
+    rp, nnz = p.symbolic()
+    full_c, full_v = p.numeric()
+    rph = rp.cpu().numpy()
+    for b, e in [(0, 1), (0, 100), (37, 2000), (4000, 4096), (0, 4096)]:
+        n = int(rph[e] - rph[b])
+        c = torch.empty(max(n, 1), dtype=torch.int32, device="cuda")
+        v = torch.empty(max(n, 1), dtype=torch.float64, device="cuda")
+        p.numeric_rows(b, e, c, v)
+        torch.cuda.synchronize()
+        assert torch.equal(c[:n], full_c[rph[b]:rph[e]])
+        assert torch.equal(v[:n], full_v[rph[b]:rph[e]]) or torch.allclose(v[:n], full_v[rph[b]:rph[e]], rtol=1e-12)
+    p.close()
+
+
+def test_validate_flag_rejects_bad_column(gpu_lib):
+    import sparse_gemm_irregular_gb300 as sg
+    A = synth.random_sparse(20, 20, 0.2, 1)
+    A.col = A.col.copy()
+    A.col[3] = 25  # out of range for 20 columns
+    dA = sg.DeviceCSR.from_host(A)
+    B = sg.DeviceCSR.from_host(synth.random_sparse(20, 20, 0.2, 2))
+    with pytest.raises(sg.SpgemmError) as e:
+        sg.Product(dA, B, opts=opts(flags=8))
+    assert e.value.code == -2
