@@ -169,6 +169,27 @@ long long spgemm_kernel_launches(void);
 /* Release the workspace (stream-ordered on the handle's stream) and the handle.  NULL is ok. */
 int spgemm_destroy(spgemm_handle h);
 
+/* C.row_ptr and nnz(C) without allocating any device memory.  The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc (or any allocator) at the
+ * point where they need the row sizes of C -- code running inside an allocator or memory
+ * manager, loops that forbid allocation after start-up, hosts with a fixed memory budget.
+ * Instead of a workspace it uses one static __device__ array of 33,280 bytes that every
+ * device which loads this library holds until the process exits.
+ *   m, k, n, A, B: as for spgemm_create (A and B in device memory, borrowed);
+ *   c_row_ptr:     device, m+1 int64, caller-owned, written with the exclusive scan of the
+ *                  distinct column counts of the rows of A*B (identical to spgemm_symbolic);
+ *   c_nnz:         host, receives nnz(C);
+ *   stream:        cudaStream_t; the call synchronises it before returning.
+ * Limits: m <= 16,777,215 rows and at most 2048 intermediate products in every row of A*B;
+ * otherwise SPGEMM_ERR_INVALID_ARG (a too-long row is detected on the device, after the
+ * kernels ran, and c_row_ptr is then meaningless).  No cudaMalloc, cudaFree or allocating
+ * library call is made.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current), so make that first call before any
+ * stream capture.  Every call on a device shares the one array: calls that overlap on the
+ * GPU (other streams, other host threads) race and give wrong results; serialise them. */
+int spgemm_symbolic_noalloc(int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
+                            const spgemm_csr* B, int64_t* c_row_ptr, int64_t* c_nnz, void* stream);
+
 const char* spgemm_strerror(int code);
 /* Detail of the last failure on the calling host thread ("" if none). */
 const char* spgemm_last_error(void);

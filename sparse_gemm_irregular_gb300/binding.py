@@ -70,6 +70,7 @@ EXPORTS = {
     "spgemm_get_plan": (ctypes.c_int, [_vp, _vp]),
     "spgemm_get_phase_times": (ctypes.c_int, [_vp, _vp, _vp, _i32]),
     "spgemm_kernel_launches": (ctypes.c_longlong, []),
+    "spgemm_symbolic_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "spgemm_destroy": (ctypes.c_int, [_vp]),
     "spgemm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "spgemm_last_error": (ctypes.c_char_p, []),
@@ -167,6 +168,14 @@ def spgemm_get_phase_times(h):
 
 def spgemm_kernel_launches() -> int:
     return int(load().spgemm_kernel_launches())
+
+
+def spgemm_symbolic_noalloc(m, k, n, A: spgemm_csr, B: spgemm_csr, c_row_ptr: int, stream: int = 0) -> int:
+    """C.row_ptr and nnz(C) without device allocation (light products only; see spgemm.h)."""
+    nnz = _i64(0)
+    _check(load().spgemm_symbolic_noalloc(m, k, n, ctypes.byref(A), ctypes.byref(B), _vp(c_row_ptr),
+                                          ctypes.byref(nnz), _vp(stream)), "spgemm_symbolic_noalloc")
+    return nnz.value
 
 
 def spgemm_destroy(h):
