@@ -166,6 +166,11 @@ int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_
 /* Number of kernels this library has launched in the process so far (all handles). */
 long long spgemm_kernel_launches(void);
 
+/* Device workspace comes from a stream-ordered memory pool (one per device) that keeps freed
+ * memory cached for the next product.  This returns the cached memory to the device; call it
+ * when no product is running.  Always SPGEMM_OK. */
+int spgemm_release_memory(void);
+
 /* Release the workspace (stream-ordered on the handle's stream) and the handle.  NULL is ok. */
 int spgemm_destroy(spgemm_handle h);
 

@@ -71,6 +71,7 @@ EXPORTS = {
     "spgemm_get_phase_times": (ctypes.c_int, [_vp, _vp, _vp, _i32]),
     "spgemm_kernel_launches": (ctypes.c_longlong, []),
     "spgemm_symbolic_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "spgemm_release_memory": (ctypes.c_int, []),
     "spgemm_destroy": (ctypes.c_int, [_vp]),
     "spgemm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "spgemm_last_error": (ctypes.c_char_p, []),
@@ -180,6 +181,10 @@ def spgemm_symbolic_noalloc(m, k, n, A: spgemm_csr, B: spgemm_csr, c_row_ptr: in
 
 def spgemm_destroy(h):
     _check(load().spgemm_destroy(h), "spgemm_destroy")
+
+
+def spgemm_release_memory():
+    _check(load().spgemm_release_memory(), "spgemm_release_memory")
 
 
 def spgemm_strerror(code: int) -> str:

@@ -16,6 +16,7 @@
 #include <algorithm>
 #include <atomic>
 #include <memory>
+#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -36,10 +37,38 @@ int check_cuda(cudaError_t e, const char* what) {
   return SPGEMM_ERR_CUDA;
 }
 
+// Workspace comes from one stream-ordered memory pool per device that keeps freed memory for
+// reuse (release threshold = unlimited): products of the same size then allocate without
+// mapping new physical memory.  spgemm_release_memory() hands the cached memory back.
+static std::mutex g_pool_mu;
+static cudaMemPool_t g_pool[64] = {};
+
+cudaMemPool_t device_pool(int dev) {
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t thr = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    g_pool[dev] = pool;
+  }
+  return g_pool[dev];
+}
+
 void* ws_alloc(spgemm_ctx* h, size_t bytes) {
   void* p = nullptr;
   if (bytes == 0) bytes = 16;
-  if (cudaMallocAsync(&p, bytes, h->st) != cudaSuccess) {
+  if (cudaMallocFromPoolAsync(&p, bytes, h->pool, h->st) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
@@ -90,6 +119,10 @@ using namespace sg;
   } while (0)
 
 namespace {
+
+// Last-level chunk bins: threads per chunk and hash slots (bin 3 is the dense accumulator).
+constexpr int kChunkTpr[4] = {32, 256, 512, 1024};
+constexpr int64_t kChunkSlots[4] = {512, 2048, 2 * kChunkDenseMin, 0};
 
 // Scan scratch that grows on demand.
 int64_t* scan_scratch(spgemm_ctx* h, int64_t n) {
@@ -234,6 +267,7 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
       SG_ALLOC(hb.f_row, int32_t, R);
       SG_ALLOC(hb.f_base, int32_t, R);
       launch_final_desc(c_rowptr, 0, R, 0, nullptr, nullptr, hb.f_start, hb.f_cnt, hb.f_row, hb.f_base, h->st);
+      hb.bitmap_from = 0;
     }
     return SPGEMM_OK;
   }
@@ -340,6 +374,7 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     // light outputs of this level (all outputs at the last level) are final chunks
     if (record) {
       const int64_t q0 = last ? 0 : li.nheavy;
+      hb.bitmap_from = last ? hb.nfinal : hb.nfinal + (nout - q0);
       launch_final_desc(rptr, q0, nout, out_half * cap, out_row, out_base, hb.f_start + hb.nfinal,
                         hb.f_cnt + hb.nfinal, hb.f_row + hb.nfinal, hb.f_base + hb.nfinal, h->st);
       hb.nfinal += nout - q0;
@@ -382,7 +417,7 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
 int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
   const int64_t nf = hb.nfinal;
   const int64_t R = hb.h1 - hb.h0;
-  const int nb = h->nbins;
+  const int nb = h->lad.n + 4;  // chunk bins: hash ladder + 4 bitmap bins
   SG_ALLOC(hb.f_nnz, int64_t, nf);
   SG_ALLOC(hb.f_out, int64_t, nf);
   SG_ALLOC(hb.f_list, int32_t, nf);
@@ -395,7 +430,7 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     SG_ALLOC(fbin, uint8_t, nf);
     SG_ALLOC(fcnt, int64_t, nb * nblk + 1);
     SG_ALLOC(starts, int64_t, nb + 1);
-    launch_chunk_classify(hb.f_cnt, nf, h->rule, fbin, h->st);
+    launch_chunk_classify(hb.f_cnt, nf, hb.bitmap_from, h->rule, fbin, h->st);
     launch_bin_count(fbin, nf, nb, fcnt, h->st);
     SG_TRY(scan(h, fcnt, fcnt, nb * nblk));
     launch_bin_scatter(fbin, nf, nb, fcnt, hb.f_list, h->st);
@@ -422,14 +457,14 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     Sink sk{};
     sk.row_begin = 0;
     sk.row_end = h->m;
-    for (int L = 0; L < h->lad.n; ++L) {
-      const int b = 2 * L;
-      launch_chunks(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+    for (int L = 0; L < h->lad.n; ++L)  // light chunks of early levels: hash ladder
+      launch_chunks(cs, hb.f_list + hb.f_bin_start[L], hb.f_bin_start[L + 1] - hb.f_bin_start[L],
                     h->lad.slots[L], h->lad.tpr[L], false, 0, false, sk, h->d_err, h->st);
+    for (int j = 0; j < 4; ++j) {        // last-level chunks: bitmaps of width W
+      const int b = h->lad.n + j;
+      launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+                          h->plan.chunk_width, 0, 0, kChunkTpr[j], sk, h->d_err, h->st);
     }
-    const int bd = 2 * h->lad.n;
-    launch_chunks(cs, hb.f_list + hb.f_bin_start[bd], hb.f_bin_start[bd + 1] - hb.f_bin_start[bd], 0, 1024,
-                  true, h->plan.chunk_width, false, sk, h->d_err, h->st);
   }
   // offsets of the chunks inside their rows
   PhaseTimer toff(h, 8);
@@ -460,14 +495,14 @@ int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
   cs.heavy_rows = h->d_heavy + hb.h0;
   cs.col = h->d_chat_col;
   cs.val = h->d_chat_val;
-  for (int L = 0; L < h->lad.n; ++L) {
-    const int b = 2 * L;
-    launch_chunks(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b], h->lad.slots[L],
+  for (int L = 0; L < h->lad.n; ++L)
+    launch_chunks(cs, hb.f_list + hb.f_bin_start[L], hb.f_bin_start[L + 1] - hb.f_bin_start[L], h->lad.slots[L],
                   h->lad.tpr[L], false, 0, true, sk, h->d_err, h->st);
+  for (int j = 0; j < 4; ++j) {
+    const int b = h->lad.n + j;
+    launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+                        h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err, h->st);
   }
-  const int bd = 2 * h->lad.n;
-  launch_chunks(cs, hb.f_list + hb.f_bin_start[bd], hb.f_bin_start[bd + 1] - hb.f_bin_start[bd], 0, 1024, true,
-                h->plan.chunk_width, true, sk, h->d_err, h->st);
   return SPGEMM_OK;
 }
 
@@ -563,6 +598,11 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
   h->device = dev;
+  h->pool = device_pool(dev);
+  if (!h->pool) {
+    set_last_error("could not create the device memory pool");
+    return fail(SPGEMM_ERR_CUDA);
+  }
   h->sms = sms;
   h->smem_optin = optin;
   h->l2_bytes = l2;
@@ -734,7 +774,7 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     ws_free(h, crp);
     levels = std::max<int64_t>(levels, static_cast<int64_t>(hb.lv.size()));
     finals += hb.nfinal;
-    dense += hb.f_bin_start[2 * h->lad.n + 1] - hb.f_bin_start[2 * h->lad.n];
+    dense += hb.f_bin_start[h->lad.n + 4] - hb.f_bin_start[h->lad.n + 3];
   }
   h->stats.levels_run = levels;
   h->stats.final_chunks = finals;
@@ -807,6 +847,13 @@ int spgemm_destroy(spgemm_handle h) {
   h->allocs.clear();
   cudaStreamSynchronize(h->st);
   delete h;
+  return SPGEMM_OK;
+}
+
+int spgemm_release_memory(void) {
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  for (int d = 0; d < 64; ++d)
+    if (g_pool[d]) cudaMemPoolTrimTo(g_pool[d], 0);
   return SPGEMM_OK;
 }
 

@@ -23,6 +23,7 @@ constexpr int kSmemReserve = 7168;         // bytes kept back from s_LM for per-
 constexpr int kMaxLadder = 16;             // light bin ladder levels
 constexpr int kScanTile = 4096;            // elements per scan block (512 threads x 8)
 constexpr int kPhaseSlots = 12;            // timed regions, see spgemm_get_phase_times
+constexpr int64_t kChunkDenseMin = 2048;   // last-level chunks above this size use the dense accumulator
 
 // Light-row / chunk bin ladder derived from tau (hash tables at load factor 1/2).
 struct Ladder {
@@ -138,8 +139,11 @@ void launch_multisplit(const int64_t* row_ptr, int64_t nrows, int64_t total,
 void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t elem_base,
                        const int32_t* row, const int32_t* base, int64_t* f_start, int64_t* f_cnt,
                        int32_t* f_row, int32_t* f_base, cudaStream_t s);
-void launch_chunk_classify(const int64_t* f_cnt, int64_t n, const BinRule& rule, uint8_t* bin,
-                           cudaStream_t s);
+void launch_chunk_classify(const int64_t* f_cnt, int64_t n, int64_t bitmap_from, const BinRule& rule,
+                           uint8_t* bin, cudaStream_t s);
+// bitmap-ordered chunk accumulators (k_chunk.cu); mode 0 symbolic, 1 hash numeric, 2 dense numeric
+void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
+                         int64_t slots, int tpr, const Sink& sink, uint32_t* err, cudaStream_t s);
 void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s);
 void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s);
 void launch_grid_fill(const int32_t* f_row, const int32_t* f_base, const int64_t* f_nnz, int64_t n,
@@ -177,6 +181,7 @@ struct HeavyBatch {
   int32_t* f_list = nullptr;    // chunk ids ordered by accumulator bin
   std::vector<int64_t> f_bin_start;  // host, per chunk bin (size nbins + 1)
   int64_t nnz_c = 0;            // entries of C in the batch's rows (read after the symbolic sync)
+  int64_t bitmap_from = 0;      // descriptors from here on are last-level chunks (width W)
 };
 
 struct spgemm_ctx {
@@ -184,6 +189,7 @@ struct spgemm_ctx {
   spgemm_csr A{}, B{};
   cudaStream_t st = nullptr;
   int device = 0, sms = 0;
+  cudaMemPool_t pool = nullptr;
   int64_t smem_optin = 0, l2_bytes = 0;
   spgemm_options opt{};
   spgemm_plan plan{};

@@ -318,7 +318,7 @@ __device__ void dense_emit(const Group<WARP>& g, const Smem& s, int64_t width, i
 
 // ---- the kernel --------------------------------------------------------------------------
 template <bool WARP, bool NUMERIC, bool DENSE, bool CHUNK>
-__global__ void k_accum(AccParams p) {
+__global__ void __launch_bounds__(1024) k_accum(AccParams p) {
   extern __shared__ __align__(16) char smem_raw[];
   Group<WARP> g;
   int64_t item;

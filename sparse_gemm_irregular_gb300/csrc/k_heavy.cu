@@ -483,28 +483,32 @@ void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t
                                                                              base, f_start, f_cnt, f_row, f_base);
 }
 
-// Accumulator bin of a final chunk: hash ladder level by size, or the dense accumulator (bin
-// 2 * levels) for chunks above tau, which only occur at the last level (width W).
-__global__ void k_chunk_classify(const int64_t* __restrict__ fc, int64_t n, BinRule r, uint8_t* __restrict__ bin) {
+// Accumulator bin of a final chunk.  Chunks of the last level (width W, bitmap kernels):
+// bins nlad + 0..3 = hash for <= 256 elements (warp), <= 1024, <= kChunkDenseMin, and the
+// dense accumulator above.  Light chunks of earlier levels (wider, at most tau elements): the
+// hash ladder levels 0..nlad-1 of the row accumulators.
+__global__ void k_chunk_classify(const int64_t* __restrict__ fc, int64_t n, int64_t bitmap_from, BinRule r,
+                                 uint8_t* __restrict__ bin) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int64_t c = fc[i];
   uint8_t b;
   if (c == 0) {
     b = kBinEmpty;
-  } else if (c > r.tau) {
-    b = static_cast<uint8_t>(2 * r.n);
+  } else if (i >= bitmap_from) {
+    b = static_cast<uint8_t>(r.n + (c <= 256 ? 0 : (c <= 1024 ? 1 : (c <= kChunkDenseMin ? 2 : 3))));
   } else {
     int L = 0;
     while (L < r.n - 1 && c > r.upper[L]) ++L;
-    b = static_cast<uint8_t>(2 * L);
+    b = static_cast<uint8_t>(L);
   }
   bin[i] = b;
 }
-void launch_chunk_classify(const int64_t* f_cnt, int64_t n, const BinRule& rule, uint8_t* bin, cudaStream_t s) {
+void launch_chunk_classify(const int64_t* f_cnt, int64_t n, int64_t bitmap_from, const BinRule& rule,
+                           uint8_t* bin, cudaStream_t s) {
   if (n == 0) return;
   note_launch();
-  k_chunk_classify<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(f_cnt, n, rule, bin);
+  k_chunk_classify<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(f_cnt, n, bitmap_from, rule, bin);
 }
 
 // Offsets of the final chunks inside their C rows: a dense grid (row, finest chunk) of

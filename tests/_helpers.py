@@ -158,6 +158,14 @@ def device_rows(rp, col, val, rows):
             np.concatenate(vals) if vals else np.zeros(0))
 
 
+def release_device_memory():
+    import torch
+    import sparse_gemm_irregular_gb300 as sg
+    torch.cuda.synchronize()
+    sg.spgemm_release_memory()
+    torch.cuda.empty_cache()
+
+
 def compare_sampled_device(A, B, rp, col, val, rows, threads=16):
     rows = np.ascontiguousarray(np.sort(np.unique(rows)), np.int64)
     grp, gcol, gval = device_rows(rp, col, val, rows)

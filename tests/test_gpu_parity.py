@@ -11,7 +11,7 @@ import pytest
 import oracle
 import synth
 from _helpers import (compare_full, compare_rows, compare_sampled_device, device_invariants,
-                      gpu_product, gpu_product_device, invariants)
+                      gpu_product, gpu_product_device, invariants, release_device_memory)
 
 pytestmark = pytest.mark.gpu
 
@@ -126,6 +126,8 @@ def test_config3_full_size_sampled(gpu_lib):
     rowsum, _ = device_invariants(A, A, rp, col, val)
     compare_sampled_device(A, A, rp, col, val, sample_rows(A, A))
     p.close()
+    del rp, col, val
+    release_device_memory()
 
 
 def test_config5_full_size_sampled(gpu_lib):
@@ -139,6 +141,7 @@ def test_config5_full_size_sampled(gpu_lib):
     compare_sampled_device(M, M, rp, col, val, sample_rows(M, M, n_top=100, n_uniform=2000))
     p.close()
     del rp, col, val
+    release_device_memory()
 
 
 def test_identity_and_empty(gpu_lib):
