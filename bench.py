@@ -191,6 +191,9 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--flags", type=int, default=0, help="extra SPGEMM_FLAG_* bits for A/B runs")
+    ap.add_argument("--chunk-width", type=int, default=0, help="planner override W (A/B runs)")
+    ap.add_argument("--tau", type=int, default=0, help="planner override tau (A/B runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -215,7 +218,9 @@ def main():
     dA = sg.DeviceCSR.from_host(A)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
-    timing = sg.options(flags=sg.binding.FLAG_TIMING)
+    timing = sg.options(flags=sg.binding.FLAG_TIMING | args.flags, chunk_width=args.chunk_width, tau=args.tau)
+    plain = (sg.options(flags=args.flags, chunk_width=args.chunk_width, tau=args.tau)
+             if (args.flags or args.chunk_width or args.tau) else None)
 
     def step(opts=None, keep=False):
         p = sg.Product(dA, dA, stream=stream, opts=opts)
@@ -228,7 +233,7 @@ def main():
         return out
 
     for _ in range(args.warmup):
-        (st, _), _c = step(keep=True)
+        (st, _), _c = step(plain, keep=True)
         del _c
     torch.cuda.synchronize()
 

@@ -236,11 +236,15 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr) {
   launch_offset_copy(h->d_heavy_pre + hb.h0, R + 1, h->heavy_pre[hb.h0], c_rowptr, h->st);
   launch_copy_i64(c_rowptr, cursor, R, h->st);
   tcsc.reset();
+  int2* part;
+  SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(hb.elems, kOpTile)));
+  launch_partition(slice_off, kc, hb.elems, kOpTile, part, h->st);
   {
     PhaseTimer t(h, 3);
-    launch_outer_product(colptr, csc_row, csc_val, slice_off, kc, hb.elems, h->B, cursor, h->d_chat_col,
+    launch_outer_product(colptr, csc_row, csc_val, slice_off, part, hb.elems, h->B, cursor, h->d_chat_col,
                          vals ? h->d_chat_val : nullptr, vals, h->d_err, h->st);
   }
+  ws_free(h, part);
   ws_free(h, colcnt);
   ws_free(h, colptr);
   ws_free(h, slice_off);
@@ -320,9 +324,14 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
     const int32_t* in_col = h->d_chat_col + in_half * cap;
     const double* in_val = h->d_chat_val ? h->d_chat_val + in_half * cap : nullptr;
+    const bool match = !(h->opt.flags & SPGEMM_FLAG_NO_MATCH);
+    int2* part;
+    SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(total_in, kMsTile)));
+    launch_partition(in_ptr, nin, total_in, kMsTile, part, h->st);
     {
       PhaseTimer t(h, 4);
-      launch_histogram(in_ptr, nin, total_in, in_col, shift, v, P.group_rows, counts, h->d_err, h->st);
+      launch_histogram(in_ptr, part, total_in, in_col, shift, v, P.group_rows, counts, match, h->sms, h->d_err,
+                       h->st);
     }
     if (!last) {
       // ThreshPartition of the chunks: heavy (count > tau) first, stable
@@ -364,10 +373,11 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     const int64_t out_half = 1 - in_half;
     {
       PhaseTimer t(h, 5);
-      launch_multisplit(in_ptr, nin, total_in, in_col, in_val, shift, v, P.group_rows, xmap, cursor,
-                        h->d_chat_col + out_half * cap, vals ? h->d_chat_val + out_half * cap : nullptr, vals,
-                        h->d_err, h->st);
+      launch_multisplit(in_ptr, part, total_in, in_col, in_val, shift, v, P.group_rows, xmap, cursor,
+                        h->d_chat_col + out_half * cap, vals ? h->d_chat_val + out_half * cap : nullptr, vals, match,
+                        h->sms, h->d_err, h->st);
     }
+    ws_free(h, part);
     ws_free(h, cursor);
     ws_free(h, counts);
     if (xmap) ws_free(h, xmap);
@@ -725,7 +735,7 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
         h->batches.push_back(b);
         i = j;
       }
-      h->batch_cap = maxb;
+      h->batch_cap = (maxb + 15) / 16 * 16;  // keeps both halves of the C^ buffer 16-byte aligned
       h->resident = h->batches.size() == 1 && !(h->opt.flags & SPGEMM_FLAG_RECOMPUTE);
       h->stats.heavy_batches = static_cast<int64_t>(h->batches.size());
       h->stats.chat_bytes = maxb * 12;

@@ -118,24 +118,24 @@ void launch_slice_sizes(const int32_t* colcnt, const spgemm_csr& B, int64_t kcol
 void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows,
                         int64_t* cursor, int32_t* csc_row, double* csc_val, cudaStream_t s);
 void launch_copy_i64(const int64_t* src, int64_t* dst, int64_t n, cudaStream_t s);
+void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t tile, int2* part, cudaStream_t s);
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
-                          const int64_t* slice_off, int64_t kcols, int64_t total,
-                          const spgemm_csr& B, int64_t* row_cursor, int32_t* chat_col,
-                          double* chat_val, bool with_vals, uint32_t* err, cudaStream_t s);
-void launch_histogram(const int64_t* row_ptr, int64_t nrows, int64_t total, const int32_t* col,
-                      int shift, int64_t nchunks, int64_t group_rows,
-                      unsigned long long* counts, uint32_t* err, cudaStream_t s);
+                          const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
+                          int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
+                          uint32_t* err, cudaStream_t s);
+void launch_histogram(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* col, int shift,
+                      int64_t nchunks, int64_t group_rows, unsigned long long* counts, bool match, int sms,
+                      uint32_t* err, cudaStream_t s);
 void launch_chunk_partition(const unsigned long long* counts, int64_t n, int64_t tau,
                             uint8_t* bin, cudaStream_t s);
 void launch_reord_meta(const unsigned long long* counts, int64_t nrows_in, int64_t nchunks,
                        const int32_t* xmap, const int32_t* in_row, const int32_t* in_base,
                        int64_t width, int64_t* reord_cnt, int32_t* out_row, int32_t* out_base,
                        cudaStream_t s);
-void launch_multisplit(const int64_t* row_ptr, int64_t nrows, int64_t total,
-                       const int32_t* in_col, const double* in_val, int shift, int64_t nchunks,
-                       int64_t group_rows, const int32_t* xmap, unsigned long long* reord_cursor,
-                       int32_t* out_col, double* out_val, bool with_vals, uint32_t* err,
-                       cudaStream_t s);
+void launch_multisplit(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
+                       const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
+                       unsigned long long* reord_cursor, int32_t* out_col, double* out_val, bool with_vals, bool match,
+                       int sms, uint32_t* err, cudaStream_t s);
 void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t elem_base,
                        const int32_t* row, const int32_t* base, int64_t* f_start, int64_t* f_cnt,
                        int32_t* f_row, int32_t* f_base, cudaStream_t s);

@@ -224,6 +224,89 @@ __device__ __forceinline__ int64_t expand_chunk(const Group<WARP>& g, const Smem
 }
 
 // ---- outputs -----------------------------------------------------------------------------
+// Ordered write of the `n` compacted entries [0, n) of a block's hash table without sorting:
+// the unused part of the table becomes a column bitmap (keys region: bit words, values
+// region: their exclusive prefix) covering a window of 32 * (slots - n) columns; the window
+// slides over the row's column range [lo, hi], and an entry's output position is the number
+// of set bits below its column.  slots >= 2n, so every window covers at least 32n columns.
+__device__ void block_rank_emit(const Group<false>& g, const Smem& s, int64_t slots, int64_t n, int64_t expected,
+                                int32_t col_base, int32_t* c_col, double* c_val, uint32_t* err) {
+  if (n != expected) {
+    if (g.lane == 0) set_error(err, kErrRowOverflow);
+    return;
+  }
+  if (n == 0) return;
+  int32_t lo = 0x7fffffff, hi = -1;
+  for (int64_t i = g.lane; i < n; i += g.size) {
+    lo = min(lo, s.keys[i]);
+    hi = max(hi, s.keys[i]);
+  }
+  // block min / max through the scan scratch
+  for (int d = 16; d > 0; d >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, d));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, d));
+  }
+  int32_t* red = reinterpret_cast<int32_t*>(s.tmp);
+  if (lane_id() == 0) {
+    red[2 * (threadIdx.x >> 5)] = lo;
+    red[2 * (threadIdx.x >> 5) + 1] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int nw = (blockDim.x + 31) >> 5;
+    int32_t a = threadIdx.x < nw ? red[2 * threadIdx.x] : 0x7fffffff;
+    int32_t b = threadIdx.x < nw ? red[2 * threadIdx.x + 1] : -1;
+    for (int d = 16; d > 0; d >>= 1) {
+      a = min(a, __shfl_xor_sync(0xffffffffu, a, d));
+      b = max(b, __shfl_xor_sync(0xffffffffu, b, d));
+    }
+    if (threadIdx.x == 0) {
+      red[64] = a;
+      red[65] = b;
+    }
+  }
+  __syncthreads();
+  lo = red[64];
+  hi = red[65];
+  __syncthreads();
+  uint32_t* bits = reinterpret_cast<uint32_t*>(s.keys + n);        // slots - n words
+  int32_t* pre = reinterpret_cast<int32_t*>(s.vals + n);           // 2 (slots - n) words available
+  const int64_t nw_max = slots - n;
+  int64_t base = 0;
+  for (int64_t ws = lo; ws <= hi; ws += 32 * nw_max) {
+    const int64_t nwin = min(nw_max, (static_cast<int64_t>(hi) - ws) / 32 + 1);
+    for (int64_t w = g.lane; w < nwin; w += g.size) bits[w] = 0u;
+    __syncthreads();
+    for (int64_t i = g.lane; i < n; i += g.size) {
+      const int64_t c = static_cast<int64_t>(s.keys[i]) - ws;
+      if (c >= 0 && c < 32 * nwin) atomicOr(&bits[c >> 5], 1u << (c & 31));
+    }
+    __syncthreads();
+    int64_t run = 0;
+    for (int64_t w0 = 0; w0 < nwin; w0 += g.size) {
+      const int64_t w = w0 + g.lane;
+      const int64_t cnt = w < nwin ? __popc(bits[w]) : 0;
+      int64_t tot;
+      const int64_t incl = block_incl_scan(cnt, s.tmp, &tot);
+      if (w < nwin) pre[w] = static_cast<int32_t>(run + incl - cnt);
+      run += tot;
+    }
+    __syncthreads();
+    for (int64_t i = g.lane; i < n; i += g.size) {
+      const int32_t k = s.keys[i];
+      const int64_t c = static_cast<int64_t>(k) - ws;
+      if (c >= 0 && c < 32 * nwin) {
+        const uint32_t word = bits[c >> 5];
+        const int64_t r = base + pre[c >> 5] + __popc(word & ((1u << (c & 31)) - 1u));
+        c_col[r] = k + col_base;
+        c_val[r] = s.vals[i];
+      }
+    }
+    base += run;
+    __syncthreads();
+  }
+}
+
 // Sorted write of a hash table holding `n` entries: compact in place (rounds over the
 // slots; every entry moves to a lower or equal slot), bitonic sort of the first 2^ceil(log2 n)
 // slots, then a coalesced write.
@@ -251,6 +334,10 @@ __device__ void hash_emit(const Group<WARP>& g, const Smem& s, int64_t slots, in
     }
     written += total;
     g.sync();
+  }
+  if constexpr (!WARP) {
+    block_rank_emit(g, s, slots, n, expected, col_base, c_col, c_val, err);
+    return;
   }
   int64_t P = 1;
   while (P < n) P <<= 1;

@@ -11,6 +11,8 @@
 //                      permute in shared memory, coalesced write with the column shifted into
 //                      the chunk's local range.
 // plus the bookkeeping that turns the final chunks into offsets inside the rows of C.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace sg {
@@ -103,42 +105,60 @@ void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t 
       csc_row, csc_val);
 }
 
+// ---- static partition of a flattened index space (GroupRange + Search, Algorithms 4 and 5) -----
+// For every block b covering [b*tile, min(total, (b+1)*tile)): the index of the segment (row of
+// C^, or slice of the outer product) holding its first and its last element, found by one
+// thread per block boundary in parallel, so no block starts with a serial search.
+__global__ void k_partition(const int64_t* __restrict__ off, int64_t nseg, int64_t total, int64_t tile,
+                            int64_t nblk, int2* __restrict__ part) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const int64_t g0 = b * tile;
+  const int64_t g1 = min(total, g0 + tile);
+  const int64_t s0 = upper_bound_minus1(off, 0, nseg + 1, g0);
+  const int64_t s1 = upper_bound_minus1(off, s0, nseg + 1, g1 - 1);
+  part[b] = make_int2(static_cast<int>(s0), static_cast<int>(s1));
+}
+void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t tile, int2* part, cudaStream_t s) {
+  const int64_t nblk = ceil_div(total, tile);
+  if (nblk == 0) return;
+  note_launch();
+  k_partition<<<static_cast<unsigned>(ceil_div(nblk, 256)), 256, 0, s>>>(off, nseg, total, tile, nblk, part);
+}
+
 // ---- outer product (Algorithm 4) ---------------------------------------------------------------
 struct OpSmem {
-  int64_t s0, s1, a_first, nent;
+  int64_t a_first, nent;
 };
 
 template <bool VALS>
 __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     const int64_t* __restrict__ colptr, const int32_t* __restrict__ crow, const double* __restrict__ cval,
-    const int64_t* __restrict__ slice_off, int64_t kcols, int64_t total, const int64_t* __restrict__ brp,
-    const int32_t* __restrict__ bcol, const double* __restrict__ bval, unsigned long long* __restrict__ cursor,
-    int32_t* __restrict__ out_col, double* __restrict__ out_val, uint32_t* err) {
+    const int64_t* __restrict__ slice_off, const int2* __restrict__ part, int64_t total,
+    const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol, const double* __restrict__ bval,
+    unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col, double* __restrict__ out_val,
+    uint32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
   __shared__ OpSmem hdr;
   int64_t* dst_delta = reinterpret_cast<int64_t*>(smem_raw);
   int64_t* src_delta = dst_delta + kOpTile;
-  double* a_val = reinterpret_cast<double*>(src_delta + kOpTile);
-  int32_t* seg_start = reinterpret_cast<int32_t*>(a_val + kOpTile);
+  int32_t* seg_start = reinterpret_cast<int32_t*>(src_delta + kOpTile);
 
   const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kOpTile;
   const int64_t g1 = min(total, g0 + kOpTile);
+  const int2 sp = part[blockIdx.x];
+  const int64_t s0 = sp.x, s1 = sp.y;
   if (threadIdx.x == 0) {
-    // GroupRange + Search: the slices holding the first and the last element of this block
-    const int64_t s0 = upper_bound_minus1(slice_off, 0, kcols + 1, g0);
-    const int64_t s1 = upper_bound_minus1(slice_off, s0, kcols + 1, g1 - 1);
+    // ARange (GetAEntry, Eq. 3): first and last entry of A~_CSC touched by this block
     const int64_t len0 = brp[s0 + 1] - brp[s0];
     const int64_t len1 = brp[s1 + 1] - brp[s1];
-    // ARange (GetAEntry, Eq. 3): first and last entry of A~_CSC touched by this block
     const int64_t a_first = colptr[s0] + (g0 - slice_off[s0]) / len0;
     const int64_t a_last = colptr[s1] + (g1 - 1 - slice_off[s1]) / len1;
-    hdr.s0 = s0;
-    hdr.s1 = s1;
     hdr.a_first = a_first;
     hdr.nent = a_last - a_first + 1;
   }
   __syncthreads();
-  const int64_t s0 = hdr.s0, s1 = hdr.s1, a_first = hdr.a_first, nent = hdr.nent;
+  const int64_t a_first = hdr.a_first, nent = hdr.nent;
   if (nent > kOpTile || nent <= 0) {  // impossible for consistent offsets
     if (threadIdx.x == 0) set_error(err, kErrBounds);
     return;
@@ -147,7 +167,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
   // partial B rows at both ends of the block's range).
   for (int64_t e = threadIdx.x; e < nent; e += blockDim.x) {
     const int64_t a = a_first + e;
-    const int64_t s = upper_bound_minus1(colptr, s0, s1 + 1, a);
+    const int64_t s = (s0 == s1) ? s0 : upper_bound_minus1(colptr, s0, s1 + 1, a);
     const int64_t b0 = brp[s];
     const int64_t len = brp[s + 1] - b0;
     const int64_t F = slice_off[s] + (a - colptr[s]) * len;
@@ -159,7 +179,6 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     seg_start[e] = static_cast<int32_t>(clo - g0);
     dst_delta[e] = base - (clo - g0);
     src_delta[e] = b0 + (clo - F) - (clo - g0);
-    a_val[e] = VALS ? cval[a] : 0.0;
   }
   __syncthreads();
   // Step 3: populate C^, consecutive threads -> consecutive elements of a B row
@@ -180,240 +199,312 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     const int64_t src = src_delta[e] + p;
     const int64_t dst = dst_delta[e] + p;
     out_col[dst] = bcol[src];
-    if (VALS) out_val[dst] = a_val[e] * bval[src];
+    if (VALS) out_val[dst] = __ldg(&cval[a_first + e]) * bval[src];
   }
 }
 
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
-                          const int64_t* slice_off, int64_t kcols, int64_t total, const spgemm_csr& B,
+                          const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
                           int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
                           uint32_t* err, cudaStream_t s) {
   if (total == 0) return;
-  const size_t smem = kOpTile * (8 + 8 + 8 + 4);
+  const size_t smem = kOpTile * (8 + 8 + 4);
   const unsigned grid = static_cast<unsigned>(ceil_div(total, kOpTile));
   auto* ull = reinterpret_cast<unsigned long long*>(row_cursor);
   if (with_vals) {
     cudaFuncSetAttribute(k_outer_product<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     note_launch();
-    k_outer_product<true><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, kcols, total,
-                                                         B.row_ptr, B.col_idx, B.vals, ull, chat_col,
-                                                         chat_val, err);
+    k_outer_product<true><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,
+                                                         B.row_ptr, B.col_idx, B.vals, ull, chat_col, chat_val,
+                                                         err);
   } else {
     cudaFuncSetAttribute(k_outer_product<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     note_launch();
-    k_outer_product<false><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, kcols, total,
-                                                          B.row_ptr, B.col_idx, B.vals, ull, chat_col,
-                                                          nullptr, err);
+    k_outer_product<false><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,
+                                                          B.row_ptr, B.col_idx, B.vals, ull, chat_col, nullptr,
+                                                          err);
   }
 }
 
 // ---- histogram and multisplit (Algorithm 5) -----------------------------------------------------
+// Both kernels use the same static partition: block b owns elements [b*kMsTile, (b+1)*kMsTile),
+// each thread 8 consecutive ones (loaded as 16-byte vectors when the tile is full), and the rows
+// of C^ the tile touches (at most group_rows when every row holds more than tau elements;
+// processed in windows of group_rows rows otherwise).
 constexpr int kMsItems = static_cast<int>(kMsTile) / kMsThreads;  // 8 per thread
 
-// Row window of one block: rows [r0, r0 + nr) intersect elements [e0, e1).
-struct MsHdr {
-  int64_t r0, r_last;
-};
-
-__device__ __forceinline__ int find_local_row(const int64_t* rstart, int nr, int64_t pos) {
-  int lo = 0, hi = nr - 1;  // last local row with rstart <= pos
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (rstart[mid] <= pos) lo = mid; else hi = mid - 1;
+template <bool VALS>
+__device__ __forceinline__ void ms_load_tile(const int32_t* __restrict__ col, const double* __restrict__ val,
+                                             int64_t p0, int64_t g1, int32_t (&c)[kMsItems],
+                                             double (&v)[kMsItems]) {
+  if (p0 + kMsItems <= g1) {
+    const int4 x = __ldcs(reinterpret_cast<const int4*>(col + p0));
+    const int4 y = __ldcs(reinterpret_cast<const int4*>(col + p0 + 4));
+    c[0] = x.x; c[1] = x.y; c[2] = x.z; c[3] = x.w;
+    c[4] = y.x; c[5] = y.y; c[6] = y.z; c[7] = y.w;
+    if (VALS) {
+#pragma unroll
+      for (int j = 0; j < kMsItems; j += 2) {
+        const double2 d = __ldcs(reinterpret_cast<const double2*>(val + p0 + j));
+        v[j] = d.x;
+        v[j + 1] = d.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMsItems; ++j) {
+      c[j] = (p0 + j < g1) ? col[p0 + j] : 0;
+      if (VALS) v[j] = (p0 + j < g1) ? val[p0 + j] : 0.0;
+    }
   }
-  return lo;
 }
 
-__global__ void __launch_bounds__(kMsThreads) k_histogram(const int64_t* __restrict__ rp, int64_t nrows,
-                                                         int64_t total, const int32_t* __restrict__ col,
+// Bins (local row * v + chunk) of a thread's 8 consecutive elements inside row window
+// [rstart[0], rstart[nr]); -1 outside the tile or the window.
+__device__ __forceinline__ void ms_bins(const int64_t* rstart, int nr, int64_t p0, int64_t g1,
+                                        const int32_t (&c)[kMsItems], int shift, int64_t v, int (&bin)[kMsItems],
+                                        uint32_t* err) {
+  int r = 0;
+  while (r + 1 < nr && p0 >= rstart[r + 1]) ++r;
+#pragma unroll
+  for (int j = 0; j < kMsItems; ++j) {
+    const int64_t p = p0 + j;
+    while (r + 1 < nr && p >= rstart[r + 1]) ++r;
+    int b = -1;
+    if (p < g1 && p >= rstart[0] && p < rstart[nr]) {
+      const int64_t ch = static_cast<int64_t>(c[j]) >> shift;
+      if (ch < v) b = static_cast<int>(r * v + ch);
+      else set_error(err, kErrBounds);
+    }
+    bin[j] = b;
+  }
+}
+
+template <bool MATCH>
+__device__ __forceinline__ void ms_count(unsigned* hist, int b) {
+  if (MATCH) {
+    // warp-aggregated: one shared-memory atomic per distinct bin per warp
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    if (b >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[b], __popc(peers));
+  } else if (b >= 0) {
+    atomicAdd(&hist[b], 1u);
+  }
+}
+
+template <bool MATCH>
+__global__ void __launch_bounds__(kMsThreads) k_histogram(const int64_t* __restrict__ rp, const int2* __restrict__ part,
+                                                         int64_t total, int64_t ntiles, const int32_t* __restrict__ col,
                                                          int shift, int64_t v, int64_t gr,
                                                          unsigned long long* __restrict__ counts, uint32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
-  __shared__ MsHdr hdr;
-  int64_t* rstart = reinterpret_cast<int64_t*>(smem_raw);  // gr + 1
+  int64_t* rstart = reinterpret_cast<int64_t*>(smem_raw);         // gr + 1
   unsigned* hist = reinterpret_cast<unsigned*>(rstart + gr + 1);  // gr * v
-  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kMsTile;
-  const int64_t g1 = min(total, g0 + kMsTile);
-  if (threadIdx.x == 0) {
-    hdr.r0 = upper_bound_minus1(rp, 0, nrows + 1, g0);
-    hdr.r_last = upper_bound_minus1(rp, hdr.r0, nrows + 1, g1 - 1);
-  }
-  __syncthreads();
-  const int64_t rfirst = hdr.r0, rlast = hdr.r_last;
-  for (int64_t w0 = rfirst; w0 <= rlast; w0 += gr) {  // windows of at most gr rows
-    const int nr = static_cast<int>(min(gr, rlast - w0 + 1));
-    const int64_t e0 = max(g0, rp[w0]);
-    const int64_t e1 = min(g1, rp[w0 + nr]);
-    for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
-    for (int64_t i = threadIdx.x; i < nr * v; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
+  // persistent blocks: tile t, then t + gridDim.x, ...; the next tile is loaded while the
+  // current one is counted
+  int64_t t = blockIdx.x;
+  if (t >= ntiles) return;
+  int32_t c[kMsItems], cn[kMsItems];
+  double unused[kMsItems];
+  ms_load_tile<false>(col, nullptr, t * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
+                      min(total, (t + 1) * kMsTile), c, unused);
+  int2 pr = part[t];
+  for (; t < ntiles; t += gridDim.x) {
+    const int64_t g0 = t * kMsTile;
+    const int64_t g1 = min(total, g0 + kMsTile);
+    const int64_t p0 = g0 + static_cast<int64_t>(threadIdx.x) * kMsItems;
+    const int64_t tn = t + gridDim.x;
+    int2 prn = pr;
+    if (tn < ntiles) {
+      ms_load_tile<false>(col, nullptr, tn * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
+                          min(total, (tn + 1) * kMsTile), cn, unused);
+      prn = part[tn];
+    }
+    for (int64_t w0 = pr.x; w0 <= pr.y; w0 += gr) {  // windows of at most gr rows
+      const int nr = static_cast<int>(min(gr, static_cast<int64_t>(pr.y) - w0 + 1));
+      for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
+      for (int64_t i = threadIdx.x; i < nr * v; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      int bin[kMsItems];
+      ms_bins(rstart, nr, p0, g1, c, shift, v, bin, err);
 #pragma unroll
-    for (int j = 0; j < kMsItems; ++j) {
-      const int64_t p = e0 + j * kMsThreads + threadIdx.x;
-      int bin = -1;
-      if (p < e1) {
-        const int r = find_local_row(rstart, nr, p);
-        const int64_t c = static_cast<int64_t>(col[p]) >> shift;
-        if (c < v) bin = static_cast<int>(r * v + c);
-        else set_error(err, kErrBounds);
+      for (int j = 0; j < kMsItems; ++j) ms_count<MATCH>(hist, bin[j]);
+      __syncthreads();
+      for (int64_t b = threadIdx.x; b < nr * v; b += blockDim.x) {
+        const unsigned h = hist[b];
+        if (h) atomicAdd(&counts[(w0 + b / v) * v + (b % v)], static_cast<unsigned long long>(h));
       }
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[bin], __popc(peers));
+      __syncthreads();
     }
-    __syncthreads();
-    for (int64_t b = threadIdx.x; b < nr * v; b += blockDim.x) {
-      const unsigned h = hist[b];
-      if (h) atomicAdd(&counts[(w0 + b / v) * v + (b % v)], static_cast<unsigned long long>(h));
-    }
-    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMsItems; ++j) c[j] = cn[j];
+    pr = prn;
   }
 }
 
-void launch_histogram(const int64_t* row_ptr, int64_t nrows, int64_t total, const int32_t* col, int shift,
-                      int64_t nchunks, int64_t group_rows, unsigned long long* counts, uint32_t* err,
-                      cudaStream_t s) {
+void launch_histogram(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* col, int shift,
+                      int64_t nchunks, int64_t group_rows, unsigned long long* counts, bool match, int sms,
+                      uint32_t* err, cudaStream_t s) {
   if (total == 0) return;
   const size_t smem = (group_rows + 1) * 8 + group_rows * nchunks * 4;
-  cudaFuncSetAttribute(k_histogram, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  note_launch();
-  k_histogram<<<static_cast<unsigned>(ceil_div(total, kMsTile)), kMsThreads, smem, s>>>(
-      row_ptr, nrows, total, col, shift, nchunks, group_rows, counts, err);
+  const int64_t ntiles = ceil_div(total, kMsTile);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * 4));
+  if (match) {
+    cudaFuncSetAttribute(k_histogram<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    note_launch();
+    k_histogram<true><<<grid, kMsThreads, smem, s>>>(row_ptr, part, total, ntiles, col, shift, nchunks, group_rows,
+                                                     counts, err);
+  } else {
+    cudaFuncSetAttribute(k_histogram<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    note_launch();
+    k_histogram<false><<<grid, kMsThreads, smem, s>>>(row_ptr, part, total, ntiles, col, shift, nchunks, group_rows,
+                                                      counts, err);
+  }
 }
 
-template <bool VALS>
+template <bool VALS, bool MATCH>
 __global__ void __launch_bounds__(kMsThreads) k_multisplit(
-    const int64_t* __restrict__ rp, int64_t nrows, int64_t total, const int32_t* __restrict__ in_col,
-    const double* __restrict__ in_val, int shift, int64_t v, int64_t gr, const int32_t* __restrict__ xmap,
-    unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col, double* __restrict__ out_val,
-    uint32_t* err) {
+    const int64_t* __restrict__ rp, const int2* __restrict__ part, int64_t total, int64_t ntiles,
+    const int32_t* __restrict__ in_col, const double* __restrict__ in_val, int shift, int64_t v, int64_t gr,
+    const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
+    double* __restrict__ out_val, uint32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
-  __shared__ MsHdr hdr;
   __shared__ unsigned scan_tmp[33];
-  double* val_buf = reinterpret_cast<double*>(smem_raw);                       // kMsTile
-  unsigned long long* goff = reinterpret_cast<unsigned long long*>(val_buf + kMsTile);  // gr*v
-  int64_t* rstart = reinterpret_cast<int64_t*>(goff + gr * v);                 // gr + 1
-  int32_t* col_buf = reinterpret_cast<int32_t*>(rstart + gr + 1);             // kMsTile
-  unsigned* hist = reinterpret_cast<unsigned*>(col_buf + kMsTile);             // gr*v (count, then cursor)
-  unsigned* loff = hist + gr * v;                                              // gr*v + 1
-  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kMsTile;
-  const int64_t g1 = min(total, g0 + kMsTile);
-  if (threadIdx.x == 0) {
-    hdr.r0 = upper_bound_minus1(rp, 0, nrows + 1, g0);
-    hdr.r_last = upper_bound_minus1(rp, hdr.r0, nrows + 1, g1 - 1);
-  }
-  __syncthreads();
-  const int64_t rfirst = hdr.r0, rlast = hdr.r_last;
+  double* val_buf = reinterpret_cast<double*>(smem_raw);                                  // kMsTile
+  unsigned long long* goff = reinterpret_cast<unsigned long long*>(val_buf + kMsTile);    // gr*v
+  int64_t* rstart = reinterpret_cast<int64_t*>(goff + gr * v);                            // gr + 1
+  int32_t* col_buf = reinterpret_cast<int32_t*>(rstart + gr + 1);                        // kMsTile
+  unsigned* hist = reinterpret_cast<unsigned*>(col_buf + kMsTile);                        // gr*v: count, then cursor
+  unsigned* loff = hist + gr * v;                                                         // gr*v + 1
   const int64_t wmask = (int64_t(1) << shift) - 1;
-  for (int64_t w0 = rfirst; w0 <= rlast; w0 += gr) {
-    const int nr = static_cast<int>(min(gr, rlast - w0 + 1));
-    const int64_t e0 = max(g0, rp[w0]);
-    const int64_t e1 = min(g1, rp[w0 + nr]);
-    const int nbins = static_cast<int>(nr * v);
-    for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
-    for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    // load the tile into registers and build the local histogram
-    int32_t c_reg[kMsItems];
-    double v_reg[kMsItems];
-    int bin_reg[kMsItems];
+  int64_t t = blockIdx.x;
+  if (t >= ntiles) return;
+  int32_t c[kMsItems];
+  double vv[kMsItems];
+  ms_load_tile<VALS>(in_col, in_val, t * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
+                     min(total, (t + 1) * kMsTile), c, vv);
+  int2 pr = part[t];
+  for (; t < ntiles; t += gridDim.x) {
+    const int64_t g0 = t * kMsTile;
+    const int64_t g1 = min(total, g0 + kMsTile);
+    const int64_t p0 = g0 + static_cast<int64_t>(threadIdx.x) * kMsItems;
+    const int64_t tn = t + gridDim.x;
+    for (int64_t w0 = pr.x; w0 <= pr.y; w0 += gr) {
+      const int nr = static_cast<int>(min(gr, static_cast<int64_t>(pr.y) - w0 + 1));
+      const int nbins = static_cast<int>(nr * v);
+      for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
+      for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      int bin[kMsItems];
+      ms_bins(rstart, nr, p0, g1, c, shift, v, bin, err);
 #pragma unroll
-    for (int j = 0; j < kMsItems; ++j) {
-      const int64_t p = e0 + j * kMsThreads + threadIdx.x;
-      int bin = -1;
-      c_reg[j] = 0;
-      v_reg[j] = 0.0;
-      if (p < e1) {
-        c_reg[j] = in_col[p];
-        if (VALS) v_reg[j] = in_val[p];
-        const int r = find_local_row(rstart, nr, p);
-        const int64_t c = static_cast<int64_t>(c_reg[j]) >> shift;
-        if (c < v) bin = static_cast<int>(r * v + c);
-        else set_error(err, kErrBounds);
-      }
-      bin_reg[j] = bin;
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[bin], __popc(peers));
-    }
-    __syncthreads();
-    // local offsets (exclusive scan of the histogram) and global reservations
-    {
-      const int per = (nbins + kMsThreads - 1) / kMsThreads;
-      const int b0 = threadIdx.x * per;
-      unsigned local = 0;
-      for (int b = b0; b < min(nbins, b0 + per); ++b) local += hist[b];
-      unsigned tot;
-      const unsigned incl = block_incl_scan(local, scan_tmp, &tot);
-      unsigned run = incl - local;
-      for (int b = b0; b < min(nbins, b0 + per); ++b) {
-        const unsigned h = hist[b];
-        loff[b] = run;
-        if (h) {
-          const int64_t gchunk = (w0 + b / v) * v + (b % v);
-          const int64_t q = xmap ? xmap[gchunk] : gchunk;
-          goff[b] = atomicAdd(&cursor[q], static_cast<unsigned long long>(h));
-        }
-        hist[b] = run;  // becomes the permute cursor
-        run += h;
-      }
-      if (threadIdx.x == 0) loff[nbins] = tot;
-    }
-    __syncthreads();
-    // permute into shared memory, grouped by (row, chunk)
-#pragma unroll
-    for (int j = 0; j < kMsItems; ++j) {
-      const int bin = bin_reg[j];
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      const int leader = __ffs(peers) - 1;
-      unsigned base = 0;
-      if (bin >= 0 && static_cast<int>(lane_id()) == leader) base = atomicAdd(&hist[bin], __popc(peers));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      if (bin >= 0) {
-        const unsigned pos = base + __popc(peers & lanemask_lt());
-        col_buf[pos] = c_reg[j];
-        if (VALS) val_buf[pos] = v_reg[j];
-      }
-    }
-    __syncthreads();
-    // coalesced write: runs of one local chunk go to consecutive global positions
-    const int cnt = static_cast<int>(e1 - e0);
-    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-      const int32_t c = col_buf[i];
-      int r = 0;
+      for (int j = 0; j < kMsItems; ++j) ms_count<MATCH>(hist, bin[j]);
+      __syncthreads();
+      // local offsets (exclusive scan of the histogram) and one global reservation per bin
       {
-        int lo = 0, hi = nr - 1;  // last row whose first bin starts at or before i
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (static_cast<int>(loff[mid * v]) <= i) lo = mid; else hi = mid - 1;
+        const int per = (nbins + kMsThreads - 1) / kMsThreads;
+        const int b0 = threadIdx.x * per;
+        unsigned local = 0;
+        for (int b = b0; b < min(nbins, b0 + per); ++b) local += hist[b];
+        unsigned tot;
+        const unsigned incl = block_incl_scan(local, scan_tmp, &tot);
+        unsigned run = incl - local;
+        for (int b = b0; b < min(nbins, b0 + per); ++b) {
+          const unsigned h = hist[b];
+          loff[b] = run;
+          if (h) {
+            const int64_t gchunk = (w0 + b / v) * v + (b % v);
+            const int64_t q = xmap ? xmap[gchunk] : gchunk;
+            goff[b] = atomicAdd(&cursor[q], static_cast<unsigned long long>(h));
+          }
+          hist[b] = run;  // becomes the permute cursor
+          run += h;
         }
-        r = lo;
+        if (threadIdx.x == 0) loff[nbins] = tot;
       }
-      const int b = static_cast<int>(r * v + (static_cast<int64_t>(c) >> shift));
-      const int64_t dst = static_cast<int64_t>(goff[b]) + (i - static_cast<int>(loff[b]));
-      out_col[dst] = static_cast<int32_t>(c & wmask);
-      if (VALS) out_val[dst] = val_buf[i];
+      __syncthreads();
+      // permute into shared memory, grouped by (row, chunk); order inside a chunk is free
+#pragma unroll
+      for (int j = 0; j < kMsItems; ++j) {
+        const int b = bin[j];
+        unsigned pos = 0;
+        if (MATCH) {
+          const uint32_t peers = __match_any_sync(0xffffffffu, b);
+          const int leader = __ffs(peers) - 1;
+          unsigned base = 0;
+          if (b >= 0 && static_cast<int>(lane_id()) == leader) base = atomicAdd(&hist[b], __popc(peers));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          pos = base + __popc(peers & lanemask_lt());
+        } else if (b >= 0) {
+          pos = atomicAdd(&hist[b], 1u);
+        }
+        if (b >= 0) {
+          col_buf[pos] = c[j];
+          if (VALS) val_buf[pos] = vv[j];
+        }
+      }
+      __syncthreads();
+      // the registers are free again: start loading the next tile, then write this one out
+      if (w0 + gr > pr.y && tn < ntiles)
+        ms_load_tile<VALS>(in_col, in_val, tn * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
+                           min(total, (tn + 1) * kMsTile), c, vv);
+      // coalesced write: runs of one local chunk go to consecutive global positions
+      const int cnt = static_cast<int>(loff[nbins]);
+      for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+        const int32_t cc = col_buf[i];
+        int r = 0;
+        {
+          int lo = 0, hi = nr - 1;  // last row whose first bin starts at or before i
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<int>(loff[mid * v]) <= i) lo = mid; else hi = mid - 1;
+          }
+          r = lo;
+        }
+        const int b = static_cast<int>(r * v + (static_cast<int64_t>(cc) >> shift));
+        const int64_t dst = static_cast<int64_t>(goff[b]) + (i - static_cast<int>(loff[b]));
+        __stcs(&out_col[dst], static_cast<int32_t>(cc & wmask));
+        if (VALS) __stcs(&out_val[dst], val_buf[i]);
+      }
+      __syncthreads();
     }
-    __syncthreads();
+    if (tn < ntiles) pr = part[tn];
   }
 }
 
-void launch_multisplit(const int64_t* row_ptr, int64_t nrows, int64_t total, const int32_t* in_col,
-                       const double* in_val, int shift, int64_t nchunks, int64_t group_rows,
-                       const int32_t* xmap, unsigned long long* reord_cursor, int32_t* out_col,
-                       double* out_val, bool with_vals, uint32_t* err, cudaStream_t s) {
-  if (total == 0) return;
+template <bool VALS, bool MATCH>
+static void ms_launch(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
+                      const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
+                      unsigned long long* cursor, int32_t* out_col, double* out_val, int sms, uint32_t* err,
+                      cudaStream_t s) {
   const int64_t bins = group_rows * nchunks;
   const size_t smem = kMsTile * 8 + bins * 8 + (group_rows + 1) * 8 + kMsTile * 4 + bins * 4 + (bins + 1) * 4;
-  const unsigned grid = static_cast<unsigned>(ceil_div(total, kMsTile));
+  const int64_t ntiles = ceil_div(total, kMsTile);
+  auto kern = k_multisplit<VALS, MATCH>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMsThreads, smem);
+  if (per_sm < 1) per_sm = 1;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * per_sm));
+  note_launch();
+  kern<<<grid, kMsThreads, smem, s>>>(row_ptr, part, total, ntiles, in_col, in_val, shift, nchunks, group_rows, xmap,
+                                      cursor, out_col, out_val, err);
+}
+
+void launch_multisplit(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
+                       const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
+                       unsigned long long* reord_cursor, int32_t* out_col, double* out_val, bool with_vals, bool match,
+                       int sms, uint32_t* err, cudaStream_t s) {
+  if (total == 0) return;
   if (with_vals) {
-    cudaFuncSetAttribute(k_multisplit<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    note_launch();
-    k_multisplit<true><<<grid, kMsThreads, smem, s>>>(row_ptr, nrows, total, in_col, in_val, shift, nchunks,
-                                                      group_rows, xmap, reord_cursor, out_col, out_val, err);
+    if (match) ms_launch<true, true>(row_ptr, part, total, in_col, in_val, shift, nchunks, group_rows, xmap,
+                                     reord_cursor, out_col, out_val, sms, err, s);
+    else ms_launch<true, false>(row_ptr, part, total, in_col, in_val, shift, nchunks, group_rows, xmap,
+                                reord_cursor, out_col, out_val, sms, err, s);
   } else {
-    cudaFuncSetAttribute(k_multisplit<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    note_launch();
-    k_multisplit<false><<<grid, kMsThreads, smem, s>>>(row_ptr, nrows, total, in_col, nullptr, shift, nchunks,
-                                                       group_rows, xmap, reord_cursor, out_col, nullptr, err);
+    if (match) ms_launch<false, true>(row_ptr, part, total, in_col, nullptr, shift, nchunks, group_rows, xmap,
+                                      reord_cursor, out_col, nullptr, sms, err, s);
+    else ms_launch<false, false>(row_ptr, part, total, in_col, nullptr, shift, nchunks, group_rows, xmap,
+                                 reord_cursor, out_col, nullptr, sms, err, s);
   }
 }
 
