@@ -56,8 +56,10 @@ extern "C" {
 #define SPGEMM_FLAG_VALIDATE 8        /* check A and B (row_ptr monotone, columns in range)  */
 #define SPGEMM_FLAG_RECOMPUTE 16      /* never keep C^_reord between symbolic and numeric    */
 #define SPGEMM_FLAG_TIMING 32         /* record device time per phase (CUDA events, no syncs) */
-#define SPGEMM_FLAG_NO_MATCH 64       /* histogram/multisplit: plain shared atomics instead of
+#define SPGEMM_FLAG_NO_MATCH 64       /* multisplit: plain shared atomics instead of
                                          __match_any_sync warp aggregation */
+#define SPGEMM_FLAG_DENSE_L2 128      /* heavy dense chunks sum with L2 reductions into a global
+                                         per-SM array instead of shared-memory atomics */
 
 /* A CSR matrix in device memory, borrowed by the library (never written or freed). */
 typedef struct {

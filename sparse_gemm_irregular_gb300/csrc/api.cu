@@ -122,6 +122,7 @@ namespace {
 
 // Last-level chunk bins: threads per chunk and hash slots (bin 3 is the dense accumulator).
 constexpr int kChunkTpr[4] = {32, 256, 512, 1024};
+constexpr int kChunkSymTpr[4] = {32, 256, 256, 256};  // symbolic: bitmap only, more blocks per SM
 constexpr int64_t kChunkSlots[4] = {512, 2048, 2 * kChunkDenseMin, 0};
 
 // Scan scratch that grows on demand.
@@ -165,16 +166,17 @@ struct PhaseTimer {
   spgemm_ctx* h;
   int slot;
   cudaEvent_t a{};
-  PhaseTimer(spgemm_ctx* hh, int s) : h(hh), slot(s) {
+  cudaStream_t st;
+  PhaseTimer(spgemm_ctx* hh, int s, cudaStream_t stream = nullptr) : h(hh), slot(s), st(stream ? stream : hh->st) {
     if (!h->timing) return;
     cudaEventCreate(&a);
-    cudaEventRecord(a, h->st);
+    cudaEventRecord(a, st);
   }
   ~PhaseTimer() {
     if (!h->timing) return;
     cudaEvent_t b;
     cudaEventCreate(&b);
-    cudaEventRecord(b, h->st);
+    cudaEventRecord(b, st);
     h->timed[slot].push_back({a, b});
   }
 };
@@ -330,7 +332,7 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     launch_partition(in_ptr, nin, total_in, kMsTile, part, h->st);
     {
       PhaseTimer t(h, 4);
-      launch_histogram(in_ptr, part, total_in, in_col, shift, v, P.group_rows, counts, match, h->sms, h->d_err,
+      launch_histogram(in_ptr, part, total_in, in_col, shift, v, P.group_rows, counts, false, h->sms, h->d_err,
                        h->st);
     }
     if (!last) {
@@ -473,7 +475,7 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     for (int j = 0; j < 4; ++j) {        // last-level chunks: bitmaps of width W
       const int b = h->lad.n + j;
       launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
-                          h->plan.chunk_width, 0, 0, kChunkTpr[j], sk, h->d_err, h->st);
+                          h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk, h->d_err, h->d_counter, nullptr, h->st);
     }
   }
   // offsets of the chunks inside their rows
@@ -508,10 +510,13 @@ int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
   for (int L = 0; L < h->lad.n; ++L)
     launch_chunks(cs, hb.f_list + hb.f_bin_start[L], hb.f_bin_start[L + 1] - hb.f_bin_start[L], h->lad.slots[L],
                   h->lad.tpr[L], false, 0, true, sk, h->d_err, h->st);
+  if ((h->opt.flags & SPGEMM_FLAG_DENSE_L2) && !h->d_gacc)
+    SG_ALLOC(h->d_gacc, double, static_cast<int64_t>(h->sms) * h->plan.chunk_width);
   for (int j = 0; j < 4; ++j) {
     const int b = h->lad.n + j;
     launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
-                        h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err, h->st);
+                        h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err,
+                        h->d_counter, h->d_gacc, h->st);
   }
   return SPGEMM_OK;
 }
@@ -520,6 +525,18 @@ int ensure_chat(spgemm_ctx* h, bool vals) {
   if (!h->d_chat_col) SG_ALLOC(h->d_chat_col, int32_t, 2 * h->batch_cap);
   if (vals && !h->d_chat_val) SG_ALLOC(h->d_chat_val, double, 2 * h->batch_cap);
   return SPGEMM_OK;
+}
+
+// Light rows run on their own stream (the paper's light queue) so that they overlap the heavy
+// pipeline on the handle's stream: fork after everything enqueued so far, join before the
+// next dependent step.
+void fork_light(spgemm_ctx* h) {
+  cudaEventRecord(h->ev_fork, h->st);
+  cudaStreamWaitEvent(h->st_light, h->ev_fork, 0);
+}
+void join_light(spgemm_ctx* h) {
+  cudaEventRecord(h->ev_join, h->st_light);
+  cudaStreamWaitEvent(h->st, h->ev_join, 0);
 }
 
 void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
@@ -532,7 +549,7 @@ void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
       job.slots = h->lad.slots[L];
       job.tpr = h->lad.tpr[L];
       job.dense = d == 1;
-      launch_light(h->A, h->B, h->d_span_lo, job, numeric, sk, h->d_err, h->st);
+      launch_light(h->A, h->B, h->d_span_lo, job, numeric, sk, h->d_err, h->st_light);
     }
   }
 }
@@ -548,8 +565,9 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
   sk.c_val = c_val;
   sk.row_begin = rb;
   sk.row_end = re;
+  fork_light(h);
   {
-    PhaseTimer t(h, 10);
+    PhaseTimer t(h, 10, h->st_light);
     light_pass(h, true, sk);
   }
   for (auto& hb : h->batches) {
@@ -566,6 +584,7 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
       SG_TRY(heavy_chunk_numeric(h, hb, sk));
     }
   }
+  join_light(h);
   return sync_and_check(h, "numeric");
 }
 
@@ -644,6 +663,18 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
     return fail(SPGEMM_ERR_OUT_OF_MEMORY);
   }
   cudaMemsetAsync(h->d_err, 0, sizeof(uint32_t), h->st);
+  if (cudaStreamCreateWithFlags(&h->st_light, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    delete tsetup;
+    set_last_error("stream or event creation failed");
+    return fail(SPGEMM_ERR_CUDA);
+  }
+  h->d_counter = static_cast<int*>(ws_alloc(h, sizeof(int)));
+  if (!h->d_counter) {
+    delete tsetup;
+    return fail(SPGEMM_ERR_OUT_OF_MEMORY);
+  }
   auto body = [&]() -> int {
     if (h->opt.flags & SPGEMM_FLAG_VALIDATE) {
       launch_validate(h->A, h->d_err, h->st);
@@ -768,8 +799,9 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
   sk.row_nnz = c_row_ptr;
   sk.row_begin = 0;
   sk.row_end = h->m;
+  fork_light(h);
   {
-    PhaseTimer t(h, 1);
+    PhaseTimer t(h, 1, h->st_light);
     light_pass(h, false, sk);
   }
   int64_t levels = 0, finals = 0, dense = 0;
@@ -786,6 +818,7 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     finals += hb.nfinal;
     dense += hb.f_bin_start[h->lad.n + 4] - hb.f_bin_start[h->lad.n + 3];
   }
+  join_light(h);
   h->stats.levels_run = levels;
   h->stats.final_chunks = finals;
   h->stats.chunks_dense = dense;
@@ -853,9 +886,13 @@ long long spgemm_kernel_launches(void) { return launch_count(); }
 int spgemm_destroy(spgemm_handle h) {
   if (!h) return SPGEMM_OK;
   drain_timers(h);
+  if (h->st_light) cudaStreamSynchronize(h->st_light);
   for (void* p : h->allocs) cudaFreeAsync(p, h->st);
   h->allocs.clear();
   cudaStreamSynchronize(h->st);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->st_light) cudaStreamDestroy(h->st_light);
   delete h;
   return SPGEMM_OK;
 }

@@ -143,7 +143,8 @@ void launch_chunk_classify(const int64_t* f_cnt, int64_t n, int64_t bitmap_from,
                            uint8_t* bin, cudaStream_t s);
 // bitmap-ordered chunk accumulators (k_chunk.cu); mode 0 symbolic, 1 hash numeric, 2 dense numeric
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
-                         int64_t slots, int tpr, const Sink& sink, uint32_t* err, cudaStream_t s);
+                         int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
+                         cudaStream_t s);
 void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s);
 void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s);
 void launch_grid_fill(const int32_t* f_row, const int32_t* f_base, const int64_t* f_nnz, int64_t n,
@@ -188,6 +189,8 @@ struct spgemm_ctx {
   int64_t m = 0, k = 0, n = 0;
   spgemm_csr A{}, B{};
   cudaStream_t st = nullptr;
+  cudaStream_t st_light = nullptr;  // light rows (the heavy pipeline stays on st)
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int device = 0, sms = 0;
   cudaMemPool_t pool = nullptr;
   int64_t smem_optin = 0, l2_bytes = 0;
@@ -203,6 +206,8 @@ struct spgemm_ctx {
   // workspace (device)
   std::vector<void*> allocs;
   uint32_t* d_err = nullptr;
+  int* d_counter = nullptr;     // work counter of the persistent dense accumulator
+  double* d_gacc = nullptr;     // L2-resident dense accumulators (SPGEMM_FLAG_DENSE_L2)
   int64_t* d_scan = nullptr;    // scan scratch
   int64_t scan_cap = 0;
   int64_t* d_ip = nullptr;

@@ -8,11 +8,21 @@
 //              output order comes from the bitmap: the rank of column c inside the chunk is the
 //              number of set bits below c (a block scan over the bitmap words), so no sort is
 //              needed, and each entry is written straight to its final position in C.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace sg {
 
 constexpr int kCkWarpsPerBlock = 8;
+
+// Hub columns of a chunk: the lowest 64 local columns and every power of two above them.  In
+// power-law (R-MAT-like) products these few columns receive a large share of the products of
+// every chunk (local column 0 alone ~2%), so every warp keeps private sums for them instead of
+// contending on one shared-memory address; the private sums are merged once per chunk.
+constexpr int kHubWarps = 32;
+constexpr int kHubSlots = 80;  // 64 low columns + powers of two 2^6 .. 2^15
+
 
 struct CkParams {
   ChunkSet cs;
@@ -50,7 +60,8 @@ __host__ __device__ inline size_t ck_group_bytes(int64_t width, int64_t slots, i
   const int64_t words = (width + 31) / 32;
   size_t b = ck_align(33 * sizeof(int64_t)) + ck_align(words * 4) + ck_align(words * 4);
   if (mode == 1) b += ck_align(slots * 4) + ck_align(slots * 8);  // hash numeric
-  if (mode == 2) b += ck_align(width * 8);                          // dense numeric
+  if (mode == 2) b += ck_align(width * 8) + ck_align(kHubWarps * kHubSlots * 8);  // dense + warp hubs
+  if (mode == 3) b += ck_align(kHubWarps * kHubSlots * 8);                        // hubs only (L2 dense)
   return b;
 }
 
@@ -60,7 +71,14 @@ struct CkSmem {
   int32_t* pre;
   int32_t* keys;
   double* vals;
+  double* hub;   // dense mode: per-warp private sums of the hub columns
 };
+
+__device__ __forceinline__ int hub_index(uint32_t c) {
+  if (c < 64u) return static_cast<int>(c);
+  if ((c & (c - 1u)) == 0u && c < (1u << 16)) return 64 + (__ffs(c) - 1) - 6 + 0;
+  return -1;
+}
 
 __device__ __forceinline__ CkSmem ck_carve(char* p, int64_t width, int64_t slots, int mode) {
   const int64_t words = (width + 31) / 32;
@@ -73,12 +91,17 @@ __device__ __forceinline__ CkSmem ck_carve(char* p, int64_t width, int64_t slots
   p += ck_align(words * 4);
   s.keys = nullptr;
   s.vals = nullptr;
+  s.hub = nullptr;
   if (mode == 1) {
     s.keys = reinterpret_cast<int32_t*>(p);
     p += ck_align(slots * 4);
     s.vals = reinterpret_cast<double*>(p);
   } else if (mode == 2) {
     s.vals = reinterpret_cast<double*>(p);
+    p += ck_align(width * 8);
+    s.hub = reinterpret_cast<double*>(p);
+  } else if (mode == 3) {
+    s.hub = reinterpret_cast<double*>(p);
   }
   return s;
 }
@@ -140,10 +163,20 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   const double* val = p.cs.val + start;
 
   if (MODE == 0) {
-    for (int64_t f = g.lane; f < cnt; f += g.size) {
-      const uint32_t c = static_cast<uint32_t>(col[f]);
-      if (c < width) atomicOr(&s.bits[c >> 5], 1u << (c & 31));
-      else set_error(p.err, kErrBounds);
+    constexpr int U = 8;
+    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
+      uint32_t cr[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
+        cr[j] = f < cnt ? static_cast<uint32_t>(__ldcs(col + f)) : 0xffffffffu;
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = cr[j];
+        if (c < width) atomicOr(&s.bits[c >> 5], 1u << (c & 31));
+        else if (c != 0xffffffffu) set_error(p.err, kErrBounds);
+      }
     }
     g.sync();
     int64_t n = 0;
@@ -165,27 +198,43 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
     // keys and values were cleared above (values here, keys with the bitmap)
     for (int64_t j = g.lane; j < p.slots; j += g.size) s.vals[j] = 0.0;
     g.sync();
-    for (int64_t f = g.lane; f < cnt; f += g.size) {
-      const int32_t c = col[f];
-      if (static_cast<uint32_t>(c) >= width) {
-        set_error(p.err, kErrBounds);
-        continue;
-      }
-      const double v = val[f];
-      atomicOr(&s.bits[c >> 5], 1u << (c & 31));
-      uint32_t slot = hash_slot(c, slots);
-      uint32_t probe = 0;
-      for (; probe < slots; ++probe) {
-        const int32_t k = *reinterpret_cast<volatile int32_t*>(&s.keys[slot]);
-        if (k == c) break;
-        if (k == kEmptyKey) {
-          const int32_t old = atomicCAS(&s.keys[slot], kEmptyKey, c);
-          if (old == kEmptyKey || old == c) break;
+    constexpr int U = 4;
+    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
+      int32_t cr[U];
+      double vr[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
+        cr[j] = -1;
+        vr[j] = 0.0;
+        if (f < cnt) {
+          cr[j] = __ldcs(col + f);
+          vr[j] = __ldcs(val + f);
         }
-        slot = (slot + 1 == slots) ? 0 : slot + 1;
       }
-      if (probe < slots) atomicAdd(&s.vals[slot], v);
-      else set_error(p.err, kErrHashFull);
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int32_t c = cr[j];
+        if (c < 0) continue;
+        if (static_cast<uint32_t>(c) >= width) {
+          set_error(p.err, kErrBounds);
+          continue;
+        }
+        atomicOr(&s.bits[c >> 5], 1u << (c & 31));
+        uint32_t slot = hash_slot(c, slots);
+        uint32_t probe = 0;
+        for (; probe < slots; ++probe) {
+          const int32_t k = *reinterpret_cast<volatile int32_t*>(&s.keys[slot]);
+          if (k == c) break;
+          if (k == kEmptyKey) {
+            const int32_t old = atomicCAS(&s.keys[slot], kEmptyKey, c);
+            if (old == kEmptyKey || old == c) break;
+          }
+          slot = (slot + 1 == slots) ? 0 : slot + 1;
+        }
+        if (probe < slots) atomicAdd(&s.vals[slot], vr[j]);
+        else set_error(p.err, kErrHashFull);
+      }
     }
     g.sync();
     const int64_t n = ck_bitmap_prefix<WARP>(g, s, words);
@@ -206,34 +255,54 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   }
 
   if (MODE == 2) {
-    // dense: a value slot is zeroed by the thread whose atomicOr first sets its bit; adds
-    // follow after a barrier, so no add can meet an unzeroed slot
-    constexpr int kItems = 4;
-    for (int64_t b0 = 0; b0 < cnt; b0 += static_cast<int64_t>(g.size) * kItems) {
-      int32_t cr[kItems];
-      double vr[kItems];
+    // dense: the whole value array (and the warps' hub sums) is zeroed up front with vector
+    // stores, then every element ORs its bit and adds its value, with no barrier inside the
+    // stream; hub columns add into the warp's private slots
+    {
+      double2* v2 = reinterpret_cast<double2*>(s.vals);
+      const int64_t n2 = p.width / 2;
+      for (int64_t j = g.lane; j < n2; j += g.size) v2[j] = make_double2(0.0, 0.0);
+      if ((p.width & 1) && g.lane == 0) s.vals[p.width - 1] = 0.0;
+      for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
+    }
+    g.sync();
+    double* my_hub = s.hub + (threadIdx.x >> 5) % kHubWarps * kHubSlots;
+    constexpr int U = 8;
+    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
+      int32_t cr[U];
+      double vr[U];
 #pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        const int64_t f = b0 + static_cast<int64_t>(j) * g.size + g.lane;
+      for (int j = 0; j < U; ++j) {
+        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
         cr[j] = -1;
         vr[j] = 0.0;
         if (f < cnt) {
-          const int32_t c = col[f];
-          if (static_cast<uint32_t>(c) < width) {
-            cr[j] = c;
-            vr[j] = val[f];
-            const uint32_t bit = 1u << (c & 31);
-            const uint32_t old = atomicOr(&s.bits[c >> 5], bit);
-            if (!(old & bit)) s.vals[c] = 0.0;
-          } else {
-            set_error(p.err, kErrBounds);
-          }
+          cr[j] = __ldcs(col + f);
+          vr[j] = __ldcs(val + f);
         }
       }
-      g.sync();
 #pragma unroll
-      for (int j = 0; j < kItems; ++j)
-        if (cr[j] >= 0) atomicAdd(&s.vals[cr[j]], vr[j]);
+      for (int j = 0; j < U; ++j) {
+        const int32_t c = cr[j];
+        if (c < 0) continue;
+        if (static_cast<uint32_t>(c) < width) {
+          atomicOr(&s.bits[c >> 5], 1u << (c & 31));
+          const int hi = hub_index(static_cast<uint32_t>(c));
+          atomicAdd(hi >= 0 ? &my_hub[hi] : &s.vals[c], vr[j]);
+        } else {
+          set_error(p.err, kErrBounds);
+        }
+      }
+    }
+    g.sync();
+    // merge the warps' hub sums into the dense array
+    for (int j = g.lane; j < kHubSlots; j += g.size) {
+      const uint32_t c = j < 64 ? static_cast<uint32_t>(j) : (1u << (j - 64 + 6));
+      if (c < width) {
+        double sum = 0.0;
+        for (int w = 0; w < kHubWarps; ++w) sum += s.hub[w * kHubSlots + j];
+        s.vals[c] += sum;
+      }
     }
     g.sync();
     // ordered output: scan of the bitmap words, then every word writes its set bits
@@ -262,6 +331,127 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   }
 }
 
+// Dense numeric accumulation as persistent blocks (one per SM): the value array is zeroed once,
+// every chunk leaves it zeroed behind (each output slot is cleared as it is written), and
+// blocks take chunks from a shared counter so that a few very large chunks do not leave the
+// other SMs idle at the end.  Hub columns add into per-warp private sums.
+template <bool L2>
+__global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, double* gacc_all) {
+  extern __shared__ __align__(16) char smem_raw[];
+  __shared__ int64_t s_item;
+  CkGroup<false> g;
+  g.lane = threadIdx.x;
+  g.size = blockDim.x;
+  const CkSmem s = ck_carve(smem_raw, p.width, 0, L2 ? 3 : 2);
+  const int64_t words = (p.width + 31) / 32;
+  const uint32_t width = static_cast<uint32_t>(p.width);
+  // the accumulator: shared memory, or (L2) this block's slice of an L2-resident global array
+  // updated with fire-and-forget reductions performed by the L2 atomic units
+  double* acc = L2 ? gacc_all + static_cast<int64_t>(blockIdx.x) * p.width : s.vals;
+  {
+    if (L2) {
+      for (int64_t j = g.lane; j < p.width; j += g.size) __stcg(&acc[j], 0.0);
+    } else {
+      double2* v2 = reinterpret_cast<double2*>(acc);
+      for (int64_t j = g.lane; j < p.width / 2; j += g.size) v2[j] = make_double2(0.0, 0.0);
+      if ((p.width & 1) && g.lane == 0) acc[p.width - 1] = 0.0;
+    }
+    for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
+    for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
+  }
+  double* my_hub = s.hub + (threadIdx.x >> 5) % kHubWarps * kHubSlots;
+  for (;;) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_item = atomicAdd(next, 1);
+    __syncthreads();
+    const int64_t item = s_item;
+    if (item >= p.count) break;
+    const int64_t q = p.list[item];
+    const int64_t grow = p.cs.heavy_rows[p.cs.row[q]];
+    if (grow < p.sink.row_begin || grow >= p.sink.row_end) continue;
+    const int64_t start = p.cs.start[q];
+    const int64_t cnt = p.cs.cnt[q];
+    const int32_t* col = p.cs.col + start;
+    const double* val = p.cs.val + start;
+    constexpr int U = 8;
+    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
+      int32_t cr[U];
+      double vr[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
+        cr[j] = -1;
+        vr[j] = 0.0;
+        if (f < cnt) {
+          cr[j] = __ldcs(col + f);
+          vr[j] = __ldcs(val + f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int32_t c = cr[j];
+        if (c < 0) continue;
+        if (static_cast<uint32_t>(c) < width) {
+          atomicOr(&s.bits[c >> 5], 1u << (c & 31));
+          const int hi = hub_index(static_cast<uint32_t>(c));
+          if (L2) {
+            if (hi >= 0) atomicAdd(&my_hub[hi], vr[j]);
+            else atomicAdd(&acc[c], vr[j]);
+          } else {
+            atomicAdd(hi >= 0 ? &my_hub[hi] : &acc[c], vr[j]);  // one shared atomic, address selected
+          }
+        } else {
+          set_error(p.err, kErrBounds);
+        }
+      }
+    }
+    if (L2) __threadfence_block();
+    __syncthreads();
+    for (int j = g.lane; j < kHubSlots; j += g.size) {
+      const uint32_t c = j < 64 ? static_cast<uint32_t>(j) : (1u << (j - 64 + 6));
+      if (c < width) {
+        double sum = 0.0;
+        for (int w = 0; w < kHubWarps; ++w) {
+          sum += s.hub[w * kHubSlots + j];
+          s.hub[w * kHubSlots + j] = 0.0;
+        }
+        if (L2) __stcg(&acc[c], __ldcg(&acc[c]) + sum); else acc[c] += sum;
+      }
+    }
+    if (L2) __threadfence_block();
+    __syncthreads();
+    const int64_t out = p.sink.row_ptr[grow] + p.cs.out[q] - p.sink.row_ptr[p.sink.row_begin];
+    const int64_t expected = p.cs.nnz[q];
+    int32_t* c_col = p.sink.c_col + out;
+    double* c_val = p.sink.c_val + out;
+    const int32_t base = p.cs.base[q];
+    int64_t written = 0;
+    for (int64_t w0 = 0; w0 < words; w0 += g.size) {
+      const int64_t w = w0 + g.lane;
+      const uint32_t bits = w < words ? s.bits[w] : 0u;
+      const int64_t c = __popc(bits);
+      int64_t tot;
+      const int64_t incl = ck_scan<false>(g, c, s.tmp, &tot);
+      int64_t pos = written + incl - c;
+      uint32_t b = bits;
+      while (b) {
+        const int bit = __ffs(b) - 1;
+        b &= b - 1;
+        const int32_t idx = static_cast<int32_t>(w * 32 + bit);
+        if (pos < expected) {
+          c_col[pos] = idx + base;
+          c_val[pos] = L2 ? __ldcg(&acc[idx]) : acc[idx];
+        }
+        if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed for the next chunk
+        ++pos;
+      }
+      if (w < words) s.bits[w] = 0u;
+      written += tot;
+    }
+    if (written != expected && g.lane == 0) set_error(p.err, kErrRowOverflow);
+  }
+}
+
 size_t chunk_smem_bytes(int64_t width, int64_t slots, int mode, bool warp) {
   const size_t gb = ck_group_bytes(width, slots, mode);
   return warp ? gb * kCkWarpsPerBlock : gb;
@@ -279,7 +469,8 @@ static void ck_launch(const CkParams& p, int tpr, cudaStream_t s) {
 }
 
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
-                         int64_t slots, int tpr, const Sink& sink, uint32_t* err, cudaStream_t s) {
+                         int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
+                         cudaStream_t s) {
   if (count == 0) return;
   CkParams p{};
   p.cs = cs;
@@ -295,7 +486,21 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
   } else if (mode == 1) {
     if (warp) ck_launch<true, 1>(p, tpr, s); else ck_launch<false, 1>(p, tpr, s);
   } else {
-    ck_launch<false, 2>(p, tpr, s);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = std::min<int64_t>(count, sms);
+    cudaMemsetAsync(counter, 0, sizeof(int), s);
+    note_launch();
+    if (gacc) {  // L2-resident accumulators: the shared array is not needed
+      const size_t smem = chunk_smem_bytes(width, 0, 3, false);
+      cudaFuncSetAttribute(k_chunk_dense<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      k_chunk_dense<true><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, gacc);
+    } else {
+      const size_t smem = chunk_smem_bytes(width, 0, 2, false);
+      cudaFuncSetAttribute(k_chunk_dense<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      k_chunk_dense<false><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, nullptr);
+    }
   }
 }
 

@@ -308,20 +308,28 @@ __global__ void __launch_bounds__(kMsThreads) k_histogram(const int64_t* __restr
   ms_load_tile<false>(col, nullptr, t * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
                       min(total, (t + 1) * kMsTile), c, unused);
   int2 pr = part[t];
+  // row bounds of the first row window, kept in a register by the first gr+1 threads
+  int64_t rb = threadIdx.x <= min(gr, static_cast<int64_t>(pr.y - pr.x + 1)) ? rp[pr.x + threadIdx.x] : 0;
   for (; t < ntiles; t += gridDim.x) {
     const int64_t g0 = t * kMsTile;
     const int64_t g1 = min(total, g0 + kMsTile);
     const int64_t p0 = g0 + static_cast<int64_t>(threadIdx.x) * kMsItems;
     const int64_t tn = t + gridDim.x;
     int2 prn = pr;
+    int64_t rbn = 0;
     if (tn < ntiles) {
       ms_load_tile<false>(col, nullptr, tn * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
                           min(total, (tn + 1) * kMsTile), cn, unused);
       prn = part[tn];
+      if (threadIdx.x <= min(gr, static_cast<int64_t>(prn.y - prn.x + 1))) rbn = rp[prn.x + threadIdx.x];
     }
     for (int64_t w0 = pr.x; w0 <= pr.y; w0 += gr) {  // windows of at most gr rows
       const int nr = static_cast<int>(min(gr, static_cast<int64_t>(pr.y) - w0 + 1));
-      for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
+      if (w0 == pr.x && nr < static_cast<int>(blockDim.x)) {
+        if (threadIdx.x <= nr) rstart[threadIdx.x] = rb;
+      } else {
+        for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
+      }
       for (int64_t i = threadIdx.x; i < nr * v; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       int bin[kMsItems];
@@ -338,6 +346,7 @@ __global__ void __launch_bounds__(kMsThreads) k_histogram(const int64_t* __restr
 #pragma unroll
     for (int j = 0; j < kMsItems; ++j) c[j] = cn[j];
     pr = prn;
+    rb = rbn;
   }
 }
 
@@ -362,7 +371,7 @@ void launch_histogram(const int64_t* row_ptr, const int2* part, int64_t total, c
 }
 
 template <bool VALS, bool MATCH>
-__global__ void __launch_bounds__(kMsThreads) k_multisplit(
+__global__ void __launch_bounds__(kMsThreads, 2) k_multisplit(
     const int64_t* __restrict__ rp, const int2* __restrict__ part, int64_t total, int64_t ntiles,
     const int32_t* __restrict__ in_col, const double* __restrict__ in_val, int shift, int64_t v, int64_t gr,
     const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
