@@ -16,13 +16,77 @@ namespace sg {
 
 constexpr int kCkWarpsPerBlock = 8;
 
-// Hub columns of a chunk: the lowest 64 local columns and every power of two above them.  In
-// power-law (R-MAT-like) products these few columns receive a large share of the products of
-// every chunk (local column 0 alone ~2%), so every warp keeps private sums for them instead of
-// contending on one shared-memory address; the private sums are merged once per chunk.
+// Hub columns of a chunk: local columns with at most two set bits (0, 2^i, 2^i + 2^j) below
+// 2^16.  In R-MAT / Kronecker power-law products the probability of a column falls with every
+// set bit of its index, so these few columns take a large share of the products of every
+// chunk (local column 0 alone ~2% on R-MAT with a = 0.57).  Shared-memory fp64 atomics
+// serialise badly on one address, so hub products are first summed across the lanes of a warp
+// (__match_any_sync + shuffle reduction) and then added to warp-private slots; the private
+// slots are merged once per chunk.  On other inputs the hubs are just ordinary columns.
 constexpr int kHubWarps = 32;
-constexpr int kHubSlots = 80;  // 64 low columns + powers of two 2^6 .. 2^15
+constexpr int kHubBits = 16;
+constexpr int kHubSlots = 1 + kHubBits + kHubBits * (kHubBits - 1) / 2;  // 137
+static_assert(kHubSlots == kChunkHubSlots, "hub slot count");
 
+__device__ __forceinline__ int hub_index(uint32_t c) {
+  if (c >= (1u << kHubBits)) return -1;
+  const int pc = __popc(c);
+  if (pc == 0) return 0;
+  if (pc == 1) return 1 + (__ffs(c) - 1);
+  if (pc == 2) {
+    const int i = __ffs(c) - 1;
+    const int j = 31 - __clz(c);
+    return 1 + kHubBits + j * (j - 1) / 2 + i;
+  }
+  return -1;
+}
+
+__host__ __device__ inline uint32_t hub_column(int idx) {
+  if (idx == 0) return 0u;
+  if (idx <= kHubBits) return 1u << (idx - 1);
+  int k = idx - 1 - kHubBits, j = 1;
+  while (k >= j) {
+    k -= j;
+    ++j;
+  }
+  return (1u << j) | (1u << k);
+}
+
+// Position of the k-th (0-based) set bit of m (k < popc(m)).
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int k) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const uint32_t low = m & ((1u << w) - 1u);
+    const int c = __popc(low);
+    if (k >= c) {
+      k -= c;
+      m >>= w;
+      pos += w;
+    } else {
+      m = low;
+    }
+  }
+  return pos;
+}
+
+// Sum `v` over the lanes of the warp that hold the same key (key >= 0); returns true on the one
+// lane per key that must apply the group's sum (left in *sum).  All 32 lanes must call it.
+__device__ __forceinline__ bool warp_group_sum(int key, double v, double* sum) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, key);
+  const int rank = __popc(peers & lanemask_lt());
+  const int gsize = __popc(peers);
+  double acc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const bool take = ((rank & (2 * d - 1)) == 0) && (rank + d < gsize);
+    const int src = (rank + d < gsize) ? nth_set_bit(peers, rank + d) : static_cast<int>(lane_id());
+    const double o = __shfl_sync(0xffffffffu, acc, src);
+    if (take) acc += o;
+  }
+  *sum = acc;
+  return key >= 0 && rank == 0;
+}
 
 struct CkParams {
   ChunkSet cs;
@@ -32,6 +96,7 @@ struct CkParams {
   int64_t slots;         // hash slots (hash numeric)
   Sink sink;
   uint32_t* err;
+  double* hub_all;       // dense mode: kHubSlots doubles per block, L2 resident
 };
 
 template <bool WARP>
@@ -60,8 +125,7 @@ __host__ __device__ inline size_t ck_group_bytes(int64_t width, int64_t slots, i
   const int64_t words = (width + 31) / 32;
   size_t b = ck_align(33 * sizeof(int64_t)) + ck_align(words * 4) + ck_align(words * 4);
   if (mode == 1) b += ck_align(slots * 4) + ck_align(slots * 8);  // hash numeric
-  if (mode == 2) b += ck_align(width * 8) + ck_align(kHubWarps * kHubSlots * 8);  // dense + warp hubs
-  if (mode == 3) b += ck_align(kHubWarps * kHubSlots * 8);                        // hubs only (L2 dense)
+  if (mode == 2) b += ck_align(width * 8);  // dense
   return b;
 }
 
@@ -73,12 +137,6 @@ struct CkSmem {
   double* vals;
   double* hub;   // dense mode: per-warp private sums of the hub columns
 };
-
-__device__ __forceinline__ int hub_index(uint32_t c) {
-  if (c < 64u) return static_cast<int>(c);
-  if ((c & (c - 1u)) == 0u && c < (1u << 16)) return 64 + (__ffs(c) - 1) - 6 + 0;
-  return -1;
-}
 
 __device__ __forceinline__ CkSmem ck_carve(char* p, int64_t width, int64_t slots, int mode) {
   const int64_t words = (width + 31) / 32;
@@ -98,10 +156,6 @@ __device__ __forceinline__ CkSmem ck_carve(char* p, int64_t width, int64_t slots
     s.vals = reinterpret_cast<double*>(p);
   } else if (mode == 2) {
     s.vals = reinterpret_cast<double*>(p);
-    p += ck_align(width * 8);
-    s.hub = reinterpret_cast<double*>(p);
-  } else if (mode == 3) {
-    s.hub = reinterpret_cast<double*>(p);
   }
   return s;
 }
@@ -263,8 +317,7 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
       const int64_t n2 = p.width / 2;
       for (int64_t j = g.lane; j < n2; j += g.size) v2[j] = make_double2(0.0, 0.0);
       if ((p.width & 1) && g.lane == 0) s.vals[p.width - 1] = 0.0;
-      for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
-    }
+      }
     g.sync();
     double* my_hub = s.hub + (threadIdx.x >> 5) % kHubWarps * kHubSlots;
     constexpr int U = 8;
@@ -297,7 +350,7 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
     g.sync();
     // merge the warps' hub sums into the dense array
     for (int j = g.lane; j < kHubSlots; j += g.size) {
-      const uint32_t c = j < 64 ? static_cast<uint32_t>(j) : (1u << (j - 64 + 6));
+      const uint32_t c = hub_column(j);
       if (c < width) {
         double sum = 0.0;
         for (int w = 0; w < kHubWarps; ++w) sum += s.hub[w * kHubSlots + j];
@@ -342,7 +395,7 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
   CkGroup<false> g;
   g.lane = threadIdx.x;
   g.size = blockDim.x;
-  const CkSmem s = ck_carve(smem_raw, p.width, 0, L2 ? 3 : 2);
+  const CkSmem s = ck_carve(smem_raw, p.width, 0, L2 ? 0 : 2);  // mode 0: bitmap only
   const int64_t words = (p.width + 31) / 32;
   const uint32_t width = static_cast<uint32_t>(p.width);
   // the accumulator: shared memory, or (L2) this block's slice of an L2-resident global array
@@ -356,11 +409,14 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
       for (int64_t j = g.lane; j < p.width / 2; j += g.size) v2[j] = make_double2(0.0, 0.0);
       if ((p.width & 1) && g.lane == 0) acc[p.width - 1] = 0.0;
     }
-    for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
     for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
   }
-  double* my_hub = s.hub + (threadIdx.x >> 5) % kHubWarps * kHubSlots;
+  // hub sums live in this block's slots of a small global array (L2 resident), zeroed here and
+  // left zeroed after every chunk
+  double* ghub = p.hub_all + static_cast<int64_t>(blockIdx.x) * kHubSlots;
+  for (int j = g.lane; j < kHubSlots; j += g.size) __stcg(&ghub[j], 0.0);
   for (;;) {
+    __threadfence_block();
     __syncthreads();
     if (threadIdx.x == 0) s_item = atomicAdd(next, 1);
     __syncthreads();
@@ -394,27 +450,20 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
         if (static_cast<uint32_t>(c) < width) {
           atomicOr(&s.bits[c >> 5], 1u << (c & 31));
           const int hi = hub_index(static_cast<uint32_t>(c));
-          if (L2) {
-            if (hi >= 0) atomicAdd(&my_hub[hi], vr[j]);
-            else atomicAdd(&acc[c], vr[j]);
-          } else {
-            atomicAdd(hi >= 0 ? &my_hub[hi] : &acc[c], vr[j]);  // one shared atomic, address selected
-          }
+          if (hi >= 0) atomicAdd(&ghub[hi], vr[j]);  // L2 reduction, no retry loop
+          else atomicAdd(&acc[c], vr[j]);
         } else {
           set_error(p.err, kErrBounds);
         }
       }
     }
-    if (L2) __threadfence_block();
+    __threadfence_block();
     __syncthreads();
     for (int j = g.lane; j < kHubSlots; j += g.size) {
-      const uint32_t c = j < 64 ? static_cast<uint32_t>(j) : (1u << (j - 64 + 6));
+      const uint32_t c = hub_column(j);
       if (c < width) {
-        double sum = 0.0;
-        for (int w = 0; w < kHubWarps; ++w) {
-          sum += s.hub[w * kHubSlots + j];
-          s.hub[w * kHubSlots + j] = 0.0;
-        }
+        const double sum = __ldcg(&ghub[j]);
+        __stcg(&ghub[j], 0.0);
         if (L2) __stcg(&acc[c], __ldcg(&acc[c]) + sum); else acc[c] += sum;
       }
     }
@@ -470,7 +519,7 @@ static void ck_launch(const CkParams& p, int tpr, cudaStream_t s) {
 
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
                          int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
-                         cudaStream_t s) {
+                         double* hub_all, cudaStream_t s) {
   if (count == 0) return;
   CkParams p{};
   p.cs = cs;
@@ -480,6 +529,7 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
   p.slots = slots;
   p.sink = sink;
   p.err = err;
+  p.hub_all = hub_all;
   const bool warp = tpr == 32;
   if (mode == 0) {
     if (warp) ck_launch<true, 0>(p, tpr, s); else ck_launch<false, 0>(p, tpr, s);
@@ -493,7 +543,7 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
     cudaMemsetAsync(counter, 0, sizeof(int), s);
     note_launch();
     if (gacc) {  // L2-resident accumulators: the shared array is not needed
-      const size_t smem = chunk_smem_bytes(width, 0, 3, false);
+      const size_t smem = chunk_smem_bytes(width, 0, 0, false);
       cudaFuncSetAttribute(k_chunk_dense<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       k_chunk_dense<true><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, gacc);
     } else {
