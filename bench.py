@@ -42,6 +42,30 @@ def compulsory_bytes(A, B, c_nnz: int) -> int:
     return (A.rows + 1) * 8 + 12 * A.nnz + (B.rows + 1) * 8 + 12 * b_nnz + (A.rows + 1) * 8 + 12 * c_nnz
 
 
+KERNEL_OF = {"outer_product": "k_outer_product", "histogram": "k_histogram", "multisplit": "k_multisplit",
+             "chunk_symbolic": "k_chunk", "chunk_dense": "k_chunk_dense"}
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of this workload, or None
+    when there is none or the kernel's source file changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_%s.md" % workload.replace("rmat_s18_ef16", "rmat_s18"))
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 5 and parts[0] == "traffic" and parts[1] == kernel:
+            kv = dict(x.split("=", 1) for x in parts[2:])
+            src = os.path.join(ROOT, "sparse_gemm_irregular_gb300", "csrc", kv["source"])
+            if not os.path.exists(src):
+                return None
+            if hashlib.sha1(open(src, "rb").read()).hexdigest()[:12] != kv["sha1"]:
+                return None
+            return int(kv["bytes"])
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -125,10 +149,14 @@ def oracle_rate(A, B, seconds: float, threads: int):
     oracle.spgemm_rows(A, B, rows, threads=threads)
     dt = time.perf_counter() - t0
     rate = ipn / max(dt, 1e-6)
-    rows, ipn = sample_rows_by_ip(A, B, rate * seconds, seed=1)
-    t0 = time.perf_counter()
-    oracle.spgemm_rows(A, B, rows, threads=threads)
-    dt = time.perf_counter() - t0
+    for attempt in range(2):
+        rows, ipn = sample_rows_by_ip(A, B, rate * seconds, seed=1 + attempt)
+        t0 = time.perf_counter()
+        oracle.spgemm_rows(A, B, rows, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= 0.6 * seconds:
+            break
+        rate = ipn / max(dt, 1e-6)
     return 2.0 * ipn / dt / 1e9, len(rows), ipn, dt
 
 
@@ -179,6 +207,8 @@ def kernel_bytes(name, st, elems_heavy, nnz_c_heavy, final_chunks, heavy_rows):
         return 4 * elems_heavy                        # read C^_reord columns
     if name == "chunk_numeric":
         return 12 * elems_heavy + 12 * nnz_c_heavy    # read C^_reord, write the heavy rows of C
+    if name == "chunk_dense":
+        return 12 * st.dense_elems + 12 * st.dense_nnz  # its share of the same
     return None
 
 
@@ -194,14 +224,21 @@ def main():
     ap.add_argument("--flags", type=int, default=0, help="extra SPGEMM_FLAG_* bits for A/B runs")
     ap.add_argument("--chunk-width", type=int, default=0, help="planner override W (A/B runs)")
     ap.add_argument("--tau", type=int, default=0, help="planner override tau (A/B runs)")
+    ap.add_argument("--rmat-scale", type=int, default=0,
+                    help="replace the workload by a seeded R-MAT of this scale (small cases for profiling)")
+    ap.add_argument("--edge-factor", type=int, default=16)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg_name = synth.CONFIGS[args.config][0]
-    A = synth.config(args.config)
+    if args.rmat_scale:
+        cfg_name = "rmat_s%d_ef%d" % (args.rmat_scale, args.edge_factor)
+        A = synth.rmat(args.rmat_scale, args.edge_factor, seed=0)
+    else:
+        cfg_name = synth.CONFIGS[args.config][0]
+        A = synth.config(args.config)
 
     if args.impl == "reference":
         run_reference(args, A, cfg_name, rank)
@@ -275,16 +312,17 @@ def main():
     hbm_frac = comp / (t_total / args.steps) / 1e9 / peak
 
     # dominant kernel of the step and its roofline
-    kern = ["outer_product", "histogram", "multisplit", "chunk_symbolic", "chunk_numeric",
-            "light_symbolic", "light_numeric"]
+    kern = ["outer_product", "histogram", "multisplit", "chunk_symbolic", "chunk_dense"]
     dom = max(kern, key=lambda k_: phase_tot.get(k_, [0, 0])[0])
     dom_ms, dom_n = phase_tot[dom]
     roofline = None
     byt = kernel_bytes(dom, st, st.ip_heavy, st.c_nnz_heavy, st.final_chunks, st.rows_heavy)
     if dom_n and byt:
         achieved = byt * args.steps / (dom_ms / 1e3) / 1e9   # algorithmic bytes / device time
-        roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
-                    "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+        traffic = measured_traffic(KERNEL_OF.get(dom, ""), cfg_name)
+        roofline = {"kernel": KERNEL_OF.get(dom, dom), "bound": "hbm", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                    "algorithmic_bytes_per_launch": byt,
                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)",
                     "timed_regions_per_step": dom_n / args.steps,
                     "ms_per_step": dom_ms / args.steps}

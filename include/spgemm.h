@@ -113,6 +113,8 @@ typedef struct {
   int64_t chunks_dense;      /* of which on the dense accumulator                       */
   int64_t chat_bytes;        /* bytes of C^ col+val per batch buffer (largest batch)    */
   int64_t c_nnz_heavy;       /* entries of C in heavy rows (after spgemm_symbolic)      */
+  int64_t dense_elems;       /* C^_reord elements summed on the dense accumulator       */
+  int64_t dense_nnz;         /* entries of C those dense chunks produce                 */
   int32_t resident;          /* 1: C^_reord kept from symbolic to numeric               */
   int32_t reserved;
 } spgemm_stats;
@@ -161,10 +163,10 @@ int spgemm_get_plan(spgemm_handle h, spgemm_plan* out);
  *   0 setup, 1 light symbolic, 2 masked CSR-to-CSC + slice offsets, 3 outer-product kernel,
  *   4 histogram kernel, 5 multisplit kernel, 6 multisplit bookkeeping (partition, offsets),
  *   7 heavy chunk symbolic, 8 chunk offsets, 9 C.row_ptr scan, 10 light numeric,
- *   11 heavy chunk numeric.
+ *   11 heavy chunk numeric (all chunk kernels), 12 its dense-accumulator kernel alone.
  * Only recorded when the handle was created with SPGEMM_FLAG_TIMING or the environment
  * variable SPGEMM_TIMING=1.  Synchronises the stream.  t and launches (may be NULL) receive
- * min(count, 12) entries. */
+ * min(count, 13) entries. */
 int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_t count);
 
 /* Number of kernels this library has launched in the process so far (all handles). */

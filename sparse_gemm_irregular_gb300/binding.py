@@ -27,7 +27,7 @@ FLAG_NO_MATCH = 64
 FLAG_DENSE_L2 = 128
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",
-          "light_numeric", "chunk_numeric"]
+          "light_numeric", "chunk_numeric", "chunk_dense"]
 MAX_LEVELS = 8
 
 _i64 = ctypes.c_int64
@@ -58,7 +58,8 @@ class spgemm_stats(ctypes.Structure):
                 ("rows_heavy", _i64), ("rows_light", _i64), ("rows_empty", _i64),
                 ("rows_dense_light", _i64), ("c_nnz", _i64), ("heavy_batches", _i64),
                 ("levels_run", _i64), ("final_chunks", _i64), ("chunks_dense", _i64),
-                ("chat_bytes", _i64), ("c_nnz_heavy", _i64), ("resident", _i32), ("reserved", _i32)]
+                ("chat_bytes", _i64), ("c_nnz_heavy", _i64), ("dense_elems", _i64), ("dense_nnz", _i64),
+                ("resident", _i32), ("reserved", _i32)]
 
 
 EXPORTS = {

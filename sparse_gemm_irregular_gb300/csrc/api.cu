@@ -172,8 +172,13 @@ struct PhaseTimer {
     cudaEventCreate(&a);
     cudaEventRecord(a, st);
   }
+  void cancel() {
+    if (!h->timing || !a) return;
+    cudaEventDestroy(a);
+    a = nullptr;
+  }
   ~PhaseTimer() {
-    if (!h->timing) return;
+    if (!h->timing || !a) return;
     cudaEvent_t b;
     cudaEventCreate(&b);
     cudaEventRecord(b, st);
@@ -479,6 +484,18 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
                           h->st);
     }
   }
+  {
+    // element and nnz totals of the dense-accumulator chunks (for the statistics)
+    const int bd = h->lad.n + 3;
+    unsigned long long* sums;
+    SG_ALLOC(sums, unsigned long long, 2);
+    cudaMemsetAsync(sums, 0, 2 * sizeof(unsigned long long), h->st);
+    launch_list_sums(hb.f_list + hb.f_bin_start[bd], hb.f_bin_start[bd + 1] - hb.f_bin_start[bd], hb.f_cnt,
+                     hb.f_nnz, sums, h->st);
+    SG_TRY(check_cuda(cudaMemcpyAsync(hb.dense_sums, sums, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                      "copy dense sums"));
+    ws_free(h, sums);
+  }
   // offsets of the chunks inside their rows
   PhaseTimer toff(h, 8);
   const int64_t nfin = h->plan.chunks_required;
@@ -516,6 +533,8 @@ int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
   if (!h->d_hub) SG_ALLOC(h->d_hub, double, static_cast<int64_t>(h->sms) * kChunkHubSlots);
   for (int j = 0; j < 4; ++j) {
     const int b = h->lad.n + j;
+    PhaseTimer td(h, 12);  // only the dense bin is counted here (its region nests in slot 11)
+    if (j < 3) td.cancel();
     launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
                         h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err,
                         h->d_counter, h->d_gacc, h->d_hub, h->st);
@@ -835,7 +854,13 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
   *c_nnz = nnz;
   h->stats.c_nnz = nnz;
   h->stats.c_nnz_heavy = 0;
-  for (auto& hb : h->batches) h->stats.c_nnz_heavy += hb.nnz_c;
+  h->stats.dense_elems = 0;
+  h->stats.dense_nnz = 0;
+  for (auto& hb : h->batches) {
+    h->stats.c_nnz_heavy += hb.nnz_c;
+    h->stats.dense_elems += hb.dense_sums[0];
+    h->stats.dense_nnz += hb.dense_sums[1];
+  }
   h->c_row_ptr = c_row_ptr;
   h->state = 2;
   return SPGEMM_OK;

@@ -22,7 +22,7 @@ constexpr int kOpThreads = 256;
 constexpr int kSmemReserve = 7168;         // bytes kept back from s_LM for per-block staging
 constexpr int kMaxLadder = 16;             // light bin ladder levels
 constexpr int kScanTile = 4096;            // elements per scan block (512 threads x 8)
-constexpr int kPhaseSlots = 12;            // timed regions, see spgemm_get_phase_times
+constexpr int kPhaseSlots = 13;            // timed regions, see spgemm_get_phase_times
 constexpr int64_t kChunkDenseMin = 2048;   // last-level chunks above this size use the dense accumulator
 
 // Light-row / chunk bin ladder derived from tau (hash tables at load factor 1/2).
@@ -148,6 +148,9 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
 constexpr int kChunkHubSlots = 137;           // hub columns of a dense chunk (k_chunk.cu)
 void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s);
 void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s);
+// out[0] += sum of a[list[i]], out[1] += sum of b[list[i]] for i < n
+void launch_list_sums(const int32_t* list, int64_t n, const int64_t* a, const int64_t* b,
+                      unsigned long long* out, cudaStream_t s);
 void launch_grid_fill(const int32_t* f_row, const int32_t* f_base, const int64_t* f_nnz, int64_t n,
                       int shift_fin, int64_t nfin, int64_t* grid, cudaStream_t s);
 void launch_grid_finish(const int64_t* grid_scanned, const int32_t* f_row, const int32_t* f_base,
@@ -184,6 +187,7 @@ struct HeavyBatch {
   std::vector<int64_t> f_bin_start;  // host, per chunk bin (size nbins + 1)
   int64_t nnz_c = 0;            // entries of C in the batch's rows (read after the symbolic sync)
   int64_t bitmap_from = 0;      // descriptors from here on are last-level chunks (width W)
+  int64_t dense_sums[2] = {0, 0};  // elements and nnz of the chunks on the dense accumulator
 };
 
 struct spgemm_ctx {

@@ -50,6 +50,28 @@ void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* d
   k_offset_copy<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(src, n, delta, dst);
 }
 
+__global__ void k_list_sums(const int32_t* __restrict__ list, int64_t n, const int64_t* __restrict__ a,
+                            const int64_t* __restrict__ b, unsigned long long* out) {
+  unsigned long long sa = 0, sb = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    sa += static_cast<unsigned long long>(a[list[i]]);
+    sb += static_cast<unsigned long long>(b[list[i]]);
+  }
+  sa = warp_sum(sa);
+  sb = warp_sum(sb);
+  if (lane_id() == 0) {
+    atomicAdd(&out[0], sa);
+    atomicAdd(&out[1], sb);
+  }
+}
+void launch_list_sums(const int32_t* list, int64_t n, const int64_t* a, const int64_t* b, unsigned long long* out,
+                      cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_list_sums<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n, 256), 1024)), 256, 0, s>>>(list, n, a, b, out);
+}
+
 // ---- masked CSR -> CSC of the heavy rows of A ------------------------------------------------
 __global__ void k_csc_count(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
                             const int32_t* __restrict__ rows, int64_t nrows, int32_t* __restrict__ cnt) {
