@@ -210,8 +210,20 @@ int valid_csr_desc(const spgemm_csr* M, int64_t rows, int64_t cols) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Level-0 histogram of a batch, filled by the outer product (none when one chunk covers a row).
+int alloc_counts0(spgemm_ctx* h, const HeavyBatch& hb, unsigned long long** out) {
+  *out = nullptr;
+  if (h->plan.chunks_required == 1) return SPGEMM_OK;
+  const int64_t n = (hb.h1 - hb.h0) * h->plan.v_chunks[0];
+  unsigned long long* c;
+  SG_ALLOC(c, unsigned long long, n);
+  cudaMemsetAsync(c, 0, sizeof(unsigned long long) * n, h->st);
+  *out = c;
+  return SPGEMM_OK;
+}
+
 // Heavy batch: expansion (MaskedCsr2Csc + OuterProduct of Algorithm 3).
-int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr) {
+int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr, unsigned long long* counts0) {
   std::unique_ptr<PhaseTimer> tcsc(new PhaseTimer(h, 2));
   const int64_t R = hb.h1 - hb.h0;
   const int32_t* rows = h->d_heavy + hb.h0;
@@ -248,8 +260,10 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr) {
   launch_partition(slice_off, kc, hb.elems, kOpTile, part, h->st);
   {
     PhaseTimer t(h, 3);
+    const spgemm_plan& P = h->plan;
+    const int shift0 = ilog2_i64(P.chunk_width * P.chunks_required / P.v_chunks[0]);
     launch_outer_product(colptr, csc_row, csc_val, slice_off, part, hb.elems, h->B, cursor, h->d_chat_col,
-                         vals ? h->d_chat_val : nullptr, vals, h->d_err, h->st);
+                         vals ? h->d_chat_val : nullptr, vals, counts0, shift0, P.v_chunks[0], h->d_err, h->st);
   }
   ws_free(h, part);
   ws_free(h, colcnt);
@@ -264,7 +278,8 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr) {
 // Heavy batch: hierarchical multisplit (the reorder loop of Algorithm 3).  The symbolic pass records
 // the level structure (which needs the heavy-chunk counts on the host); the numeric pass of a
 // recomputed batch replays it without synchronising.
-int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const int64_t* c_rowptr) {
+int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const int64_t* c_rowptr,
+                 unsigned long long* counts0) {
   const spgemm_plan& P = h->plan;
   const int64_t R = hb.h1 - hb.h0;
   const int64_t cap = h->batch_cap;
@@ -324,18 +339,20 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     unsigned long long* counts;
     int32_t *xmap = nullptr, *out_row, *out_base;
     int64_t* rptr;
-    SG_ALLOC(counts, unsigned long long, nout);
+    const bool fused = (l == 0 && counts0 != nullptr);  // level-0 counts came from the outer product
+    if (fused) counts = counts0;
+    else SG_ALLOC(counts, unsigned long long, nout);
     SG_ALLOC(rptr, int64_t, nout + 1);
     SG_ALLOC(out_row, int32_t, nout);
     SG_ALLOC(out_base, int32_t, nout);
-    cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
+    if (!fused) cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
     const int32_t* in_col = h->d_chat_col + in_half * cap;
     const double* in_val = h->d_chat_val ? h->d_chat_val + in_half * cap : nullptr;
     const bool match = !(h->opt.flags & SPGEMM_FLAG_NO_MATCH);
     int2* part;
     SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(total_in, kMsTile)));
     launch_partition(in_ptr, nin, total_in, kMsTile, part, h->st);
-    {
+    if (!fused) {
       PhaseTimer t(h, 4);
       launch_histogram(in_ptr, part, total_in, in_col, shift, v, P.group_rows, counts, false, h->sms, h->d_err,
                        h->st);
@@ -386,7 +403,7 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     }
     ws_free(h, part);
     ws_free(h, cursor);
-    ws_free(h, counts);
+    if (!fused) ws_free(h, counts);
     if (xmap) ws_free(h, xmap);
     // light outputs of this level (all outputs at the last level) are final chunks
     if (record) {
@@ -597,8 +614,11 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
       SG_TRY(ensure_chat(h, true));
       int64_t* crp;
       SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
-      SG_TRY(heavy_expand(h, hb, true, crp));
-      SG_TRY(heavy_levels(h, hb, true, false, crp));
+      unsigned long long* counts0 = nullptr;
+      SG_TRY(alloc_counts0(h, hb, &counts0));
+      SG_TRY(heavy_expand(h, hb, true, crp, counts0));
+      SG_TRY(heavy_levels(h, hb, true, false, crp, counts0));
+      if (counts0) ws_free(h, counts0);
       SG_TRY(heavy_chunk_numeric(h, hb, sk));
       ws_free(h, crp);
     } else {
@@ -831,8 +851,11 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     SG_TRY(ensure_chat(h, vals));
     int64_t* crp;
     SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
-    SG_TRY(heavy_expand(h, hb, vals, crp));
-    SG_TRY(heavy_levels(h, hb, vals, true, crp));
+    unsigned long long* counts0 = nullptr;
+    SG_TRY(alloc_counts0(h, hb, &counts0));
+    SG_TRY(heavy_expand(h, hb, vals, crp, counts0));
+    SG_TRY(heavy_levels(h, hb, vals, true, crp, counts0));
+    if (counts0) ws_free(h, counts0);
     SG_TRY(heavy_chunk_symbolic(h, hb, c_row_ptr));
     ws_free(h, crp);
     levels = std::max<int64_t>(levels, static_cast<int64_t>(hb.lv.size()));

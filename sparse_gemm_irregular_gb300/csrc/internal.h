@@ -122,7 +122,7 @@ void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t t
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
                           const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
                           int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
-                          uint32_t* err, cudaStream_t s);
+                          unsigned long long* counts, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s);
 void launch_histogram(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* col, int shift,
                       int64_t nchunks, int64_t group_rows, unsigned long long* counts, bool match, int sms,
                       uint32_t* err, cudaStream_t s);

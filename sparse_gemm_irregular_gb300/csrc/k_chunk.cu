@@ -125,7 +125,8 @@ __host__ __device__ inline size_t ck_group_bytes(int64_t width, int64_t slots, i
   const int64_t words = (width + 31) / 32;
   size_t b = ck_align(33 * sizeof(int64_t)) + ck_align(words * 4) + ck_align(words * 4);
   if (mode == 1) b += ck_align(slots * 4) + ck_align(slots * 8);  // hash numeric
-  if (mode == 2) b += ck_align(width * 8);  // dense
+  if (mode == 2) b += ck_align(width * 8) + ck_align(kHubWarps * kHubSlots * 8);  // dense + warp hubs
+  if (mode == 3) b += ck_align(kHubWarps * kHubSlots * 8);                        // L2 dense: hubs only
   return b;
 }
 
@@ -156,6 +157,10 @@ __device__ __forceinline__ CkSmem ck_carve(char* p, int64_t width, int64_t slots
     s.vals = reinterpret_cast<double*>(p);
   } else if (mode == 2) {
     s.vals = reinterpret_cast<double*>(p);
+    p += ck_align(width * 8);
+    s.hub = reinterpret_cast<double*>(p);
+  } else if (mode == 3) {
+    s.hub = reinterpret_cast<double*>(p);
   }
   return s;
 }
@@ -384,120 +389,155 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   }
 }
 
-// Dense numeric accumulation as persistent blocks (one per SM): the value array is zeroed once,
-// every chunk leaves it zeroed behind (each output slot is cleared as it is written), and
-// blocks take chunks from a shared counter so that a few very large chunks do not leave the
-// other SMs idle at the end.  Hub columns add into per-warp private sums.
+// Dense numeric accumulation as persistent blocks (one per SM; the 16,384-double array fills
+// most of the shared memory).  With one block per SM the per-chunk latency (taking the next
+// chunk from the work counter, the chain of descriptor loads) would sit on the critical path, so
+// warp 0 is a helper: while warps 1..31 stream the current chunk it takes the next chunk and
+// loads its descriptor into a second shared slot.  The value array is zeroed once and every
+// chunk clears the slots it writes.  Hub columns (hub_index) add into per-warp private sums in
+// shared memory, merged once per chunk, so the hottest columns of power-law inputs do not
+// serialise on one address.  The L2 variant keeps the value array in an L2-resident global
+// slice instead (fire-and-forget reductions), for A/B measurements.
+struct DenseJob {
+  int64_t start, cnt, out, expected;
+  int32_t base;
+  int32_t state;  // 0 none left, 1 work, 2 outside the numeric row window
+};
+
+__device__ __forceinline__ void dense_fetch(const CkParams& p, int* next, DenseJob* j) {
+  const int64_t item = atomicAdd(next, 1);
+  if (item >= p.count) {
+    j->state = 0;
+    return;
+  }
+  const int64_t q = p.list[item];
+  const int64_t grow = p.cs.heavy_rows[p.cs.row[q]];
+  if (grow < p.sink.row_begin || grow >= p.sink.row_end) {
+    j->state = 2;
+    return;
+  }
+  j->start = p.cs.start[q];
+  j->cnt = p.cs.cnt[q];
+  j->out = p.sink.row_ptr[grow] + p.cs.out[q] - p.sink.row_ptr[p.sink.row_begin];
+  j->expected = p.cs.nnz[q];
+  j->base = p.cs.base[q];
+  j->state = 1;
+}
+
 template <bool L2>
 __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, double* gacc_all) {
   extern __shared__ __align__(16) char smem_raw[];
-  __shared__ int64_t s_item;
+  __shared__ DenseJob jobs[2];
   CkGroup<false> g;
   g.lane = threadIdx.x;
   g.size = blockDim.x;
-  const CkSmem s = ck_carve(smem_raw, p.width, 0, L2 ? 0 : 2);  // mode 0: bitmap only
+  const CkSmem s = ck_carve(smem_raw, p.width, 0, L2 ? 3 : 2);
   const int64_t words = (p.width + 31) / 32;
   const uint32_t width = static_cast<uint32_t>(p.width);
-  // the accumulator: shared memory, or (L2) this block's slice of an L2-resident global array
-  // updated with fire-and-forget reductions performed by the L2 atomic units
+  const int warp = threadIdx.x >> 5;
+  const int nwork = (blockDim.x >> 5) - 1;  // streaming warps 1..31
   double* acc = L2 ? gacc_all + static_cast<int64_t>(blockIdx.x) * p.width : s.vals;
-  {
-    if (L2) {
-      for (int64_t j = g.lane; j < p.width; j += g.size) __stcg(&acc[j], 0.0);
-    } else {
-      double2* v2 = reinterpret_cast<double2*>(acc);
-      for (int64_t j = g.lane; j < p.width / 2; j += g.size) v2[j] = make_double2(0.0, 0.0);
-      if ((p.width & 1) && g.lane == 0) acc[p.width - 1] = 0.0;
-    }
-    for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
+  double* my_hub = s.hub + (warp > 0 ? warp - 1 : 0) * kHubSlots;
+  if (L2) {
+    for (int64_t j = g.lane; j < p.width; j += g.size) __stcg(&acc[j], 0.0);
+  } else {
+    double2* v2 = reinterpret_cast<double2*>(acc);
+    for (int64_t j = g.lane; j < p.width / 2; j += g.size) v2[j] = make_double2(0.0, 0.0);
+    if ((p.width & 1) && g.lane == 0) acc[p.width - 1] = 0.0;
   }
-  // hub sums live in this block's slots of a small global array (L2 resident), zeroed here and
-  // left zeroed after every chunk
-  double* ghub = p.hub_all + static_cast<int64_t>(blockIdx.x) * kHubSlots;
-  for (int j = g.lane; j < kHubSlots; j += g.size) __stcg(&ghub[j], 0.0);
-  for (;;) {
-    __threadfence_block();
-    __syncthreads();
-    if (threadIdx.x == 0) s_item = atomicAdd(next, 1);
-    __syncthreads();
-    const int64_t item = s_item;
-    if (item >= p.count) break;
-    const int64_t q = p.list[item];
-    const int64_t grow = p.cs.heavy_rows[p.cs.row[q]];
-    if (grow < p.sink.row_begin || grow >= p.sink.row_end) continue;
-    const int64_t start = p.cs.start[q];
-    const int64_t cnt = p.cs.cnt[q];
-    const int32_t* col = p.cs.col + start;
-    const double* val = p.cs.val + start;
-    constexpr int U = 8;
-    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
-      int32_t cr[U];
-      double vr[U];
+  for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
+  for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
+  if (threadIdx.x == 0) dense_fetch(p, next, &jobs[0]);
+  __syncthreads();
+  for (int buf = 0;; buf ^= 1) {
+    const DenseJob job = jobs[buf];
+    if (job.state == 0) break;
+    if (warp == 0) {
+      if (threadIdx.x == 0) dense_fetch(p, next, &jobs[buf ^ 1]);  // overlaps the stream below
+    } else if (job.state == 1) {
+      const int32_t* col = p.cs.col + job.start;
+      const double* val = p.cs.val + job.start;
+      const int64_t cnt = job.cnt;
+      const int nt = nwork * 32;
+      const int t = threadIdx.x - 32;
+      constexpr int U = 8;
+      for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(nt) * U) {
+        int32_t cr[U];
+        double vr[U];
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
-        cr[j] = -1;
-        vr[j] = 0.0;
-        if (f < cnt) {
-          cr[j] = __ldcs(col + f);
-          vr[j] = __ldcs(val + f);
+        for (int j = 0; j < U; ++j) {
+          const int64_t f = f0 + static_cast<int64_t>(j) * nt + t;
+          cr[j] = -1;
+          vr[j] = 0.0;
+          if (f < cnt) {
+            cr[j] = __ldcs(col + f);
+            vr[j] = __ldcs(val + f);
+          }
         }
-      }
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int32_t c = cr[j];
-        if (c < 0) continue;
-        if (static_cast<uint32_t>(c) < width) {
-          atomicOr(&s.bits[c >> 5], 1u << (c & 31));
-          const int hi = hub_index(static_cast<uint32_t>(c));
-          if (hi >= 0) atomicAdd(&ghub[hi], vr[j]);  // L2 reduction, no retry loop
-          else atomicAdd(&acc[c], vr[j]);
-        } else {
-          set_error(p.err, kErrBounds);
+        for (int j = 0; j < U; ++j) {
+          const int32_t c = cr[j];
+          if (c < 0) continue;
+          if (static_cast<uint32_t>(c) < width) {
+            atomicOr(&s.bits[c >> 5], 1u << (c & 31));
+            const int hi = hub_index(static_cast<uint32_t>(c));
+            if (L2) {
+              if (hi >= 0) atomicAdd(&my_hub[hi], vr[j]);
+              else atomicAdd(&acc[c], vr[j]);
+            } else {
+              atomicAdd(hi >= 0 ? &my_hub[hi] : &acc[c], vr[j]);  // one shared atomic, address selected
+            }
+          } else {
+            set_error(p.err, kErrBounds);
+          }
         }
-      }
-    }
-    __threadfence_block();
-    __syncthreads();
-    for (int j = g.lane; j < kHubSlots; j += g.size) {
-      const uint32_t c = hub_column(j);
-      if (c < width) {
-        const double sum = __ldcg(&ghub[j]);
-        __stcg(&ghub[j], 0.0);
-        if (L2) __stcg(&acc[c], __ldcg(&acc[c]) + sum); else acc[c] += sum;
       }
     }
     if (L2) __threadfence_block();
     __syncthreads();
-    const int64_t out = p.sink.row_ptr[grow] + p.cs.out[q] - p.sink.row_ptr[p.sink.row_begin];
-    const int64_t expected = p.cs.nnz[q];
-    int32_t* c_col = p.sink.c_col + out;
-    double* c_val = p.sink.c_val + out;
-    const int32_t base = p.cs.base[q];
-    int64_t written = 0;
-    for (int64_t w0 = 0; w0 < words; w0 += g.size) {
-      const int64_t w = w0 + g.lane;
-      const uint32_t bits = w < words ? s.bits[w] : 0u;
-      const int64_t c = __popc(bits);
-      int64_t tot;
-      const int64_t incl = ck_scan<false>(g, c, s.tmp, &tot);
-      int64_t pos = written + incl - c;
-      uint32_t b = bits;
-      while (b) {
-        const int bit = __ffs(b) - 1;
-        b &= b - 1;
-        const int32_t idx = static_cast<int32_t>(w * 32 + bit);
-        if (pos < expected) {
-          c_col[pos] = idx + base;
-          c_val[pos] = L2 ? __ldcg(&acc[idx]) : acc[idx];
+    if (job.state == 1) {
+      // fold the warps' hub sums into the value array
+      for (int j = g.lane; j < kHubSlots; j += g.size) {
+        const uint32_t c = hub_column(j);
+        double sum = 0.0;
+        for (int w = 0; w < nwork; ++w) {
+          sum += s.hub[w * kHubSlots + j];
+          s.hub[w * kHubSlots + j] = 0.0;
         }
-        if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed for the next chunk
-        ++pos;
+        if (c < width && sum != 0.0) {
+          if (L2) __stcg(&acc[c], __ldcg(&acc[c]) + sum); else acc[c] += sum;
+        }
       }
-      if (w < words) s.bits[w] = 0u;
-      written += tot;
+      if (L2) __threadfence_block();
+      __syncthreads();
+      int32_t* c_col = p.sink.c_col + job.out;
+      double* c_val = p.sink.c_val + job.out;
+      int64_t written = 0;
+      for (int64_t w0 = 0; w0 < words; w0 += g.size) {
+        const int64_t w = w0 + g.lane;
+        const uint32_t bits = w < words ? s.bits[w] : 0u;
+        const int64_t c = __popc(bits);
+        int64_t tot;
+        const int64_t incl = ck_scan<false>(g, c, s.tmp, &tot);
+        int64_t pos = written + incl - c;
+        uint32_t b = bits;
+        while (b) {
+          const int bit = __ffs(b) - 1;
+          b &= b - 1;
+          const int32_t idx = static_cast<int32_t>(w * 32 + bit);
+          if (pos < job.expected) {
+            c_col[pos] = idx + job.base;
+            c_val[pos] = L2 ? __ldcg(&acc[idx]) : acc[idx];
+          }
+          if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed
+          ++pos;
+        }
+        if (w < words) s.bits[w] = 0u;
+        written += tot;
+      }
+      if (written != job.expected && g.lane == 0) set_error(p.err, kErrRowOverflow);
     }
-    if (written != expected && g.lane == 0) set_error(p.err, kErrRowOverflow);
+    __syncthreads();
   }
 }
 
@@ -543,7 +583,7 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
     cudaMemsetAsync(counter, 0, sizeof(int), s);
     note_launch();
     if (gacc) {  // L2-resident accumulators: the shared array is not needed
-      const size_t smem = chunk_smem_bytes(width, 0, 0, false);
+      const size_t smem = chunk_smem_bytes(width, 0, 3, false);
       cudaFuncSetAttribute(k_chunk_dense<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       k_chunk_dense<true><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, gacc);
     } else {

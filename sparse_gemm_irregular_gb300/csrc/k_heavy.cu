@@ -153,13 +153,17 @@ struct OpSmem {
   int64_t a_first, nent;
 };
 
-template <bool VALS>
+// With `counts` set, the kernel also produces the level-0 histogram of C^ (elements per
+// (row, chunk), chunk = column >> shift): lanes of a warp that write the same (entry, chunk)
+// combine their counts with __match_any_sync and the leader adds them to the global counter,
+// which saves a separate pass over the columns of C^.
+template <bool VALS, bool HIST>
 __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     const int64_t* __restrict__ colptr, const int32_t* __restrict__ crow, const double* __restrict__ cval,
     const int64_t* __restrict__ slice_off, const int2* __restrict__ part, int64_t total,
     const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol, const double* __restrict__ bval,
     unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col, double* __restrict__ out_val,
-    uint32_t* err) {
+    unsigned long long* __restrict__ counts, int shift, int64_t v, uint32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
   __shared__ OpSmem hdr;
   int64_t* dst_delta = reinterpret_cast<int64_t*>(smem_raw);
@@ -206,9 +210,8 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
   // Step 3: populate C^, consecutive threads -> consecutive elements of a B row
   const int32_t n = static_cast<int32_t>(g1 - g0);
   int32_t p = threadIdx.x;
-  if (p >= n) return;
-  int32_t e;
-  {
+  int32_t e = 0;
+  if (p < n) {
     int32_t lo = 0, hi = static_cast<int32_t>(nent) - 1;
     while (lo < hi) {  // last entry with seg_start <= p
       const int32_t mid = (lo + hi + 1) >> 1;
@@ -216,36 +219,62 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     }
     e = lo;
   }
-  for (; p < n; p += blockDim.x) {
-    while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
-    const int64_t src = src_delta[e] + p;
-    const int64_t dst = dst_delta[e] + p;
-    out_col[dst] = bcol[src];
-    if (VALS) out_val[dst] = __ldg(&cval[a_first + e]) * bval[src];
+  if (!HIST) {
+    for (; p < n; p += blockDim.x) {
+      while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
+      const int64_t src = src_delta[e] + p;
+      const int64_t dst = dst_delta[e] + p;
+      out_col[dst] = bcol[src];
+      if (VALS) out_val[dst] = __ldg(&cval[a_first + e]) * bval[src];
+    }
+    return;
+  }
+  // uniform trip count across the block so that every lane can join the warp match
+  for (int32_t p0 = 0; p0 < n; p0 += blockDim.x) {
+    p = p0 + static_cast<int32_t>(threadIdx.x);
+    int key = -1;
+    int64_t row = 0;
+    if (p < n) {
+      while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
+      const int64_t src = src_delta[e] + p;
+      const int64_t dst = dst_delta[e] + p;
+      const int32_t c = bcol[src];
+      out_col[dst] = c;
+      if (VALS) out_val[dst] = __ldg(&cval[a_first + e]) * bval[src];
+      const int64_t ch = static_cast<int64_t>(c) >> shift;
+      row = crow[a_first + e];
+      if (ch < v) key = static_cast<int>(e * v + ch);
+      else set_error(err, kErrBounds);
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (peers & lanemask_lt()) == 0)
+      atomicAdd(&counts[row * v + key % v], static_cast<unsigned long long>(__popc(peers)));
   }
 }
 
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
                           const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
                           int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
-                          uint32_t* err, cudaStream_t s) {
+                          unsigned long long* counts, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s) {
   if (total == 0) return;
   const size_t smem = kOpTile * (8 + 8 + 4);
   const unsigned grid = static_cast<unsigned>(ceil_div(total, kOpTile));
   auto* ull = reinterpret_cast<unsigned long long*>(row_cursor);
+#define SG_OP(V, H)                                                                                          \
+  do {                                                                                                      \
+    cudaFuncSetAttribute(k_outer_product<V, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
+                         static_cast<int>(smem));                                                           \
+    note_launch();                                                                                          \
+    k_outer_product<V, H><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,  \
+                                                         B.row_ptr, B.col_idx, B.vals, ull, chat_col,        \
+                                                         V ? chat_val : nullptr, counts, shift, nchunks, err); \
+  } while (0)
   if (with_vals) {
-    cudaFuncSetAttribute(k_outer_product<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    note_launch();
-    k_outer_product<true><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,
-                                                         B.row_ptr, B.col_idx, B.vals, ull, chat_col, chat_val,
-                                                         err);
+    if (counts) SG_OP(true, true); else SG_OP(true, false);
   } else {
-    cudaFuncSetAttribute(k_outer_product<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    note_launch();
-    k_outer_product<false><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,
-                                                          B.row_ptr, B.col_idx, B.vals, ull, chat_col, nullptr,
-                                                          err);
+    if (counts) SG_OP(false, true); else SG_OP(false, false);
   }
+#undef SG_OP
 }
 
 // ---- histogram and multisplit (Algorithm 5) -----------------------------------------------------
