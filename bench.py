@@ -227,6 +227,7 @@ def main():
     ap.add_argument("--rmat-scale", type=int, default=0,
                     help="replace the workload by a seeded R-MAT of this scale (small cases for profiling)")
     ap.add_argument("--edge-factor", type=int, default=16)
+    ap.add_argument("--no-variants", action="store_true", help="skip the direct-split variant measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -343,6 +344,29 @@ def main():
         "clocks": clk.summary(),
         "step_ms": step_ms,
     }
+
+    # the same product on the direct-split path (SPGEMM_FLAG_DIRECT_SPLIT), measured the same way
+    if not args.no_variants:
+        vopt = sg.options(flags=sg.binding.FLAG_TIMING | sg.binding.FLAG_DIRECT_SPLIT | args.flags,
+                          chunk_width=args.chunk_width, tau=args.tau)
+        for _ in range(2):
+            step(vopt)
+        torch.cuda.synchronize()
+        vms, vph = [], {}
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            _, ph = step(vopt)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            vms.append(a_.elapsed_time(b_))
+            for k_, (ms, n_) in ph.items():
+                vph[k_] = vph.get(k_, 0.0) + ms
+        result["variants"] = {"direct_split": {
+            "value": 2.0 * ip * args.steps * world / (sum(vms) / 1e3) / 1e9, "unit": UNIT,
+            "ms_per_step": sum(vms) / args.steps,
+            "phases_ms_per_step": {k_: v / args.steps for k_, v in vph.items() if v > 0}}}
 
     # end to end through the public API with host buffers
     if not args.no_e2e:

@@ -60,6 +60,9 @@ extern "C" {
                                          __match_any_sync warp aggregation */
 #define SPGEMM_FLAG_DENSE_L2 128      /* heavy dense chunks sum with L2 reductions into a global
                                          per-SM array instead of shared-memory atomics */
+#define SPGEMM_FLAG_DIRECT_SPLIT 256  /* one-level plans: the outer product writes straight into
+                                         C^_reord (counts from per-B-row chunk histograms), so C^
+                                         is never stored and level 0 needs no multisplit pass */
 
 /* A CSR matrix in device memory, borrowed by the library (never written or freed). */
 typedef struct {

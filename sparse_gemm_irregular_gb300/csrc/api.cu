@@ -446,6 +446,97 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
   return SPGEMM_OK;
 }
 
+// Heavy batch, direct split (SPGEMM_FLAG_DIRECT_SPLIT, one-level plans): the per-(row, chunk)
+// counts come from per-B-row chunk histograms, and the outer product writes every element straight
+// into its C^_reord row, so C^ never reaches global memory and level 0 needs no multisplit pass.
+int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
+  const spgemm_plan& P = h->plan;
+  const int64_t R = hb.h1 - hb.h0;
+  const int32_t* rows = h->d_heavy + hb.h0;
+  const int64_t kc = h->k;
+  const int64_t v = P.v_chunks[0];
+  const int64_t width = P.chunk_width;
+  const int shift = ilog2_i64(width);
+  std::unique_ptr<PhaseTimer> tcsc(new PhaseTimer(h, 2));
+  int32_t* colcnt;
+  int64_t *colptr, *slice_off;
+  SG_ALLOC(colcnt, int32_t, kc);
+  SG_ALLOC(colptr, int64_t, kc + 1);
+  SG_ALLOC(slice_off, int64_t, kc + 1);
+  cudaMemsetAsync(colcnt, 0, sizeof(int32_t) * kc, h->st);
+  launch_csc_count(h->A, rows, R, colcnt, h->st);
+  launch_slice_sizes(colcnt, h->B, kc, colptr, slice_off, h->st);
+  SG_TRY(scan(h, colptr, colptr, kc));
+  SG_TRY(scan(h, slice_off, slice_off, kc));
+  int64_t nnzh = 0;
+  SG_TRY(check_cuda(cudaMemcpyAsync(&nnzh, colptr + kc, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy masked nnz"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "masked csc"));
+  int32_t* csc_row;
+  double* csc_val;
+  int64_t* cursor;
+  SG_ALLOC(csc_row, int32_t, nnzh);
+  SG_ALLOC(csc_val, double, nnzh);
+  SG_ALLOC(cursor, int64_t, std::max<int64_t>(kc, R * v));
+  launch_copy_i64(colptr, cursor, kc, h->st);
+  launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, h->st);
+  // level-0 histogram from the chunk histograms of the rows of B
+  int32_t* bh;
+  unsigned long long* counts;
+  int64_t* rptr;
+  int32_t *out_row, *out_base;
+  const int64_t nout = R * v;
+  SG_ALLOC(bh, int32_t, kc * v);
+  SG_ALLOC(counts, unsigned long long, nout);
+  SG_ALLOC(rptr, int64_t, nout + 1);
+  SG_ALLOC(out_row, int32_t, nout);
+  SG_ALLOC(out_base, int32_t, nout);
+  cudaMemsetAsync(bh, 0, sizeof(int32_t) * kc * v, h->st);
+  launch_b_chunk_hist(h->B, colcnt, shift, v, bh, h->d_err, h->st);
+  launch_row_chunk_counts(h->A, rows, R, bh, v, counts, h->st);
+  launch_reord_meta(counts, R, v, nullptr, nullptr, nullptr, width, rptr, out_row, out_base, h->st);
+  SG_TRY(scan(h, rptr, rptr, nout));
+  launch_copy_i64(rptr, cursor, nout, h->st);
+  int2* part;
+  SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(hb.elems, kOpTile)));
+  launch_partition(slice_off, kc, hb.elems, kOpTile, part, h->st);
+  tcsc.reset();
+  {
+    PhaseTimer t(h, 3);
+    launch_outer_direct(colptr, csc_row, csc_val, slice_off, part, hb.elems, h->B, nullptr,
+                        reinterpret_cast<unsigned long long*>(cursor), h->d_chat_col,
+                        vals ? h->d_chat_val : nullptr, vals, shift, v, h->d_err, h->st);
+  }
+  if (record) {
+    hb.lv.clear();
+    LevelInfo li;
+    li.nin = R;
+    li.v = v;
+    li.width = width;
+    li.nheavy = 0;
+    li.desc0 = 0;
+    li.elem_base = 0;
+    hb.lv.push_back(li);
+    hb.nfinal = nout;
+    hb.bitmap_from = 0;
+    SG_ALLOC(hb.f_start, int64_t, nout);
+    SG_ALLOC(hb.f_cnt, int64_t, nout);
+    SG_ALLOC(hb.f_row, int32_t, nout);
+    SG_ALLOC(hb.f_base, int32_t, nout);
+    launch_final_desc(rptr, 0, nout, 0, out_row, out_base, hb.f_start, hb.f_cnt, hb.f_row, hb.f_base, h->st);
+  }
+  for (void* p : {static_cast<void*>(colcnt), static_cast<void*>(colptr), static_cast<void*>(slice_off),
+                  static_cast<void*>(csc_row), static_cast<void*>(csc_val), static_cast<void*>(cursor),
+                  static_cast<void*>(bh), static_cast<void*>(counts), static_cast<void*>(rptr),
+                  static_cast<void*>(out_row), static_cast<void*>(out_base), static_cast<void*>(part)})
+    ws_free(h, p);
+  return SPGEMM_OK;
+}
+
+bool use_direct(const spgemm_ctx* h) {
+  return (h->opt.flags & SPGEMM_FLAG_DIRECT_SPLIT) && h->plan.levels == 1 && h->plan.chunks_required > 1;
+}
+
 // Accumulator bins of the final chunks (stable order), then their symbolic counts and the
 // offsets of every chunk inside its row of C.
 int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
@@ -614,11 +705,15 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
       SG_TRY(ensure_chat(h, true));
       int64_t* crp;
       SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
-      unsigned long long* counts0 = nullptr;
-      SG_TRY(alloc_counts0(h, hb, &counts0));
-      SG_TRY(heavy_expand(h, hb, true, crp, counts0));
-      SG_TRY(heavy_levels(h, hb, true, false, crp, counts0));
-      if (counts0) ws_free(h, counts0);
+      if (use_direct(h)) {
+        SG_TRY(heavy_direct(h, hb, true, false));
+      } else {
+        unsigned long long* counts0 = nullptr;
+        SG_TRY(alloc_counts0(h, hb, &counts0));
+        SG_TRY(heavy_expand(h, hb, true, crp, counts0));
+        SG_TRY(heavy_levels(h, hb, true, false, crp, counts0));
+        if (counts0) ws_free(h, counts0);
+      }
       SG_TRY(heavy_chunk_numeric(h, hb, sk));
       ws_free(h, crp);
     } else {
@@ -851,11 +946,15 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     SG_TRY(ensure_chat(h, vals));
     int64_t* crp;
     SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
-    unsigned long long* counts0 = nullptr;
-    SG_TRY(alloc_counts0(h, hb, &counts0));
-    SG_TRY(heavy_expand(h, hb, vals, crp, counts0));
-    SG_TRY(heavy_levels(h, hb, vals, true, crp, counts0));
-    if (counts0) ws_free(h, counts0);
+    if (use_direct(h)) {
+      SG_TRY(heavy_direct(h, hb, vals, true));
+    } else {
+      unsigned long long* counts0 = nullptr;
+      SG_TRY(alloc_counts0(h, hb, &counts0));
+      SG_TRY(heavy_expand(h, hb, vals, crp, counts0));
+      SG_TRY(heavy_levels(h, hb, vals, true, crp, counts0));
+      if (counts0) ws_free(h, counts0);
+    }
     SG_TRY(heavy_chunk_symbolic(h, hb, c_row_ptr));
     ws_free(h, crp);
     levels = std::max<int64_t>(levels, static_cast<int64_t>(hb.lv.size()));

@@ -119,6 +119,14 @@ void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t 
                         int64_t* cursor, int32_t* csc_row, double* csc_val, cudaStream_t s);
 void launch_copy_i64(const int64_t* src, int64_t* dst, int64_t n, cudaStream_t s);
 void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t tile, int2* part, cudaStream_t s);
+void launch_b_chunk_hist(const spgemm_csr& B, const int32_t* colcnt, int shift, int64_t v, int32_t* bh, uint32_t* err,
+                         cudaStream_t s);
+void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int32_t* bh, int64_t v,
+                             unsigned long long* counts, cudaStream_t s);
+void launch_outer_direct(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
+                         const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
+                         const int32_t* xmap, unsigned long long* cursor, int32_t* out_col, double* out_val,
+                         bool with_vals, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s);
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
                           const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
                           int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,

@@ -277,6 +277,162 @@ void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const d
 #undef SG_OP
 }
 
+// ---- direct split of level 0 (optional path, SPGEMM_FLAG_DIRECT_SPLIT) ---------------------------
+// Chunk histogram of the rows of B: bh[k * v + c] = entries of row k in chunk c (column >> shift).
+// Only rows used by heavy A entries (colcnt[k] > 0) are counted.
+__global__ void k_b_chunk_hist(const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol, int64_t krows,
+                               const int32_t* __restrict__ colcnt, int shift, int64_t v, int32_t* __restrict__ bh,
+                               uint32_t* err) {
+  const int64_t k = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (k >= krows || colcnt[k] == 0) return;
+  for (int64_t q = brp[k] + lane_id(); q < brp[k + 1]; q += 32) {
+    const int64_t c = static_cast<int64_t>(bcol[q]) >> shift;
+    if (c < v) atomicAdd(&bh[k * v + c], 1);
+    else set_error(err, kErrBounds);
+  }
+}
+void launch_b_chunk_hist(const spgemm_csr& B, const int32_t* colcnt, int shift, int64_t v, int32_t* bh, uint32_t* err,
+                         cudaStream_t s) {
+  if (B.rows == 0) return;
+  note_launch();
+  k_b_chunk_hist<<<static_cast<unsigned>(ceil_div(B.rows * 32, 256)), 256, 0, s>>>(B.row_ptr, B.col_idx, B.rows,
+                                                                                   colcnt, shift, v, bh, err);
+}
+
+// counts[r * v + c] = sum over the entries A[row r, k] of bh[k * v + c]: the level-0 histogram of
+// C^ without forming C^.  One thread per (heavy row, chunk).
+__global__ void k_row_chunk_counts(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
+                                   const int32_t* __restrict__ rows, int64_t nrows, const int32_t* __restrict__ bh,
+                                   int64_t v, unsigned long long* __restrict__ counts) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= nrows * v) return;
+  const int64_t r = t / v, c = t % v;
+  const int64_t row = rows[r];
+  unsigned long long sum = 0;
+  for (int64_t e = arp[row]; e < arp[row + 1]; ++e) sum += static_cast<unsigned long long>(bh[acol[e] * v + c]);
+  counts[t] = sum;
+}
+void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int32_t* bh, int64_t v,
+                             unsigned long long* counts, cudaStream_t s) {
+  if (nrows == 0) return;
+  note_launch();
+  k_row_chunk_counts<<<static_cast<unsigned>(ceil_div(nrows * v, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows,
+                                                                                     nrows, bh, v, counts);
+}
+
+// Outer product writing straight into C^_reord: the same static partition as Algorithm 4, but each
+// run of consecutive elements that belong to one (entry, chunk) reserves its space with one
+// atomic on that C^_reord row's cursor (warp runs found with __match_any_sync) and is written
+// with the column shifted into the chunk's range.
+template <bool VALS>
+__global__ void __launch_bounds__(kOpThreads) k_outer_direct(
+    const int64_t* __restrict__ colptr, const int32_t* __restrict__ crow, const double* __restrict__ cval,
+    const int64_t* __restrict__ slice_off, const int2* __restrict__ part, int64_t total,
+    const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol, const double* __restrict__ bval,
+    const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
+    double* __restrict__ out_val, int shift, int64_t v, uint32_t* err) {
+  extern __shared__ __align__(16) char smem_raw[];
+  __shared__ int64_t hdr[2];
+  int64_t* src_delta = reinterpret_cast<int64_t*>(smem_raw);
+  int32_t* seg_start = reinterpret_cast<int32_t*>(src_delta + kOpTile);
+  int32_t* seg_row = seg_start + kOpTile;
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kOpTile;
+  const int64_t g1 = min(total, g0 + kOpTile);
+  const int2 sp = part[blockIdx.x];
+  const int64_t s0 = sp.x, s1 = sp.y;
+  if (threadIdx.x == 0) {
+    const int64_t len0 = brp[s0 + 1] - brp[s0];
+    const int64_t len1 = brp[s1 + 1] - brp[s1];
+    const int64_t a_first = colptr[s0] + (g0 - slice_off[s0]) / len0;
+    const int64_t a_last = colptr[s1] + (g1 - 1 - slice_off[s1]) / len1;
+    hdr[0] = a_first;
+    hdr[1] = a_last - a_first + 1;
+  }
+  __syncthreads();
+  const int64_t a_first = hdr[0], nent = hdr[1];
+  if (nent > kOpTile || nent <= 0) {
+    if (threadIdx.x == 0) set_error(err, kErrBounds);
+    return;
+  }
+  for (int64_t e = threadIdx.x; e < nent; e += blockDim.x) {
+    const int64_t a = a_first + e;
+    const int64_t s = (s0 == s1) ? s0 : upper_bound_minus1(colptr, s0, s1 + 1, a);
+    const int64_t b0 = brp[s];
+    const int64_t len = brp[s + 1] - b0;
+    const int64_t F = slice_off[s] + (a - colptr[s]) * len;
+    const int64_t lo = max(F, g0);
+    const int64_t clo = lo < g1 ? lo : g1;
+    seg_start[e] = static_cast<int32_t>(clo - g0);
+    src_delta[e] = b0 + (clo - F) - (clo - g0);
+    seg_row[e] = crow[a];
+  }
+  __syncthreads();
+  const int32_t n = static_cast<int32_t>(g1 - g0);
+  const int64_t wmask = (int64_t(1) << shift) - 1;
+  int32_t e = 0;
+  if (static_cast<int32_t>(threadIdx.x) < n) {
+    int32_t lo = 0, hi = static_cast<int32_t>(nent) - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (seg_start[mid] <= static_cast<int32_t>(threadIdx.x)) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+  }
+  for (int32_t p0 = 0; p0 < n; p0 += blockDim.x) {
+    const int32_t p = p0 + static_cast<int32_t>(threadIdx.x);
+    int key = -1;
+    int32_t c = 0;
+    double val = 0.0;
+    int64_t q = 0;
+    if (p < n) {
+      while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
+      const int64_t src = src_delta[e] + p;
+      c = bcol[src];
+      if (VALS) val = __ldg(&cval[a_first + e]) * bval[src];
+      const int64_t ch = static_cast<int64_t>(c) >> shift;
+      if (ch < v) {
+        key = static_cast<int>(e * v + ch);
+        const int64_t gid = static_cast<int64_t>(seg_row[e]) * v + ch;
+        q = xmap ? xmap[gid] : gid;
+      } else {
+        set_error(err, kErrBounds);
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(peers) - 1;
+    unsigned long long base = 0;
+    if (key >= 0 && static_cast<int>(lane_id()) == leader)
+      base = atomicAdd(&cursor[q], static_cast<unsigned long long>(__popc(peers)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (key >= 0) {
+      const int64_t dst = static_cast<int64_t>(base) + __popc(peers & lanemask_lt());
+      out_col[dst] = static_cast<int32_t>(c & wmask);
+      if (VALS) out_val[dst] = val;
+    }
+  }
+}
+
+void launch_outer_direct(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
+                         const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
+                         const int32_t* xmap, unsigned long long* cursor, int32_t* out_col, double* out_val,
+                         bool with_vals, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s) {
+  if (total == 0) return;
+  const size_t smem = kOpTile * (8 + 4 + 4);
+  const unsigned grid = static_cast<unsigned>(ceil_div(total, kOpTile));
+  note_launch();
+  if (with_vals) {
+    cudaFuncSetAttribute(k_outer_direct<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_outer_direct<true><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total, B.row_ptr,
+                                                        B.col_idx, B.vals, xmap, cursor, out_col, out_val, shift,
+                                                        nchunks, err);
+  } else {
+    cudaFuncSetAttribute(k_outer_direct<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_outer_direct<false><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,
+                                                         B.row_ptr, B.col_idx, B.vals, xmap, cursor, out_col, nullptr,
+                                                         shift, nchunks, err);
+  }
+}
+
 // ---- histogram and multisplit (Algorithm 5) -----------------------------------------------------
 // Both kernels use the same static partition: block b owns elements [b*kMsTile, (b+1)*kMsTile),
 // each thread 8 consecutive ones (loaded as 16-byte vectors when the tile is full), and the rows

@@ -43,6 +43,10 @@ FORCED = [
     dict(tau=16, chunk_width=64, chunks_max=4, heavy_batch_elems=700, flags=16),
     # light rows only, hash accumulators
     dict(flags=2 | 4, tau=4096),
+    # direct split of level 0 (outer product writes C^_reord), one level of 8 chunks
+    dict(flags=256, tau=16, chunk_width=64, chunks_max=16),
+    dict(flags=256 | 1, tau=64, chunk_width=64, chunks_max=8),
+    dict(flags=256 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
 ]
 
 
@@ -70,11 +74,13 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-def test_rmat_small_full(gpu_lib):
+@pytest.mark.parametrize("flags", [0, 256])
+def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
-    row, thousands of light rows in every ladder bin -- compared in full."""
+    row, thousands of light rows in every ladder bin -- compared in full (multisplit path and
+    direct split)."""
     A = synth.rmat(14, 16, seed=5)
-    rp, col, val, st = gpu_product(A, A)
+    rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
     assert st.rows_heavy > 0 and st.rows_light > 0
     compare_full(A, A, rp, col, val, threads=16)
 
@@ -118,9 +124,10 @@ def sample_rows(A, B, n_top=300, n_uniform=3000, seed=0):
     return np.unique(np.concatenate([top, uni]))
 
 
-def test_config3_full_size_sampled(gpu_lib):
+@pytest.mark.parametrize("flags", [0, 256])
+def test_config3_full_size_sampled(gpu_lib, flags):
     A = synth.config(3)
-    p, rp, col, val = gpu_product_device(A, A)
+    p, rp, col, val = gpu_product_device(A, A, opts(flags=flags) if flags else None)
     st = p.stats()
     assert st.rows_heavy > 0 and st.resident == 1
     rowsum, _ = device_invariants(A, A, rp, col, val)
@@ -130,9 +137,10 @@ def test_config3_full_size_sampled(gpu_lib):
     release_device_memory()
 
 
-def test_config5_full_size_sampled(gpu_lib):
+@pytest.mark.parametrize("flags", [0, 256])
+def test_config5_full_size_sampled(gpu_lib, flags):
     M = synth.config(5)
-    p, rp, col, val = gpu_product_device(M, M)
+    p, rp, col, val = gpu_product_device(M, M, opts(flags=flags) if flags else None)
     st = p.stats()
     assert st.rows_heavy > 0
     _, colsum = device_invariants(M, M, rp, col, val)
