@@ -668,13 +668,59 @@ void join_light(spgemm_ctx* h) {
   cudaStreamWaitEvent(h->st, h->ev_join, 0);
 }
 
+// Numeric bins of the light hash rows by their exact nnz (once per handle, after symbolic).
+int numeric_bins(spgemm_ctx* h) {
+  if (!h->nbin_start.empty()) return SPGEMM_OK;
+  const int nl = h->lad.n;
+  int64_t nh = 0;
+  for (int L = 0; L < nl; ++L) nh += h->bin_start[2 * L + 1] - h->bin_start[2 * L];
+  h->nbin_start.assign(nl + 1, 0);
+  if (nh == 0) return SPGEMM_OK;
+  int32_t* all;
+  uint8_t* bin;
+  int64_t *cnt, *starts;
+  const int64_t nblk = bin_blocks(nh);
+  SG_ALLOC(all, int32_t, nh);
+  SG_ALLOC(h->d_nrows, int32_t, nh);
+  SG_ALLOC(bin, uint8_t, nh);
+  SG_ALLOC(cnt, int64_t, nl * nblk + 1);
+  SG_ALLOC(starts, int64_t, nl + 1);
+  int64_t off = 0;
+  for (int L = 0; L < nl; ++L) {
+    const int64_t c = h->bin_start[2 * L + 1] - h->bin_start[2 * L];
+    if (c) cudaMemcpyAsync(all + off, h->d_rows + h->bin_start[2 * L], sizeof(int32_t) * c, cudaMemcpyDeviceToDevice,
+                           h->st);
+    off += c;
+  }
+  launch_nnz_bins(all, nh, h->c_row_ptr, h->rule, bin, h->st);
+  launch_bin_count(bin, nh, nl, cnt, h->st);
+  SG_TRY(scan(h, cnt, cnt, nl * nblk));
+  // the scatter writes positions into the concatenated list; map them back to row ids
+  launch_bin_scatter(bin, nh, nl, cnt, h->d_nrows, h->st);
+  launch_gather_rows(all, h->d_nrows, nh, h->st);
+  launch_bin_starts(cnt, nblk, nl, starts, h->st);
+  SG_TRY(check_cuda(cudaMemcpyAsync(h->nbin_start.data(), starts, sizeof(int64_t) * (nl + 1), cudaMemcpyDeviceToHost,
+                                    h->st), "copy numeric bins"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "numeric bins"));
+  ws_free(h, all);
+  ws_free(h, bin);
+  ws_free(h, cnt);
+  ws_free(h, starts);
+  return SPGEMM_OK;
+}
+
 void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
   for (int L = 0; L < h->lad.n; ++L) {
     for (int d = 0; d < 2; ++d) {
       const int b = 2 * L + d;
       RowJob job;
-      job.rows = h->d_rows + h->bin_start[b];
-      job.count = h->bin_start[b + 1] - h->bin_start[b];
+      if (numeric && d == 0) {  // hash rows: numeric bins by exact size
+        job.rows = h->d_nrows + h->nbin_start[L];
+        job.count = h->nbin_start[L + 1] - h->nbin_start[L];
+      } else {
+        job.rows = h->d_rows + h->bin_start[b];
+        job.count = h->bin_start[b + 1] - h->bin_start[b];
+      }
       job.slots = h->lad.slots[L];
       job.tpr = h->lad.tpr[L];
       job.dense = d == 1;
@@ -694,6 +740,7 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
   sk.c_val = c_val;
   sk.row_begin = rb;
   sk.row_end = re;
+  SG_TRY(numeric_bins(h));
   fork_light(h);
   {
     PhaseTimer t(h, 10, h->st_light);

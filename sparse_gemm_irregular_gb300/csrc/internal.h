@@ -72,6 +72,8 @@ void launch_bin_scatter(const uint8_t* bin, int64_t n, int nbins, const int64_t*
                         int32_t* out, cudaStream_t s);
 void launch_bin_starts(const int64_t* off, int64_t nblk, int nbins, int64_t* starts, cudaStream_t s);
 void launch_validate(const spgemm_csr& M, uint32_t* err, cudaStream_t s);
+void launch_nnz_bins(const int32_t* rows, int64_t n, const int64_t* row_ptr, const BinRule& rule, uint8_t* bin,
+                     cudaStream_t s);
 
 // ---- light rows and chunk accumulators (k_accum.cu) ------------------------------------
 // Source of one accumulation: a light row of A*B, or a final chunk of C^_reord.
@@ -118,6 +120,7 @@ void launch_slice_sizes(const int32_t* colcnt, const spgemm_csr& B, int64_t kcol
 void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows,
                         int64_t* cursor, int32_t* csc_row, double* csc_val, cudaStream_t s);
 void launch_copy_i64(const int64_t* src, int64_t* dst, int64_t n, cudaStream_t s);
+void launch_gather_rows(const int32_t* src, int32_t* io, int64_t n, cudaStream_t s);
 void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t tile, int2* part, cudaStream_t s);
 void launch_b_chunk_hist(const spgemm_csr& B, const int32_t* colcnt, int shift, int64_t v, int32_t* bh, uint32_t* err,
                          cudaStream_t s);
@@ -230,6 +233,9 @@ struct spgemm_ctx {
   int32_t* d_rows = nullptr;    // concatenated stable bin lists
   int64_t* d_binoff = nullptr;
   std::vector<int64_t> bin_start;  // host copy (nbins + 1)
+  // numeric-phase bins of the light hash rows, by their exact size (built on the first numeric call)
+  int32_t* d_nrows = nullptr;
+  std::vector<int64_t> nbin_start;
 
   // heavy rows
   int64_t nheavy = 0;

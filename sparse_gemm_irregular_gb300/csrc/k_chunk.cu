@@ -427,7 +427,7 @@ __device__ __forceinline__ void dense_fetch(const CkParams& p, int* next, DenseJ
 template <bool L2>
 __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, double* gacc_all) {
   extern __shared__ __align__(16) char smem_raw[];
-  __shared__ DenseJob jobs[2];
+  __shared__ DenseJob jobs[3];  // current, next, and the one the helper is fetching
   CkGroup<false> g;
   g.lane = threadIdx.x;
   g.size = blockDim.x;
@@ -436,6 +436,8 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
   const uint32_t width = static_cast<uint32_t>(p.width);
   const int warp = threadIdx.x >> 5;
   const int nwork = (blockDim.x >> 5) - 1;  // streaming warps 1..31
+  const int nt = nwork * 32;
+  const int t = static_cast<int>(threadIdx.x) - 32;
   double* acc = L2 ? gacc_all + static_cast<int64_t>(blockIdx.x) * p.width : s.vals;
   double* my_hub = s.hub + (warp > 0 ? warp - 1 : 0) * kHubSlots;
   if (L2) {
@@ -447,45 +449,65 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
   }
   for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
   for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
-  if (threadIdx.x == 0) dense_fetch(p, next, &jobs[0]);
+  if (threadIdx.x == 0) {
+    dense_fetch(p, next, &jobs[0]);
+    if (jobs[0].state != 0) dense_fetch(p, next, &jobs[1]);
+    else jobs[1].state = 0;
+  }
   __syncthreads();
-  for (int buf = 0;; buf ^= 1) {
-    const DenseJob job = jobs[buf];
+  // streaming registers: batch b of the current chunk is loaded while batch b-1 is added
+  constexpr int U = 4;
+  int32_t cr[U];
+  double vr[U];
+  auto load_batch = [&](const DenseJob& jb, int64_t f0) {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t f = f0 + static_cast<int64_t>(j) * nt + t;
+      cr[j] = -1;
+      vr[j] = 0.0;
+      if (jb.state == 1 && f < jb.cnt) {
+        cr[j] = __ldcs(p.cs.col + jb.start + f);
+        vr[j] = __ldcs(p.cs.val + jb.start + f);
+      }
+    }
+  };
+  if (warp > 0) load_batch(jobs[0], 0);
+  for (int it = 0;; ++it) {
+    const DenseJob job = jobs[it % 3];
     if (job.state == 0) break;
     if (warp == 0) {
-      if (threadIdx.x == 0) dense_fetch(p, next, &jobs[buf ^ 1]);  // overlaps the stream below
-    } else if (job.state == 1) {
-      const int32_t* col = p.cs.col + job.start;
-      const double* val = p.cs.val + job.start;
-      const int64_t cnt = job.cnt;
-      const int nt = nwork * 32;
-      const int t = threadIdx.x - 32;
-      constexpr int U = 8;
-      for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(nt) * U) {
-        int32_t cr[U];
-        double vr[U];
+      if (threadIdx.x == 0) {
+        const DenseJob nx = jobs[(it + 1) % 3];
+        if (nx.state != 0) dense_fetch(p, next, &jobs[(it + 2) % 3]);
+        else jobs[(it + 2) % 3].state = 0;
+      }
+    } else {
+      const DenseJob nxt = jobs[(it + 1) % 3];
+      const int64_t step = static_cast<int64_t>(nt) * U;
+      const int64_t cnt = job.state == 1 ? job.cnt : 0;
+      for (int64_t f0 = 0; f0 < (cnt > 0 ? cnt : 1); f0 += step) {
+        int32_t c2[U];
+        double v2[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-          const int64_t f = f0 + static_cast<int64_t>(j) * nt + t;
-          cr[j] = -1;
-          vr[j] = 0.0;
-          if (f < cnt) {
-            cr[j] = __ldcs(col + f);
-            vr[j] = __ldcs(val + f);
-          }
+          c2[j] = cr[j];
+          v2[j] = vr[j];
         }
+        // next batch of this chunk, or the first batch of the next chunk
+        if (f0 + step < cnt) load_batch(job, f0 + step);
+        else load_batch(nxt, 0);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-          const int32_t c = cr[j];
+          const int32_t c = c2[j];
           if (c < 0) continue;
           if (static_cast<uint32_t>(c) < width) {
             atomicOr(&s.bits[c >> 5], 1u << (c & 31));
             const int hi = hub_index(static_cast<uint32_t>(c));
             if (L2) {
-              if (hi >= 0) atomicAdd(&my_hub[hi], vr[j]);
-              else atomicAdd(&acc[c], vr[j]);
+              if (hi >= 0) atomicAdd(&my_hub[hi], v2[j]);
+              else atomicAdd(&acc[c], v2[j]);
             } else {
-              atomicAdd(hi >= 0 ? &my_hub[hi] : &acc[c], vr[j]);  // one shared atomic, address selected
+              atomicAdd(hi >= 0 ? &my_hub[hi] : &acc[c], v2[j]);  // one shared atomic, address selected
             }
           } else {
             set_error(p.err, kErrBounds);

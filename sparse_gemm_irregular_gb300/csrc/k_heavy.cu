@@ -72,6 +72,17 @@ void launch_list_sums(const int32_t* list, int64_t n, const int64_t* a, const in
   k_list_sums<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n, 256), 1024)), 256, 0, s>>>(list, n, a, b, out);
 }
 
+// out[i] = src[out[i]]: turn positions of a concatenated list into its elements, in place.
+__global__ void k_gather_rows(const int32_t* __restrict__ src, int32_t* __restrict__ io, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) io[i] = src[io[i]];
+}
+void launch_gather_rows(const int32_t* src, int32_t* io, int64_t n, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_gather_rows<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(src, io, n);
+}
+
 // ---- masked CSR -> CSC of the heavy rows of A ------------------------------------------------
 __global__ void k_csc_count(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
                             const int32_t* __restrict__ rows, int64_t nrows, int32_t* __restrict__ cnt) {
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     }
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     if (key >= 0 && (peers & lanemask_lt()) == 0)
-      atomicAdd(&counts[row * v + key % v], static_cast<unsigned long long>(__popc(peers)));
+      atomicAdd(&counts[row * v + (key & (v - 1))], static_cast<unsigned long long>(__popc(peers)));
   }
 }
 

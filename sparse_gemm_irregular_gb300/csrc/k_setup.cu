@@ -190,6 +190,27 @@ void launch_bin_starts(const int64_t* off, int64_t nblk, int nbins, int64_t* sta
   k_bin_starts<<<1, 64, 0, s>>>(off, nblk, nbins, starts);
 }
 
+// ---- numeric bins of the light hash rows by their exact size -------------------------------
+// After the symbolic phase the size of every row of C is known; the numeric hash tables are then
+// sized by it (the Ocean page bins the numeric phase by output size), which for power-law rows
+// (two to three products per distinct column) shrinks the tables and raises occupancy.
+__global__ void k_nnz_bins(const int32_t* __restrict__ rows, int64_t n, const int64_t* __restrict__ rp,
+                           BinRule r, uint8_t* __restrict__ bin) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int64_t row = rows[i];
+  const int64_t nnz = rp[row + 1] - rp[row];
+  int L = 0;
+  while (L < r.n - 1 && nnz > r.upper[L]) ++L;
+  bin[i] = static_cast<uint8_t>(L);
+}
+void launch_nnz_bins(const int32_t* rows, int64_t n, const int64_t* row_ptr, const BinRule& rule, uint8_t* bin,
+                     cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_nnz_bins<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(rows, n, row_ptr, rule, bin);
+}
+
 // ---- optional input validation ------------------------------------------------------------
 __global__ void k_validate(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
                            int64_t rows, int64_t cols, int64_t nnz, uint32_t* err) {
