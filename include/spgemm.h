@@ -60,6 +60,10 @@ extern "C" {
                                          __match_any_sync warp aggregation */
 #define SPGEMM_FLAG_DENSE_L2 128      /* heavy dense chunks sum with L2 reductions into a global
                                          per-SM array instead of shared-memory atomics */
+#define SPGEMM_FLAG_TMA_SPLIT 512     /* multisplit: tiles of C^ staged in shared memory by
+                                         bulk copies (one 1024-thread block per SM, double
+                                         buffered) instead of the register-tiled kernel (two
+                                         512-thread blocks per SM); slower on the R-MAT cases */
 #define SPGEMM_FLAG_DIRECT_SPLIT 256  /* one-level plans: the outer product writes straight into
                                          C^_reord (counts from per-B-row chunk histograms), so C^
                                          is never stored and level 0 needs no multisplit pass */

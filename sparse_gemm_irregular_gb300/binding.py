@@ -26,6 +26,7 @@ FLAG_TIMING = 32
 FLAG_NO_MATCH = 64
 FLAG_DENSE_L2 = 128
 FLAG_DIRECT_SPLIT = 256
+FLAG_TMA_SPLIT = 512
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",
           "light_numeric", "chunk_numeric", "chunk_dense"]

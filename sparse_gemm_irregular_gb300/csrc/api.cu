@@ -397,9 +397,15 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
     const int64_t out_half = 1 - in_half;
     {
       PhaseTimer t(h, 5);
-      launch_multisplit(in_ptr, part, total_in, in_col, in_val, shift, v, P.group_rows, xmap, cursor,
-                        h->d_chat_col + out_half * cap, vals ? h->d_chat_val + out_half * cap : nullptr, vals, match,
-                        h->sms, h->d_err, h->st);
+      const bool tma = (h->opt.flags & SPGEMM_FLAG_TMA_SPLIT) &&
+                       launch_multisplit_tma(in_ptr, part, total_in, in_col, in_val, shift, v, P.group_rows, xmap,
+                                             cursor, h->d_chat_col + out_half * cap,
+                                             vals ? h->d_chat_val + out_half * cap : nullptr, vals, h->sms, h->d_err,
+                                             h->st);
+      if (!tma)
+        launch_multisplit(in_ptr, part, total_in, in_col, in_val, shift, v, P.group_rows, xmap, cursor,
+                          h->d_chat_col + out_half * cap, vals ? h->d_chat_val + out_half * cap : nullptr, vals, match,
+                          h->sms, h->d_err, h->st);
     }
     ws_free(h, part);
     ws_free(h, cursor);

@@ -17,6 +17,7 @@ enum DevErr : uint32_t {
   kErrBounds = 2u,         // an index left its range (inconsistent input or a planner bug)
   kErrRowOverflow = 4u,    // a row wrote more entries than the symbolic phase counted
   kErrCsr = 8u,            // input validation failed
+  kErrTimeout = 16u,       // a bounded wait on an asynchronous copy gave up
 };
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }

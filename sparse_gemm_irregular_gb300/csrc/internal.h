@@ -147,6 +147,11 @@ void launch_multisplit(const int64_t* row_ptr, const int2* part, int64_t total, 
                        const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
                        unsigned long long* reord_cursor, int32_t* out_col, double* out_val, bool with_vals, bool match,
                        int sms, uint32_t* err, cudaStream_t s);
+// TMA-staged multisplit (k_msplit_tma.cu); returns false when it cannot run (alignment, bins).
+bool launch_multisplit_tma(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
+                           const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
+                           unsigned long long* cursor, int32_t* out_col, double* out_val, bool with_vals, int sms,
+                           uint32_t* err, cudaStream_t s);
 void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t elem_base,
                        const int32_t* row, const int32_t* base, int64_t* f_start, int64_t* f_cnt,
                        int32_t* f_row, int32_t* f_base, cudaStream_t s);

@@ -47,6 +47,9 @@ FORCED = [
     dict(flags=256, tau=16, chunk_width=64, chunks_max=16),
     dict(flags=256 | 1, tau=64, chunk_width=64, chunks_max=8),
     dict(flags=256 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
+    # bulk-copy staged multisplit: two levels, and four levels with recompute batches
+    dict(flags=512, tau=16, chunk_width=32, chunks_max=4),
+    dict(flags=512 | 16, tau=8, chunk_width=32, chunks_max=2, heavy_batch_elems=700),
 ]
 
 
@@ -74,11 +77,11 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 256])
+@pytest.mark.parametrize("flags", [0, 256, 512])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
-    row, thousands of light rows in every ladder bin -- compared in full (multisplit path and
-    direct split)."""
+    row, thousands of light rows in every ladder bin -- compared in full (multisplit path,
+    direct split, bulk-copy staged multisplit)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
     assert st.rows_heavy > 0 and st.rows_light > 0
