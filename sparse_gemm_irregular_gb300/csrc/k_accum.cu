@@ -17,6 +17,7 @@ namespace sg {
 
 constexpr int kWarpGroupsPerBlock = 8;
 constexpr int kMaxBatch = 256;  // A entries staged per expansion step
+constexpr int kExpandUnroll = 4;  // products per thread whose loads are issued together
 
 struct AccParams {
   // row source
@@ -185,22 +186,41 @@ __device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& 
     if (g.lane < nent) s.incl[g.lane] = incl;
     g.sync();
     int j = 0;
-    for (int64_t f = g.lane; f < total; f += g.size) {
-      // staged entry j holds flattened positions [incl[j-1], incl[j])
-      if (s.incl[j] <= f) {
-        int lo = j, hi = nent - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (s.incl[mid] <= f) lo = mid + 1; else hi = mid;
+    // kExpandUnroll products per thread per step: their B loads are all issued before the
+    // first accumulator update, so each thread keeps several L2 requests in flight
+    for (int64_t f0 = g.lane; f0 < total; f0 += kExpandUnroll * g.size) {
+      int32_t col[kExpandUnroll];
+      double bv[kExpandUnroll], av[kExpandUnroll];
+#pragma unroll
+      for (int u = 0; u < kExpandUnroll; ++u) {
+        const int64_t f = f0 + static_cast<int64_t>(u) * g.size;
+        col[u] = kEmptyKey;
+        if (f < total) {
+          // staged entry j holds flattened positions [incl[j-1], incl[j])
+          if (s.incl[j] <= f) {
+            int lo = j, hi = nent - 1;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (s.incl[mid] <= f) lo = mid + 1; else hi = mid;
+            }
+            j = lo;
+          }
+          const int64_t before = j > 0 ? s.incl[j - 1] : 0;
+          const int64_t q = s.bstart[j] + (f - before);
+          col[u] = p.bcol[q];
+          if (NUMERIC) {
+            bv[u] = p.bval[q];
+            av[u] = s.av[j];
+          }
         }
-        j = lo;
       }
-      const int64_t before = j > 0 ? s.incl[j - 1] : 0;
-      const int64_t q = s.bstart[j] + (f - before);
-      const int32_t col = p.bcol[q];
-      const double v = NUMERIC ? s.av[j] * p.bval[q] : 0.0;
-      if (DENSE) fresh += dense_insert<NUMERIC>(s, slots, col - base, v, p.err);
-      else fresh += hash_insert<NUMERIC>(s, slots, col, v, p.err);
+#pragma unroll
+      for (int u = 0; u < kExpandUnroll; ++u) {
+        if (col[u] == kEmptyKey) continue;
+        const double v = NUMERIC ? av[u] * bv[u] : 0.0;
+        if (DENSE) fresh += dense_insert<NUMERIC>(s, slots, col[u] - base, v, p.err);
+        else fresh += hash_insert<NUMERIC>(s, slots, col[u], v, p.err);
+      }
     }
     g.sync();
   }
@@ -224,6 +244,80 @@ __device__ __forceinline__ int64_t expand_chunk(const Group<WARP>& g, const Smem
 }
 
 // ---- outputs -----------------------------------------------------------------------------
+// Block-wide exclusive prefix of the set-bit counts of `words` bitmap words, written to pre[];
+// returns the total.  Each warp owns a contiguous run of words (read lane-strided, so without
+// bank conflicts) and scans it with shuffles; one barrier exchanges the warp totals.
+// `tmp` holds 32 unsigned.  Ends with a barrier.
+__device__ unsigned block_word_prefix(const Group<false>& g, const uint32_t* bits, int64_t words,
+                                      int32_t* pre, unsigned* tmp) {
+  const int nwarps = g.size >> 5, warp = g.lane >> 5, l = g.lane & 31;
+  const int64_t per = ceil_div(ceil_div(words, nwarps), 32) * 32;
+  const int64_t wb = warp * per, we = min(words, wb + per);
+  unsigned c = 0;
+  for (int64_t w = wb + l; w < we; w += 32) c += __popc(bits[w]);
+  c = warp_sum(c);
+  if (l == 0) tmp[warp] = c;
+  __syncthreads();
+  const unsigned mine = l < warp ? tmp[l] : 0u;
+  const unsigned all = l < nwarps ? tmp[l] : 0u;
+  unsigned run = warp_sum(mine);
+  const unsigned total = warp_sum(all);
+  for (int64_t w0 = wb; w0 < we; w0 += 32) {
+    const int64_t w = w0 + l;
+    const unsigned x = w < we ? __popc(bits[w]) : 0u;
+    const unsigned incl = warp_incl_scan(x);
+    if (w < we) pre[w] = static_cast<int32_t>(run + incl - x);
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncthreads();
+  return total;
+}
+
+// Compact the occupied slots of a block's hash table to [0, n) in place; returns n.  The order
+// is free (the ranked write orders by column).  Slabs of four slots per thread: a warp reads its
+// 128 slots as four lane-strided rows, so every read of a slab precedes the barrier that
+// releases its writes, and writes never reach past the slab.  The warp totals alternate between
+// two halves of `tmp` (64 unsigned), so a fast warp cannot overwrite totals still being read.
+__device__ int64_t block_compact(const Group<false>& g, const Smem& s, int64_t slots) {
+  const int nwarps = g.size >> 5, warp = g.lane >> 5, l = g.lane & 31;
+  unsigned* tmp = reinterpret_cast<unsigned*>(s.tmp);
+  const int64_t slab = 128 * static_cast<int64_t>(nwarps);
+  int64_t written = 0;
+  int parity = 0;
+  for (int64_t s0 = 0; s0 < slots; s0 += slab, parity ^= 1) {
+    const int64_t b = s0 + 128 * warp + l;
+    int32_t k[4];
+    double v[4];
+    unsigned occ[4], c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t i = b + 32 * j;
+      k[j] = i < slots ? s.keys[i] : kEmptyKey;
+      v[j] = i < slots ? s.vals[i] : 0.0;
+      occ[j] = __ballot_sync(0xffffffffu, k[j] != kEmptyKey);
+      c += __popc(occ[j]);
+    }
+    unsigned* t = tmp + 32 * parity;
+    if (l == 0) t[warp] = c;
+    __syncthreads();
+    const unsigned mine = l < warp ? t[l] : 0u;
+    const unsigned all = l < nwarps ? t[l] : 0u;
+    int64_t pos = written + warp_sum(mine);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (k[j] != kEmptyKey) {
+        const int64_t d = pos + __popc(occ[j] & lanemask_lt());
+        s.keys[d] = k[j];
+        s.vals[d] = v[j];
+      }
+      pos += __popc(occ[j]);
+    }
+    written += warp_sum(all);
+  }
+  __syncthreads();
+  return written;
+}
+
 // Ordered write of the `n` compacted entries [0, n) of a block's hash table without sorting:
 // the unused part of the table becomes a column bitmap (keys region: bit words, values
 // region: their exclusive prefix) covering a window of 32 * (slots - n) columns; the window
@@ -282,16 +376,7 @@ __device__ void block_rank_emit(const Group<false>& g, const Smem& s, int64_t sl
       if (c >= 0 && c < 32 * nwin) atomicOr(&bits[c >> 5], 1u << (c & 31));
     }
     __syncthreads();
-    int64_t run = 0;
-    for (int64_t w0 = 0; w0 < nwin; w0 += g.size) {
-      const int64_t w = w0 + g.lane;
-      const int64_t cnt = w < nwin ? __popc(bits[w]) : 0;
-      int64_t tot;
-      const int64_t incl = block_incl_scan(cnt, s.tmp, &tot);
-      if (w < nwin) pre[w] = static_cast<int32_t>(run + incl - cnt);
-      run += tot;
-    }
-    __syncthreads();
+    const int64_t run = block_word_prefix(g, bits, nwin, pre, reinterpret_cast<unsigned*>(s.tmp));
     for (int64_t i = g.lane; i < n; i += g.size) {
       const int32_t k = s.keys[i];
       const int64_t c = static_cast<int64_t>(k) - ws;
@@ -314,6 +399,11 @@ template <bool WARP>
 __device__ void hash_emit(const Group<WARP>& g, const Smem& s, int64_t slots, int64_t n,
                           int64_t expected, int32_t col_base, int32_t* c_col, double* c_val,
                           uint32_t* err) {
+  if constexpr (!WARP) {
+    const int64_t m = block_compact(g, s, slots);
+    block_rank_emit(g, s, slots, m, expected, col_base, c_col, c_val, err);
+    return;
+  }
   int64_t written = 0;
   for (int64_t r0 = 0; r0 < slots; r0 += g.size) {
     const int64_t slot = r0 + g.lane;
@@ -334,10 +424,6 @@ __device__ void hash_emit(const Group<WARP>& g, const Smem& s, int64_t slots, in
     }
     written += total;
     g.sync();
-  }
-  if constexpr (!WARP) {
-    block_rank_emit(g, s, slots, n, expected, col_base, c_col, c_val, err);
-    return;
   }
   int64_t P = 1;
   while (P < n) P <<= 1;
