@@ -594,8 +594,7 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     for (int j = 0; j < 4; ++j) {        // last-level chunks: bitmaps of width W
       const int b = h->lad.n + j;
       launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
-                          h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk, h->d_err, h->d_counter, nullptr, nullptr,
-                          h->st);
+                          h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk, h->d_err, h->d_counter, nullptr, h->st);
     }
   }
   {
@@ -644,14 +643,13 @@ int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
                   h->lad.tpr[L], false, 0, true, sk, h->d_err, h->st);
   if ((h->opt.flags & SPGEMM_FLAG_DENSE_L2) && !h->d_gacc)
     SG_ALLOC(h->d_gacc, double, static_cast<int64_t>(h->sms) * h->plan.chunk_width);
-  if (!h->d_hub) SG_ALLOC(h->d_hub, double, static_cast<int64_t>(h->sms) * kChunkHubSlots);
   for (int j = 0; j < 4; ++j) {
     const int b = h->lad.n + j;
     PhaseTimer td(h, 12);  // only the dense bin is counted here (its region nests in slot 11)
     if (j < 3) td.cancel();
     launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
                         h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err,
-                        h->d_counter, h->d_gacc, h->d_hub, h->st);
+                        h->d_counter, h->d_gacc, h->st);
   }
   return SPGEMM_OK;
 }

@@ -160,7 +160,7 @@ void launch_chunk_classify(const int64_t* f_cnt, int64_t n, int64_t bitmap_from,
 // bitmap-ordered chunk accumulators (k_chunk.cu); mode 0 symbolic, 1 hash numeric, 2 dense numeric
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
                          int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
-                         double* hub_all, cudaStream_t s);
+                         cudaStream_t s);
 constexpr int kChunkHubSlots = 137;           // hub columns of a dense chunk (k_chunk.cu)
 void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s);
 void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s);
@@ -229,7 +229,6 @@ struct spgemm_ctx {
   uint32_t* d_err = nullptr;
   int* d_counter = nullptr;     // work counter of the persistent dense accumulator
   double* d_gacc = nullptr;     // L2-resident dense accumulators (SPGEMM_FLAG_DENSE_L2)
-  double* d_hub = nullptr;      // L2-resident hub-column sums of the dense accumulator
   int64_t* d_scan = nullptr;    // scan scratch
   int64_t scan_cap = 0;
   int64_t* d_ip = nullptr;

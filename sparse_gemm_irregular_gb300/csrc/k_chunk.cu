@@ -70,24 +70,6 @@ __device__ __forceinline__ int nth_set_bit(uint32_t m, int k) {
   return pos;
 }
 
-// Sum `v` over the lanes of the warp that hold the same key (key >= 0); returns true on the one
-// lane per key that must apply the group's sum (left in *sum).  All 32 lanes must call it.
-__device__ __forceinline__ bool warp_group_sum(int key, double v, double* sum) {
-  const uint32_t peers = __match_any_sync(0xffffffffu, key);
-  const int rank = __popc(peers & lanemask_lt());
-  const int gsize = __popc(peers);
-  double acc = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const bool take = ((rank & (2 * d - 1)) == 0) && (rank + d < gsize);
-    const int src = (rank + d < gsize) ? nth_set_bit(peers, rank + d) : static_cast<int>(lane_id());
-    const double o = __shfl_sync(0xffffffffu, acc, src);
-    if (take) acc += o;
-  }
-  *sum = acc;
-  return key >= 0 && rank == 0;
-}
-
 struct CkParams {
   ChunkSet cs;
   const int32_t* list;   // chunk ids of this bin
@@ -96,7 +78,6 @@ struct CkParams {
   int64_t slots;         // hash slots (hash numeric)
   Sink sink;
   uint32_t* err;
-  double* hub_all;       // dense mode: kHubSlots doubles per block, L2 resident
 };
 
 template <bool WARP>
@@ -185,7 +166,7 @@ __device__ __forceinline__ int32_t ck_rank(const CkSmem& s, int32_t col) {
   return s.pre[col >> 5] + __popc(w & ((1u << (col & 31)) - 1u));
 }
 
-// mode 0: symbolic, 1: hash numeric, 2: dense numeric
+// mode 0: symbolic, 1: hash numeric (the dense numeric accumulator is k_chunk_dense below)
 template <bool WARP, int MODE>
 __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   extern __shared__ __align__(16) char smem_raw[];
@@ -310,82 +291,6 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
         c_val[r] = s.vals[j];
       }
     }
-    return;
-  }
-
-  if (MODE == 2) {
-    // dense: the whole value array (and the warps' hub sums) is zeroed up front with vector
-    // stores, then every element ORs its bit and adds its value, with no barrier inside the
-    // stream; hub columns add into the warp's private slots
-    {
-      double2* v2 = reinterpret_cast<double2*>(s.vals);
-      const int64_t n2 = p.width / 2;
-      for (int64_t j = g.lane; j < n2; j += g.size) v2[j] = make_double2(0.0, 0.0);
-      if ((p.width & 1) && g.lane == 0) s.vals[p.width - 1] = 0.0;
-      }
-    g.sync();
-    double* my_hub = s.hub + (threadIdx.x >> 5) % kHubWarps * kHubSlots;
-    constexpr int U = 8;
-    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
-      int32_t cr[U];
-      double vr[U];
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
-        cr[j] = -1;
-        vr[j] = 0.0;
-        if (f < cnt) {
-          cr[j] = __ldcs(col + f);
-          vr[j] = __ldcs(val + f);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int32_t c = cr[j];
-        if (c < 0) continue;
-        if (static_cast<uint32_t>(c) < width) {
-          atomicOr(&s.bits[c >> 5], 1u << (c & 31));
-          const int hi = hub_index(static_cast<uint32_t>(c));
-          atomicAdd(hi >= 0 ? &my_hub[hi] : &s.vals[c], vr[j]);
-        } else {
-          set_error(p.err, kErrBounds);
-        }
-      }
-    }
-    g.sync();
-    // merge the warps' hub sums into the dense array
-    for (int j = g.lane; j < kHubSlots; j += g.size) {
-      const uint32_t c = hub_column(j);
-      if (c < width) {
-        double sum = 0.0;
-        for (int w = 0; w < kHubWarps; ++w) sum += s.hub[w * kHubSlots + j];
-        s.vals[c] += sum;
-      }
-    }
-    g.sync();
-    // ordered output: scan of the bitmap words, then every word writes its set bits
-    int64_t written = 0;
-    for (int64_t w0 = 0; w0 < words; w0 += g.size) {
-      const int64_t w = w0 + g.lane;
-      const uint32_t bits = w < words ? s.bits[w] : 0u;
-      const int64_t c = __popc(bits);
-      int64_t tot;
-      const int64_t incl = ck_scan<WARP>(g, c, s.tmp, &tot);
-      int64_t pos = written + incl - c;
-      uint32_t b = bits;
-      while (b) {
-        const int bit = __ffs(b) - 1;
-        b &= b - 1;
-        const int32_t idx = static_cast<int32_t>(w * 32 + bit);
-        if (pos < expected) {
-          c_col[pos] = idx + base;
-          c_val[pos] = s.vals[idx];
-        }
-        ++pos;
-      }
-      written += tot;
-    }
-    if (written != expected && g.lane == 0) set_error(p.err, kErrRowOverflow);
   }
 }
 
@@ -532,32 +437,31 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
       }
       if (L2) __threadfence_block();
       __syncthreads();
+      // ordered write, balanced over the block: thread t writes output positions t, t + 1024, ...
+      // (consecutive threads, consecutive positions), finding its column by a binary search of
+      // the word prefix and a select inside the word.  The bits of power-law inputs crowd into
+      // the low columns, so one thread per word would serialise the densest words.
+      const int64_t total = ck_bitmap_prefix(g, s, words);
+      __syncthreads();
+      if (total != job.expected && g.lane == 0) set_error(p.err, kErrRowOverflow);
+      const int64_t n_out = total < job.expected ? total : job.expected;
       int32_t* c_col = p.sink.c_col + job.out;
       double* c_val = p.sink.c_val + job.out;
-      int64_t written = 0;
-      for (int64_t w0 = 0; w0 < words; w0 += g.size) {
-        const int64_t w = w0 + g.lane;
-        const uint32_t bits = w < words ? s.bits[w] : 0u;
-        const int64_t c = __popc(bits);
-        int64_t tot;
-        const int64_t incl = ck_scan<false>(g, c, s.tmp, &tot);
-        int64_t pos = written + incl - c;
-        uint32_t b = bits;
-        while (b) {
-          const int bit = __ffs(b) - 1;
-          b &= b - 1;
-          const int32_t idx = static_cast<int32_t>(w * 32 + bit);
-          if (pos < job.expected) {
-            c_col[pos] = idx + job.base;
-            c_val[pos] = L2 ? __ldcg(&acc[idx]) : acc[idx];
-          }
-          if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed
-          ++pos;
+      for (int64_t k = g.lane; k < total; k += g.size) {
+        int lo = 0, hi = static_cast<int>(words) - 1;
+        while (lo < hi) {  // last word whose prefix is <= k: it holds bit number k
+          const int mid = (lo + hi + 1) >> 1;
+          if (s.pre[mid] <= k) lo = mid; else hi = mid - 1;
         }
-        if (w < words) s.bits[w] = 0u;
-        written += tot;
+        const int32_t idx = lo * 32 + nth_set_bit(s.bits[lo], static_cast<int>(k - s.pre[lo]));
+        if (k < n_out) {
+          c_col[k] = idx + job.base;
+          c_val[k] = L2 ? __ldcg(&acc[idx]) : acc[idx];
+        }
+        if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed
       }
-      if (written != job.expected && g.lane == 0) set_error(p.err, kErrRowOverflow);
+      __syncthreads();
+      for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
     }
     __syncthreads();
   }
@@ -581,7 +485,7 @@ static void ck_launch(const CkParams& p, int tpr, cudaStream_t s) {
 
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
                          int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
-                         double* hub_all, cudaStream_t s) {
+                         cudaStream_t s) {
   if (count == 0) return;
   CkParams p{};
   p.cs = cs;
@@ -591,7 +495,6 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
   p.slots = slots;
   p.sink = sink;
   p.err = err;
-  p.hub_all = hub_all;
   const bool warp = tpr == 32;
   if (mode == 0) {
     if (warp) ck_launch<true, 0>(p, tpr, s); else ck_launch<false, 0>(p, tpr, s);
