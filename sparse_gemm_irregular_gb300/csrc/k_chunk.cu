@@ -20,10 +20,11 @@ constexpr int kCkWarpsPerBlock = 8;
 // 2^16.  In R-MAT / Kronecker power-law products the probability of a column falls with every
 // set bit of its index, so these few columns take a large share of the products of every
 // chunk (local column 0 alone ~2% on R-MAT with a = 0.57).  Shared-memory fp64 atomics
-// serialise badly on one address, so hub products are first summed across the lanes of a warp
-// (__match_any_sync + shuffle reduction) and then added to warp-private slots; the private
-// slots are merged once per chunk.  On other inputs the hubs are just ordinary columns.
-constexpr int kHubWarps = 32;
+// serialise badly on one address, so hub products add into one of kHubCopies private copies of
+// the hub slots (every group of four streaming warps shares a copy); the copies are merged once
+// per chunk.  Eight copies measured best: fewer copies contend, more copies lengthen the merge,
+// a serial chain of fp64 adds per slot.  On other inputs the hubs are just ordinary columns.
+constexpr int kHubCopies = 8;
 constexpr int kHubBits = 16;
 constexpr int kHubSlots = 1 + kHubBits + kHubBits * (kHubBits - 1) / 2;  // 137
 static_assert(kHubSlots == kChunkHubSlots, "hub slot count");
@@ -106,8 +107,8 @@ __host__ __device__ inline size_t ck_group_bytes(int64_t width, int64_t slots, i
   const int64_t words = (width + 31) / 32;
   size_t b = ck_align(33 * sizeof(int64_t)) + ck_align(words * 4) + ck_align(words * 4);
   if (mode == 1) b += ck_align(slots * 4) + ck_align(slots * 8);  // hash numeric
-  if (mode == 2) b += ck_align(width * 8) + ck_align(kHubWarps * kHubSlots * 8);  // dense + warp hubs
-  if (mode == 3) b += ck_align(kHubWarps * kHubSlots * 8);                        // L2 dense: hubs only
+  if (mode == 2) b += ck_align(width * 8) + ck_align(kHubCopies * kHubSlots * 8);  // dense + hub copies
+  if (mode == 3) b += ck_align(kHubCopies * kHubSlots * 8);                        // L2 dense: hubs only
   return b;
 }
 
@@ -117,7 +118,7 @@ struct CkSmem {
   int32_t* pre;
   int32_t* keys;
   double* vals;
-  double* hub;   // dense mode: per-warp private sums of the hub columns
+  double* hub;   // dense mode: private copies of the hub-column sums
 };
 
 __device__ __forceinline__ CkSmem ck_carve(char* p, int64_t width, int64_t slots, int mode) {
@@ -299,9 +300,9 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
 // chunk from the work counter, the chain of descriptor loads) would sit on the critical path, so
 // warp 0 is a helper: while warps 1..31 stream the current chunk it takes the next chunk and
 // loads its descriptor into a second shared slot.  The value array is zeroed once and every
-// chunk clears the slots it writes.  Hub columns (hub_index) add into per-warp private sums in
-// shared memory, merged once per chunk, so the hottest columns of power-law inputs do not
-// serialise on one address.  The L2 variant keeps the value array in an L2-resident global
+// chunk clears the slots it writes.  Hub columns (hub_index) add into private copies of their
+// sums in shared memory, merged once per chunk, so the hottest columns of power-law inputs do
+// not serialise on one address.  The L2 variant keeps the value array in an L2-resident global
 // slice instead (fire-and-forget reductions), for A/B measurements.
 struct DenseJob {
   int64_t start, cnt, out, expected;
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
   const int nt = nwork * 32;
   const int t = static_cast<int>(threadIdx.x) - 32;
   double* acc = L2 ? gacc_all + static_cast<int64_t>(blockIdx.x) * p.width : s.vals;
-  double* my_hub = s.hub + (warp > 0 ? warp - 1 : 0) * kHubSlots;
+  double* my_hub = s.hub + ((warp > 0 ? warp - 1 : 0) % kHubCopies) * kHubSlots;
   if (L2) {
     for (int64_t j = g.lane; j < p.width; j += g.size) __stcg(&acc[j], 0.0);
   } else {
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
     for (int64_t j = g.lane; j < p.width / 2; j += g.size) v2[j] = make_double2(0.0, 0.0);
     if ((p.width & 1) && g.lane == 0) acc[p.width - 1] = 0.0;
   }
-  for (int j = g.lane; j < kHubWarps * kHubSlots; j += g.size) s.hub[j] = 0.0;
+  for (int j = g.lane; j < kHubCopies * kHubSlots; j += g.size) s.hub[j] = 0.0;
   for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
   if (threadIdx.x == 0) {
     dense_fetch(p, next, &jobs[0]);
@@ -423,11 +424,11 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
     if (L2) __threadfence_block();
     __syncthreads();
     if (job.state == 1) {
-      // fold the warps' hub sums into the value array
+      // fold the hub copies into the value array
       for (int j = g.lane; j < kHubSlots; j += g.size) {
         const uint32_t c = hub_column(j);
         double sum = 0.0;
-        for (int w = 0; w < nwork; ++w) {
+        for (int w = 0; w < kHubCopies; ++w) {
           sum += s.hub[w * kHubSlots + j];
           s.hub[w * kHubSlots + j] = 0.0;
         }
