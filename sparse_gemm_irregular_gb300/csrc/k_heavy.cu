@@ -7,9 +7,10 @@
 //   Histogram       -> histogram: per (C^ row, chunk) counts, warp-aggregated with
 //                      __match_any_sync into a block histogram, one global atomic per bin.
 //   ThreshPartition -> chunk_partition + the stable bin scatter: heavy chunks first.
-//   Multisplit      -> multisplit: block histogram, global reservation per bin, block scan,
-//                      permute in shared memory, coalesced write with the column shifted into
-//                      the chunk's local range.
+//   Multisplit      -> multisplit: block histogram whose warp-aggregated atomics also rank every
+//                      element inside its bin, one global reservation per bin, then every
+//                      element is written at (its bin's reserved run + its rank) with the
+//                      column shifted into the chunk's local range.
 // plus the bookkeeping that turns the final chunks into offsets inside the rows of C.
 #include <algorithm>
 
@@ -510,6 +511,20 @@ __device__ __forceinline__ void ms_count(unsigned* hist, int b) {
 }
 
 template <bool MATCH>
+__device__ __forceinline__ unsigned ms_rank(unsigned* hist, int b) {
+  // count and rank in one step: the group's atomic returns the bin's count so far
+  if (MATCH) {
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    const int leader = __ffs(peers) - 1;
+    unsigned base = 0;
+    if (b >= 0 && static_cast<int>(lane_id()) == leader) base = atomicAdd(&hist[b], __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return base + __popc(peers & lanemask_lt());
+  }
+  return b >= 0 ? atomicAdd(&hist[b], 1u) : 0u;
+}
+
+template <bool MATCH>
 __global__ void __launch_bounds__(kMsThreads) k_histogram(const int64_t* __restrict__ rp, const int2* __restrict__ part,
                                                          int64_t total, int64_t ntiles, const int32_t* __restrict__ col,
                                                          int shift, int64_t v, int64_t gr,
@@ -595,13 +610,9 @@ __global__ void __launch_bounds__(kMsThreads, 2) k_multisplit(
     const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
     double* __restrict__ out_val, uint32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
-  __shared__ unsigned scan_tmp[33];
-  double* val_buf = reinterpret_cast<double*>(smem_raw);                                  // kMsTile
-  unsigned long long* goff = reinterpret_cast<unsigned long long*>(val_buf + kMsTile);    // gr*v
-  int64_t* rstart = reinterpret_cast<int64_t*>(goff + gr * v);                            // gr + 1
-  int32_t* col_buf = reinterpret_cast<int32_t*>(rstart + gr + 1);                        // kMsTile
-  unsigned* hist = reinterpret_cast<unsigned*>(col_buf + kMsTile);                        // gr*v: count, then cursor
-  unsigned* loff = hist + gr * v;                                                         // gr*v + 1
+  unsigned long long* goff = reinterpret_cast<unsigned long long*>(smem_raw);  // gr*v: global run starts
+  int64_t* rstart = reinterpret_cast<int64_t*>(goff + gr * v);                 // gr + 1
+  unsigned* hist = reinterpret_cast<unsigned*>(rstart + gr + 1);               // gr*v
   const int64_t wmask = (int64_t(1) << shift) - 1;
   int64_t t = blockIdx.x;
   if (t >= ntiles) return;
@@ -622,77 +633,41 @@ __global__ void __launch_bounds__(kMsThreads, 2) k_multisplit(
       for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       int bin[kMsItems];
+      unsigned rank[kMsItems];
       ms_bins(rstart, nr, p0, g1, c, shift, v, bin, err);
 #pragma unroll
-      for (int j = 0; j < kMsItems; ++j) ms_count<MATCH>(hist, bin[j]);
+      for (int j = 0; j < kMsItems; ++j) rank[j] = ms_rank<MATCH>(hist, bin[j]);
       __syncthreads();
-      // local offsets (exclusive scan of the histogram) and one global reservation per bin
+      // one global reservation per bin: its run of the bin's chunk in C^_reord
       {
         const int per = (nbins + kMsThreads - 1) / kMsThreads;
         const int b0 = threadIdx.x * per;
-        unsigned local = 0;
-        for (int b = b0; b < min(nbins, b0 + per); ++b) local += hist[b];
-        unsigned tot;
-        const unsigned incl = block_incl_scan(local, scan_tmp, &tot);
-        unsigned run = incl - local;
         for (int b = b0; b < min(nbins, b0 + per); ++b) {
           const unsigned h = hist[b];
-          loff[b] = run;
           if (h) {
             const int64_t gchunk = (w0 + b / v) * v + (b % v);
             const int64_t q = xmap ? xmap[gchunk] : gchunk;
             goff[b] = atomicAdd(&cursor[q], static_cast<unsigned long long>(h));
           }
-          hist[b] = run;  // becomes the permute cursor
-          run += h;
         }
-        if (threadIdx.x == 0) loff[nbins] = tot;
       }
       __syncthreads();
-      // permute into shared memory, grouped by (row, chunk); order inside a chunk is free
+      // scatter: every element goes straight to its bin's reserved run (run start + rank).  A
+      // bin's run is written by this block alone within this tile, so the partial sectors of
+      // neighbouring lanes merge in L2 and DRAM sees whole lines (no permute in shared memory)
 #pragma unroll
       for (int j = 0; j < kMsItems; ++j) {
         const int b = bin[j];
-        unsigned pos = 0;
-        if (MATCH) {
-          const uint32_t peers = __match_any_sync(0xffffffffu, b);
-          const int leader = __ffs(peers) - 1;
-          unsigned base = 0;
-          if (b >= 0 && static_cast<int>(lane_id()) == leader) base = atomicAdd(&hist[b], __popc(peers));
-          base = __shfl_sync(0xffffffffu, base, leader);
-          pos = base + __popc(peers & lanemask_lt());
-        } else if (b >= 0) {
-          pos = atomicAdd(&hist[b], 1u);
-        }
         if (b >= 0) {
-          col_buf[pos] = c[j];
-          if (VALS) val_buf[pos] = vv[j];
+          const int64_t dst = static_cast<int64_t>(goff[b]) + rank[j];
+          __stcs(&out_col[dst], static_cast<int32_t>(c[j] & wmask));
+          if (VALS) __stcs(&out_val[dst], vv[j]);
         }
       }
-      __syncthreads();
-      // the registers are free again: start loading the next tile, then write this one out
+      // no barrier here: the next window's first barrier orders the reuse of hist and goff
       if (w0 + gr > pr.y && tn < ntiles)
         ms_load_tile<VALS>(in_col, in_val, tn * kMsTile + static_cast<int64_t>(threadIdx.x) * kMsItems,
                            min(total, (tn + 1) * kMsTile), c, vv);
-      // coalesced write: runs of one local chunk go to consecutive global positions
-      const int cnt = static_cast<int>(loff[nbins]);
-      for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-        const int32_t cc = col_buf[i];
-        int r = 0;
-        {
-          int lo = 0, hi = nr - 1;  // last row whose first bin starts at or before i
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (static_cast<int>(loff[mid * v]) <= i) lo = mid; else hi = mid - 1;
-          }
-          r = lo;
-        }
-        const int b = static_cast<int>(r * v + (static_cast<int64_t>(cc) >> shift));
-        const int64_t dst = static_cast<int64_t>(goff[b]) + (i - static_cast<int>(loff[b]));
-        __stcs(&out_col[dst], static_cast<int32_t>(cc & wmask));
-        if (VALS) __stcs(&out_val[dst], val_buf[i]);
-      }
-      __syncthreads();
     }
     if (tn < ntiles) pr = part[tn];
   }
@@ -704,7 +679,7 @@ static void ms_launch(const int64_t* row_ptr, const int2* part, int64_t total, c
                       unsigned long long* cursor, int32_t* out_col, double* out_val, int sms, uint32_t* err,
                       cudaStream_t s) {
   const int64_t bins = group_rows * nchunks;
-  const size_t smem = kMsTile * 8 + bins * 8 + (group_rows + 1) * 8 + kMsTile * 4 + bins * 4 + (bins + 1) * 4;
+  const size_t smem = bins * 8 + (group_rows + 1) * 8 + bins * 4;
   const int64_t ntiles = ceil_div(total, kMsTile);
   auto kern = k_multisplit<VALS, MATCH>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
