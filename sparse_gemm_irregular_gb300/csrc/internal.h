@@ -13,8 +13,8 @@
 namespace sg {
 
 // ---- tile sizes shared by the planner and the kernels ---------------------------------
-constexpr int64_t kMsTile = 4096;          // elements per histogram / multisplit block
-constexpr int kMsThreads = 512;            // threads per multisplit block (8 elements each)
+constexpr int64_t kMsTile = 1024;          // elements per histogram / multisplit tile
+constexpr int kMsThreads = 128;            // threads per multisplit block (8 elements each)
 constexpr int64_t kMsSmemBudget = 65536;   // bytes of shared memory per multisplit block (Eq. 6)
 constexpr int64_t kMsMaxBins = 2048;       // group_rows * chunks bins held by one block
 constexpr int64_t kOpTile = 2048;          // elements per outer-product block

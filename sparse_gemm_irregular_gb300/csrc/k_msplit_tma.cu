@@ -1,23 +1,23 @@
 // Multisplit (gMAGNUS page, section III-C, Algorithm 5) with the tiles of C^ staged in shared
-// memory by the bulk-copy (TMA) engine.  Persistent blocks, one per SM; tile t is processed while
-// tile t + gridDim.x streams into the second stage, so global loads never sit on the critical path.
-// Per tile: local histogram over (row, chunk) bins with warp-aggregated updates, exclusive scan,
-// one global reservation per non-empty bin, permute in shared memory, and a coalesced write of
-// every local chunk run with the column shifted into the chunk's range.
+// memory by the bulk-copy (TMA) engine.  Persistent blocks keep two stages: while tile t is
+// counted and scattered from one stage, tile t + grid streams into the other, so no thread holds
+// a tile in registers and no load sits on the critical path.  Counting, ranking and the scatter
+// are those of k_multisplit: the warp-aggregated shared atomics of the count return every
+// element's rank inside its bin, one global reservation per bin, then every element is written
+// at (its bin's run start + its rank) with the column shifted into the chunk's local range.
 //
 // Every wait on an mbarrier is bounded: after kMaxSpins failed polls the block records
 // kErrTimeout, drains its own copies in flight (again bounded) and returns.
 #include <algorithm>
 
 #include "internal.h"
+#include "ms_tile.cuh"
 
 namespace sg {
 
 namespace {
 
-constexpr int kT = static_cast<int>(kMsTile);   // 4096 elements per tile
-constexpr int kThreads = 1024;
-constexpr int kItems = kT / kThreads;            // 4
+constexpr int kT = static_cast<int>(kMsTile);  // elements per tile: the partition of k_multisplit
 constexpr uint32_t kMaxSpins = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -81,30 +81,26 @@ __device__ __forceinline__ void issue_tile(const int32_t* in_col, const double* 
 }  // namespace
 
 template <bool VALS>
-__global__ void __launch_bounds__(kThreads, 1) k_multisplit_tma(
+__global__ void __launch_bounds__(kMsThreads, 8) k_multisplit_tma(
     const int64_t* __restrict__ rp, const int2* __restrict__ part, int64_t total, int64_t ntiles,
     const int32_t* __restrict__ in_col, const double* __restrict__ in_val, int shift, int64_t v, int64_t gr,
     const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
     double* __restrict__ out_val, uint32_t* err) {
   extern __shared__ __align__(128) char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2];
-  __shared__ unsigned scan_tmp[33];
   __shared__ int s_fail;
-  // layout (bulk-copy destinations first, all 16-byte aligned): stage 0/1 vals | stage 0/1 cols |
-  // permuted vals | permuted cols | goff | rstart | hist | loff
+  // layout (bulk-copy destinations first, all 16-byte aligned): stage 0/1 values | stage 0/1
+  // columns | goff | rstart | hist
   const int64_t bins_cap = gr * v;
   char* p = smem_raw;
-  Stage stg[2];
-  stg[0].val = reinterpret_cast<double*>(p); p += kT * 8;
-  stg[1].val = reinterpret_cast<double*>(p); p += kT * 8;
-  stg[0].col = reinterpret_cast<int32_t*>(p); p += kT * 4;
-  stg[1].col = reinterpret_cast<int32_t*>(p); p += kT * 4;
-  double* val_buf = reinterpret_cast<double*>(p); p += kT * 8;
-  int32_t* col_buf = reinterpret_cast<int32_t*>(p); p += kT * 4;
+  double* const val0 = reinterpret_cast<double*>(p);  // stage s: val0 + s * kT
+  p += 2 * kT * 8;
+  int32_t* const col0 = reinterpret_cast<int32_t*>(p);  // stage s: col0 + s * kT
+  p += 2 * kT * 4;
+  auto stage = [&](int st) { return Stage{col0 + st * kT, val0 + st * kT}; };
   unsigned long long* goff = reinterpret_cast<unsigned long long*>(p); p += bins_cap * 8;
   int64_t* rstart = reinterpret_cast<int64_t*>(p); p += (gr + 1) * 8;
-  unsigned* hist = reinterpret_cast<unsigned*>(p); p += bins_cap * 4;
-  unsigned* loff = reinterpret_cast<unsigned*>(p);
+  unsigned* hist = reinterpret_cast<unsigned*>(p);
 
   const int64_t wmask = (int64_t(1) << shift) - 1;
   int64_t t = blockIdx.x;
@@ -117,135 +113,98 @@ __global__ void __launch_bounds__(kThreads, 1) k_multisplit_tma(
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
   if (threadIdx.x == 0) {
-    issue_tile<VALS>(in_col, in_val, total, t, stg[0], &bars[0]);
-    if (t + gridDim.x < ntiles) issue_tile<VALS>(in_col, in_val, total, t + gridDim.x, stg[1], &bars[1]);
+    issue_tile<VALS>(in_col, in_val, total, t, stage(0), &bars[0]);
+    if (t + gridDim.x < ntiles) issue_tile<VALS>(in_col, in_val, total, t + gridDim.x, stage(1), &bars[1]);
   }
-  uint32_t phase[2] = {0u, 0u};
-  int pending[2] = {1, t + gridDim.x < ntiles ? 1 : 0};  // thread 0's view: copies issued, not yet waited
+  // bit s of `phase`: parity to wait for on stage s; bit s of `pending` (thread 0's view): a copy
+  // into stage s was issued and not yet waited for
+  uint32_t phase = 0u;
+  uint32_t pending = 1u | (t + gridDim.x < ntiles ? 2u : 0u);
   int s = 0;
   for (; t < ntiles; t += gridDim.x, s ^= 1) {
     const int64_t g0 = t * kT;
     const int64_t g1 = min(total, g0 + kT);
     const int n = static_cast<int>(g1 - g0);
     const int body = n & ~3;
+    const int2 pr = part[t];
     // wait for the stage (bounded)
-    if (!mbar_wait(&bars[s], phase[s])) {
+    if (!mbar_wait(&bars[s], (phase >> s) & 1u)) {
       if (threadIdx.x == 0) {
         set_error(err, kErrTimeout);
         s_fail = 1;
       }
     } else {
-      pending[s] = 0;
+      pending &= ~(1u << s);
     }
-    phase[s] ^= 1u;
+    phase ^= 1u << s;
+    const Stage cur = stage(s);
     // ragged tail of the last tile: plain loads
     for (int i = body + static_cast<int>(threadIdx.x); i < n; i += blockDim.x) {
-      stg[s].col[i] = in_col[g0 + i];
-      if (VALS) stg[s].val[i] = in_val[g0 + i];
+      cur.col[i] = in_col[g0 + i];
+      if (VALS) cur.val[i] = in_val[g0 + i];
     }
     __syncthreads();
     if (s_fail) break;
-    const int2 pr = part[t];
-    const int32_t* scol = stg[s].col;
-    const double* sval = stg[s].val;
+    const int i0 = static_cast<int>(threadIdx.x) * kMsItems;
+    const int64_t p0 = g0 + i0;
+    int32_t c[kMsItems];
+#pragma unroll
+    for (int j = 0; j < kMsItems; j += 4) {
+      const int4 x = *reinterpret_cast<const int4*>(cur.col + i0 + j);
+      c[j] = x.x; c[j + 1] = x.y; c[j + 2] = x.z; c[j + 3] = x.w;
+    }
     for (int64_t w0 = pr.x; w0 <= pr.y; w0 += gr) {
       const int nr = static_cast<int>(min(gr, static_cast<int64_t>(pr.y) - w0 + 1));
       const int nbins = static_cast<int>(nr * v);
-      for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i] - g0;  // tile-relative
+      for (int i = threadIdx.x; i <= nr; i += blockDim.x) rstart[i] = rp[w0 + i];
       for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      const int64_t e0 = max(int64_t(0), rstart[0]);
-      const int64_t e1 = min(static_cast<int64_t>(n), rstart[nr]);
-      int bin[kItems];
+      int bin[kMsItems];
+      unsigned rank[kMsItems];
+      ms_bins(rstart, nr, p0, g1, c, shift, v, bin, err);
 #pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        const int i = static_cast<int>(threadIdx.x) + j * kThreads;
-        int b = -1;
-        if (i >= e0 && i < e1) {
-          int r = 0;
-          while (r + 1 < nr && i >= rstart[r + 1]) ++r;
-          const int64_t ch = static_cast<int64_t>(scol[i]) >> shift;
-          if (ch < v) b = static_cast<int>(r * v + ch);
-          else set_error(err, kErrBounds);
-        }
-        bin[j] = b;
-        const uint32_t peers = __match_any_sync(0xffffffffu, b);
-        if (b >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[b], __popc(peers));
-      }
+      for (int j = 0; j < kMsItems; ++j) rank[j] = ms_rank<true>(hist, bin[j]);
       __syncthreads();
+      // one global reservation per bin: its run of the bin's chunk in C^_reord
       {
-        const int per = (nbins + kThreads - 1) / kThreads;
+        const int per = (nbins + kMsThreads - 1) / kMsThreads;
         const int b0 = threadIdx.x * per;
-        unsigned local = 0;
-        for (int b = b0; b < min(nbins, b0 + per); ++b) local += hist[b];
-        unsigned tot;
-        const unsigned incl = block_incl_scan(local, scan_tmp, &tot);
-        unsigned run = incl - local;
         for (int b = b0; b < min(nbins, b0 + per); ++b) {
           const unsigned h = hist[b];
-          loff[b] = run;
           if (h) {
             const int64_t gchunk = (w0 + b / v) * v + (b % v);
             const int64_t q = xmap ? xmap[gchunk] : gchunk;
             goff[b] = atomicAdd(&cursor[q], static_cast<unsigned long long>(h));
           }
-          hist[b] = run;
-          run += h;
         }
-        if (threadIdx.x == 0) loff[nbins] = tot;
       }
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        const int i = static_cast<int>(threadIdx.x) + j * kThreads;
+      for (int j = 0; j < kMsItems; ++j) {
         const int b = bin[j];
-        const uint32_t peers = __match_any_sync(0xffffffffu, b);
-        const int leader = __ffs(peers) - 1;
-        unsigned base = 0;
-        if (b >= 0 && static_cast<int>(lane_id()) == leader) base = atomicAdd(&hist[b], __popc(peers));
-        base = __shfl_sync(0xffffffffu, base, leader);
         if (b >= 0) {
-          const unsigned pos = base + __popc(peers & lanemask_lt());
-          col_buf[pos] = scol[i];
-          if (VALS) val_buf[pos] = sval[i];
+          const int64_t dst = static_cast<int64_t>(goff[b]) + rank[j];
+          __stcs(&out_col[dst], static_cast<int32_t>(c[j] & wmask));
+          if (VALS) __stcs(&out_val[dst], cur.val[i0 + j]);
         }
       }
-      __syncthreads();
-      const bool last_window = w0 + gr > pr.y;
-      if (last_window && threadIdx.x == 0 && t + 2 * static_cast<int64_t>(gridDim.x) < ntiles) {
-        issue_tile<VALS>(in_col, in_val, total, t + 2 * gridDim.x, stg[s], &bars[s]);  // stage s is free
-        pending[s] = 1;
-      }
-      const int cnt = static_cast<int>(loff[nbins]);
-      for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-        const int32_t cc = col_buf[i];
-        int r = 0;
-        {
-          int lo = 0, hi = nr - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (static_cast<int>(loff[mid * v]) <= i) lo = mid; else hi = mid - 1;
-          }
-          r = lo;
-        }
-        const int b = static_cast<int>(r * v + (static_cast<int64_t>(cc) >> shift));
-        const int64_t dst = static_cast<int64_t>(goff[b]) + (i - static_cast<int>(loff[b]));
-        __stcs(&out_col[dst], static_cast<int32_t>(cc & wmask));
-        if (VALS) __stcs(&out_val[dst], val_buf[i]);
-      }
-      __syncthreads();
+    }
+    __syncthreads();  // every read of stage s is done: it may be refilled
+    if (threadIdx.x == 0 && t + 2 * static_cast<int64_t>(gridDim.x) < ntiles) {
+      issue_tile<VALS>(in_col, in_val, total, t + 2 * gridDim.x, cur, &bars[s]);
+      pending |= 1u << s;
     }
   }
   // drain: after a timeout, wait (bounded) for this block's copies still in flight before exiting
   if (threadIdx.x == 0) {
     for (int k = 0; k < 2; ++k)
-      if (pending[k]) (void)mbar_wait(&bars[k], phase[k]);
+      if ((pending >> k) & 1u) (void)mbar_wait(&bars[k], (phase >> k) & 1u);
   }
 }
 
 size_t multisplit_tma_smem(int64_t group_rows, int64_t nchunks) {
   const int64_t bins = group_rows * nchunks;
-  return static_cast<size_t>(3 * kT * 8 + bins * 8 + (group_rows + 1) * 8 + 3 * kT * 4 + bins * 4 + (bins + 1) * 4);
+  return static_cast<size_t>(2 * kT * 8 + 2 * kT * 4 + bins * 8 + (group_rows + 1) * 8 + bins * 4);
 }
 
 bool launch_multisplit_tma(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
@@ -259,17 +218,15 @@ bool launch_multisplit_tma(const int64_t* row_ptr, const int2* part, int64_t tot
   if ((reinterpret_cast<uintptr_t>(in_col) & 15) || (with_vals && (reinterpret_cast<uintptr_t>(in_val) & 15)))
     return false;
   const int64_t ntiles = ceil_div(total, static_cast<int64_t>(kT));
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, sms));
+  auto kern = with_vals ? k_multisplit_tma<true> : k_multisplit_tma<false>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMsThreads, smem);
+  if (per_sm < 1) per_sm = 1;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * per_sm));
   note_launch();
-  if (with_vals) {
-    cudaFuncSetAttribute(k_multisplit_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k_multisplit_tma<true><<<grid, kThreads, smem, s>>>(row_ptr, part, total, ntiles, in_col, in_val, shift, nchunks,
-                                                        group_rows, xmap, cursor, out_col, out_val, err);
-  } else {
-    cudaFuncSetAttribute(k_multisplit_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k_multisplit_tma<false><<<grid, kThreads, smem, s>>>(row_ptr, part, total, ntiles, in_col, nullptr, shift,
-                                                         nchunks, group_rows, xmap, cursor, out_col, nullptr, err);
-  }
+  kern<<<grid, kMsThreads, smem, s>>>(row_ptr, part, total, ntiles, in_col, with_vals ? in_val : nullptr, shift,
+                                      nchunks, group_rows, xmap, cursor, out_col, with_vals ? out_val : nullptr, err);
   return true;
 }
 
