@@ -830,7 +830,21 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
     set_last_error("smem_bytes exceeds the device's shared memory per block");
     return fail(SPGEMM_ERR_INVALID_ARG);
   }
-  if ((rc = plan_params(n, s_lm, &h->opt, &h->plan)) != SPGEMM_OK) {
+  // The dense chunk accumulator runs kDenseBlocksPerSm blocks per SM (their per-chunk phases
+  // overlap; one 16,384-wide block per SM measured 22.4 ms against 18.1 ms for three 8,192-wide
+  // ones on R-MAT scale 18), so unless the caller fixes W its local memory is that share of the
+  // SM's shared memory: W is the widest power of two whose dense block (values, bitmap, word
+  // prefix, hub copies) fits in the share, the dense width of Eq. 5 for that s_LM.
+  spgemm_options popt = h->opt;
+  if (!popt.chunk_width && !popt.smem_bytes) {
+    int smem_sm = 0;
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    const size_t share = static_cast<size_t>(smem_sm / kDenseBlocksPerSm) - 1024;  // 1 KB per block for the system
+    int64_t w = 0;
+    for (int64_t c = 1024; c <= (int64_t(1) << 24) && chunk_smem_bytes(c, 0, 2, false) <= share; c *= 2) w = c;
+    if (w) popt.chunk_width = w;
+  }
+  if ((rc = plan_params(n, s_lm, &popt, &h->plan)) != SPGEMM_OK) {
     set_last_error("planner rejected the options");
     return fail(rc);
   }

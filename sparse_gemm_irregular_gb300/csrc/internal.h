@@ -23,7 +23,8 @@ constexpr int kSmemReserve = 7168;         // bytes kept back from s_LM for per-
 constexpr int kMaxLadder = 16;             // light bin ladder levels
 constexpr int kScanTile = 4096;            // elements per scan block (512 threads x 8)
 constexpr int kPhaseSlots = 13;            // timed regions, see spgemm_get_phase_times
-constexpr int64_t kChunkDenseMin = 2048;   // last-level chunks above this size use the dense accumulator
+constexpr int64_t kChunkDenseMin = 1024;   // last-level chunks above this size use the dense accumulator
+constexpr int kDenseBlocksPerSm = 3;        // dense chunk accumulator blocks per SM (sets the default W)
 
 // Light-row / chunk bin ladder derived from tau (hash tables at load factor 1/2).
 struct Ladder {
@@ -158,6 +159,8 @@ void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t
 void launch_chunk_classify(const int64_t* f_cnt, int64_t n, int64_t bitmap_from, const BinRule& rule,
                            uint8_t* bin, cudaStream_t s);
 // bitmap-ordered chunk accumulators (k_chunk.cu); mode 0 symbolic, 1 hash numeric, 2 dense numeric
+// Shared memory of one chunk group (mode 2: the dense accumulator block).
+size_t chunk_smem_bytes(int64_t width, int64_t slots, int mode, bool warp);
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
                          int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
                          cudaStream_t s);

@@ -295,10 +295,10 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   }
 }
 
-// Dense numeric accumulation as persistent blocks (one per SM; the 16,384-double array fills
-// most of the shared memory).  With one block per SM the per-chunk latency (taking the next
+// Dense numeric accumulation as persistent blocks (as many per SM as the W-double value arrays
+// allow: three 256-thread blocks at the default W = 8192).  With few blocks per SM the per-chunk latency (taking the next
 // chunk from the work counter, the chain of descriptor loads) would sit on the critical path, so
-// warp 0 is a helper: while warps 1..31 stream the current chunk it takes the next chunk and
+// warp 0 is a helper: while the other warps stream the current chunk it takes the next chunk and
 // loads its descriptor into a second shared slot.  The value array is zeroed once and every
 // chunk clears the slots it writes.  Hub columns (hub_index) add into private copies of their
 // sums in shared memory, merged once per chunk, so the hottest columns of power-law inputs do
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
   const int64_t words = (p.width + 31) / 32;
   const uint32_t width = static_cast<uint32_t>(p.width);
   const int warp = threadIdx.x >> 5;
-  const int nwork = (blockDim.x >> 5) - 1;  // streaming warps 1..31
+  const int nwork = (blockDim.x >> 5) - 1;  // streaming warps 1..nwork
   const int nt = nwork * 32;
   const int t = static_cast<int>(threadIdx.x) - 32;
   double* acc = L2 ? gacc_all + static_cast<int64_t>(blockIdx.x) * p.width : s.vals;
@@ -502,20 +502,29 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
   } else if (mode == 1) {
     if (warp) ck_launch<true, 1>(p, tpr, s); else ck_launch<false, 1>(p, tpr, s);
   } else {
-    int dev = 0, sms = 0;
+    int dev = 0, sms = 0, smem_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t blocks = std::min<int64_t>(count, sms);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     cudaMemsetAsync(counter, 0, sizeof(int), s);
     note_launch();
-    if (gacc) {  // L2-resident accumulators: the shared array is not needed
+    if (gacc) {  // L2-resident accumulators (one per SM): the shared array is not needed
+      const int64_t blocks = std::min<int64_t>(count, sms);
       const size_t smem = chunk_smem_bytes(width, 0, 3, false);
       cudaFuncSetAttribute(k_chunk_dense<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       k_chunk_dense<true><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, gacc);
     } else {
+      // as many blocks per SM as the value arrays allow; the block shrinks with them (three
+      // 256-thread blocks of W = 8192 beat two of 512 threads and one of 1024 at W = 16384)
       const size_t smem = chunk_smem_bytes(width, 0, 2, false);
+      const int fit = static_cast<int>(smem_sm / (smem + 1024));
+      const int threads = fit >= 3 ? 256 : (fit == 2 ? 512 : 1024);
       cudaFuncSetAttribute(k_chunk_dense<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      k_chunk_dense<false><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, nullptr);
+      int per_sm = 1;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_chunk_dense<false>, threads, smem);
+      if (per_sm < 1) per_sm = 1;
+      const int64_t blocks = std::min<int64_t>(count, static_cast<int64_t>(sms) * per_sm);
+      k_chunk_dense<false><<<static_cast<unsigned>(blocks), threads, smem, s>>>(p, counter, nullptr);
     }
   }
 }
