@@ -21,10 +21,11 @@ constexpr int kCkWarpsPerBlock = 8;
 // set bit of its index, so these few columns take a large share of the products of every
 // chunk (local column 0 alone ~2% on R-MAT with a = 0.57).  Shared-memory fp64 atomics
 // serialise badly on one address, so hub products add into one of kHubCopies private copies of
-// the hub slots (every group of four streaming warps shares a copy); the copies are merged once
-// per chunk.  Eight copies measured best: fewer copies contend, more copies lengthen the merge,
-// a serial chain of fp64 adds per slot.  On other inputs the hubs are just ordinary columns.
-constexpr int kHubCopies = 8;
+// the hub slots (streaming warp w uses copy w mod kHubCopies); the copies are merged once per
+// chunk.  Fewer copies contend, more copies lengthen the merge, a serial chain of fp64 adds per
+// slot: with 1024-thread blocks 8 copies beat 31, 16 and 4; with the default 256-thread blocks
+// 4 copies beat 8.  On other inputs the hubs are just ordinary columns.
+constexpr int kHubCopies = 4;
 constexpr int kHubBits = 16;
 constexpr int kHubSlots = 1 + kHubBits + kHubBits * (kHubBits - 1) / 2;  // 137
 static_assert(kHubSlots == kChunkHubSlots, "hub slot count");
