@@ -162,6 +162,21 @@ int spgemm_numeric(spgemm_handle h, int32_t* c_col_idx, double* c_vals);
 int spgemm_numeric_rows(spgemm_handle h, int64_t row_begin, int64_t row_end, int32_t* c_col_idx,
                         double* c_vals);
 
+/* Numeric phase into HOST memory: c_col_idx (c_nnz int32) and c_vals (c_nnz fp64) are host
+ * arrays, caller-owned (page-locked memory reaches the full copy bandwidth; pageable memory
+ * works, slowly).  C is computed in row windows of about window_nnz entries (0: a quarter of
+ * C, at least 4 M entries, staging at most a fifth of the free device memory) into two device
+ * staging buffers from the handle's pool; each finished window is copied to the host on a
+ * second stream while the next one is computed.  When heavy batches are recomputed in the
+ * numeric phase, windows hold whole batches.  If c_row_ptr is not NULL it receives the m+1
+ * row offsets (host).  Returns after every copy has landed; no device array of C's size is
+ * needed, so a C larger than the device can be produced.  Errors: BAD_STATE before symbolic,
+ * INVALID_ARG for NULL arrays with c_nnz > 0 or a negative window, OUT_OF_MEMORY when a
+ * window's staging does not fit.  The pages have no counterpart: it is the host end of the
+ * row-window numeric phase. */
+int spgemm_numeric_host(spgemm_handle h, int64_t* c_row_ptr, int32_t* c_col_idx, double* c_vals,
+                        int64_t window_nnz);
+
 int spgemm_get_stats(spgemm_handle h, spgemm_stats* out);
 int spgemm_get_plan(spgemm_handle h, spgemm_plan* out);
 

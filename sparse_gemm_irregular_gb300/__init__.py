@@ -10,6 +10,7 @@ from dataclasses import dataclass
 
 from . import binding
 from .binding import (SpgemmError, load, options, spgemm_create, spgemm_destroy, spgemm_get_phase_times,
+                      spgemm_numeric_host,
                       spgemm_get_plan, spgemm_get_stats, spgemm_kernel_launches, spgemm_last_error, spgemm_numeric,
                       spgemm_numeric_rows, spgemm_plan_params, spgemm_release_memory, spgemm_strerror,
                       spgemm_symbolic)
@@ -92,6 +93,17 @@ class Product:
 
     def numeric_rows(self, row_begin: int, row_end: int, col, val):
         spgemm_numeric_rows(self.h, row_begin, row_end, col.data_ptr(), val.data_ptr())
+
+    def numeric_host(self, col, val, row_ptr=None, window_nnz: int = 0):
+        """Numeric phase into host (CPU) tensors col (int32, nnz) and val (float64, nnz), and
+        row_ptr (int64, rows+1) when given; pinned tensors reach the full copy bandwidth."""
+        for t in (col, val) + ((row_ptr,) if row_ptr is not None else ()):
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError("numeric_host wants contiguous CPU tensors")
+        if col.numel() < self.nnz or val.numel() < self.nnz:
+            raise ValueError("host arrays shorter than nnz(C)")
+        spgemm_numeric_host(self.h, row_ptr.data_ptr() if row_ptr is not None else 0, col.data_ptr(),
+                            val.data_ptr(), window_nnz)
 
     def stats(self):
         return spgemm_get_stats(self.h)

@@ -71,6 +71,7 @@ EXPORTS = {
     "spgemm_symbolic": (ctypes.c_int, [_vp, _vp, _vp]),
     "spgemm_numeric": (ctypes.c_int, [_vp, _vp, _vp]),
     "spgemm_numeric_rows": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
+    "spgemm_numeric_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64]),
     "spgemm_get_stats": (ctypes.c_int, [_vp, _vp]),
     "spgemm_get_plan": (ctypes.c_int, [_vp, _vp]),
     "spgemm_get_phase_times": (ctypes.c_int, [_vp, _vp, _vp, _i32]),
@@ -149,6 +150,11 @@ def spgemm_numeric(h, c_col: int, c_val: int):
 def spgemm_numeric_rows(h, row_begin: int, row_end: int, c_col: int, c_val: int):
     _check(load().spgemm_numeric_rows(h, row_begin, row_end, _vp(c_col), _vp(c_val)),
            "spgemm_numeric_rows")
+
+
+def spgemm_numeric_host(h, c_row_ptr: int, c_col: int, c_val: int, window_nnz: int = 0):
+    _check(load().spgemm_numeric_host(h, _vp(c_row_ptr) if c_row_ptr else None, _vp(c_col), _vp(c_val),
+                                      window_nnz), "spgemm_numeric_host")
 
 
 def spgemm_get_stats(h) -> spgemm_stats:

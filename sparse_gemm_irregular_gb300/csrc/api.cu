@@ -736,11 +736,9 @@ void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
   }
 }
 
-int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
-  if (h->state < 2) {
-    set_last_error("numeric called before symbolic");
-    return SPGEMM_ERR_BAD_STATE;
-  }
+// Enqueue the numeric phase of rows [rb, re) on the handle's stream, written at offset 0 =
+// row_ptr[rb] of c_col / c_val; no synchronisation.
+int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
   Sink sk{};
   sk.row_ptr = h->c_row_ptr;
   sk.c_col = c_col;
@@ -775,7 +773,46 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
     }
   }
   join_light(h);
+  return SPGEMM_OK;
+}
+
+int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
+  if (h->state < 2) {
+    set_last_error("numeric called before symbolic");
+    return SPGEMM_ERR_BAD_STATE;
+  }
+  SG_TRY(numeric_enqueue(h, rb, re, c_col, c_val));
   return sync_and_check(h, "numeric");
+}
+
+// Row windows of the host-streamed numeric phase.  A recomputed heavy batch is expanded once per
+// window that intersects its rows, so when batches are not resident every cut falls between two
+// batches (each window then holds whole batches); resident products are cut every ~target
+// entries of C.
+std::vector<int64_t> host_windows(const spgemm_ctx* h, const std::vector<int64_t>& rp, int64_t target) {
+  std::vector<int64_t> cuts{0};
+  const int64_t m = h->m;
+  if (!h->resident && h->batches.size() > 1) {
+    for (size_t b = 1; b < h->batches.size(); ++b) {
+      const int64_t c = h->batches[b].row_lo;  // first heavy row of batch b; rows before it belong to earlier windows
+      if (c > cuts.back() && rp[c] - rp[cuts.back()] >= target) cuts.push_back(c);
+    }
+  } else if (h->resident || h->batches.empty()) {
+    int64_t r = 0;
+    while (r < m) {
+      // first row whose prefix reaches the next target (binary search on the row pointer)
+      const int64_t goal = rp[r] + target;
+      int64_t lo = r + 1, hi = m;
+      while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (rp[mid] >= goal) hi = mid; else lo = mid + 1;
+      }
+      r = lo;
+      if (r < m) cuts.push_back(r);
+    }
+  }
+  cuts.push_back(m);
+  return cuts;
 }
 
 }  // namespace
@@ -1076,6 +1113,78 @@ int spgemm_numeric_rows(spgemm_handle h, int64_t row_begin, int64_t row_end, int
   return numeric_window(h, row_begin, row_end, c_col_idx, c_vals);
 }
 
+int spgemm_numeric_host(spgemm_handle h, int64_t* c_row_ptr, int32_t* c_col_idx, double* c_vals,
+                        int64_t window_nnz) {
+  g_last_error.clear();
+  if (!h || window_nnz < 0) return SPGEMM_ERR_INVALID_ARG;
+  if (h->state < 2) {
+    set_last_error("numeric called before symbolic");
+    return SPGEMM_ERR_BAD_STATE;
+  }
+  const int64_t nnz = h->stats.c_nnz, m = h->m;
+  if (nnz > 0 && (!c_col_idx || !c_vals)) return SPGEMM_ERR_INVALID_ARG;
+  std::vector<int64_t> rp(static_cast<size_t>(m + 1));
+  SG_TRY(check_cuda(cudaMemcpyAsync(rp.data(), h->c_row_ptr, sizeof(int64_t) * (m + 1), cudaMemcpyDeviceToHost, h->st),
+                    "copy row_ptr"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "copy row_ptr"));
+  if (c_row_ptr) std::copy(rp.begin(), rp.end(), c_row_ptr);
+  if (nnz == 0) return spgemm_numeric(h, nullptr, nullptr);
+  // default window: a quarter of C, at least 4 M entries, staging at most a fifth of free memory
+  size_t free_b = 0, total_b = 0;
+  cudaMemGetInfo(&free_b, &total_b);
+  int64_t target = window_nnz ? window_nnz : std::max<int64_t>(nnz / 4, int64_t(1) << 22);
+  target = std::min<int64_t>(target, std::max<int64_t>(1, static_cast<int64_t>(free_b / 5 / 24)));
+  const std::vector<int64_t> cuts = host_windows(h, rp, target);
+  int64_t wmax = 0;
+  for (size_t w = 0; w + 1 < cuts.size(); ++w) wmax = std::max(wmax, rp[cuts[w + 1]] - rp[cuts[w]]);
+  if (!h->st_copy && cudaStreamCreateWithFlags(&h->st_copy, cudaStreamNonBlocking) != cudaSuccess) {
+    set_last_error("copy stream creation failed");
+    return SPGEMM_ERR_CUDA;
+  }
+  for (int b = 0; b < 2; ++b) {
+    if (!h->ev_done[b] && cudaEventCreateWithFlags(&h->ev_done[b], cudaEventDisableTiming) != cudaSuccess)
+      return SPGEMM_ERR_CUDA;
+    if (!h->ev_copied[b] && cudaEventCreateWithFlags(&h->ev_copied[b], cudaEventDisableTiming) != cudaSuccess)
+      return SPGEMM_ERR_CUDA;
+  }
+  // two staging buffers: window w is computed into buffer w % 2 while window w - 1 is copied out
+  const int nbuf = cuts.size() > 2 ? 2 : 1;
+  int32_t* scol[2] = {nullptr, nullptr};
+  double* sval[2] = {nullptr, nullptr};
+  for (int b = 0; b < nbuf; ++b) {
+    SG_ALLOC(scol[b], int32_t, wmax);
+    SG_ALLOC(sval[b], double, wmax);
+  }
+  int rc = SPGEMM_OK;
+  for (size_t w = 0; w + 1 < cuts.size() && rc == SPGEMM_OK; ++w) {
+    const int b = static_cast<int>(w % nbuf);
+    const int64_t rb = cuts[w], re = cuts[w + 1], off = rp[rb], cnt = rp[re] - rp[rb];
+    if (w >= static_cast<size_t>(nbuf)) cudaStreamWaitEvent(h->st, h->ev_copied[b], 0);  // buffer free again
+    rc = numeric_enqueue(h, rb, re, scol[b], sval[b]);
+    if (rc != SPGEMM_OK) break;
+    cudaEventRecord(h->ev_done[b], h->st);
+    cudaStreamWaitEvent(h->st_copy, h->ev_done[b], 0);
+    if (cnt > 0) {
+      cudaMemcpyAsync(c_col_idx + off, scol[b], sizeof(int32_t) * cnt, cudaMemcpyDeviceToHost, h->st_copy);
+      cudaMemcpyAsync(c_vals + off, sval[b], sizeof(double) * cnt, cudaMemcpyDeviceToHost, h->st_copy);
+    }
+    cudaEventRecord(h->ev_copied[b], h->st_copy);
+  }
+  // the handle's stream waits for the last copies, so the staging buffers are freed after them
+  for (int b = 0; b < nbuf; ++b) cudaStreamWaitEvent(h->st, h->ev_copied[b], 0);
+  for (int b = 0; b < nbuf; ++b) {
+    ws_free(h, scol[b]);
+    ws_free(h, sval[b]);
+  }
+  if (rc != SPGEMM_OK) {
+    cudaStreamSynchronize(h->st_copy);
+    cudaStreamSynchronize(h->st);
+    return rc;
+  }
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st_copy), "numeric host copies"));
+  return sync_and_check(h, "numeric");
+}
+
 int spgemm_get_stats(spgemm_handle h, spgemm_stats* out) {
   if (!h || !out) return SPGEMM_ERR_INVALID_ARG;
   *out = h->stats;
@@ -1107,6 +1216,11 @@ int spgemm_destroy(spgemm_handle h) {
   for (void* p : h->allocs) cudaFreeAsync(p, h->st);
   h->allocs.clear();
   cudaStreamSynchronize(h->st);
+  for (int b = 0; b < 2; ++b) {
+    if (h->ev_done[b]) cudaEventDestroy(h->ev_done[b]);
+    if (h->ev_copied[b]) cudaEventDestroy(h->ev_copied[b]);
+  }
+  if (h->st_copy) cudaStreamDestroy(h->st_copy);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->st_light) cudaStreamDestroy(h->st_light);

@@ -215,6 +215,8 @@ struct spgemm_ctx {
   cudaStream_t st = nullptr;
   cudaStream_t st_light = nullptr;  // light rows (the heavy pipeline stays on st)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaStream_t st_copy = nullptr;   // device-to-host copies of the host-streamed numeric phase
+  cudaEvent_t ev_done[2] = {nullptr, nullptr}, ev_copied[2] = {nullptr, nullptr};
   int device = 0, sms = 0;
   cudaMemPool_t pool = nullptr;
   int64_t smem_optin = 0, l2_bytes = 0;

@@ -196,3 +196,38 @@ def test_validate_flag_rejects_bad_column(gpu_lib):
     with pytest.raises(sg.SpgemmError) as e:
         sg.Product(dA, B, opts=opts(flags=8))
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("case,window", [("rmat", 0), ("rmat", 20000), ("recompute", 3000), ("light", 2000),
+                                         ("rmat", 1)])
+def test_numeric_host_windows(gpu_lib, case, window):
+    """spgemm_numeric_host: C computed in row windows and streamed into pinned host arrays equals
+    the oracle -- one window, many windows (down to one row each), recomputed heavy batches
+    (windows of whole batches) and light rows only."""
+    import torch
+    import sparse_gemm_irregular_gb300 as sg
+    if case == "rmat":
+        A, B, kw = synth.rmat(13, 16, seed=8), None, None
+    elif case == "recompute":
+        A = synth.random_sparse(200, 180, 0.06, 3, duplicates=True, empty_rows=True, sort_rows=False)
+        B = synth.random_sparse(180, 500, 0.08, 12, duplicates=True, empty_rows=True, sort_rows=False)
+        kw = dict(tau=16, chunk_width=64, chunks_max=4, heavy_batch_elems=700, flags=16)
+    else:
+        A = synth.random_sparse(300, 250, 0.05, 5, duplicates=True, empty_rows=True, sort_rows=False)
+        B = synth.random_sparse(250, 400, 0.05, 6)
+        kw = dict(flags=2 | 4, tau=4096)
+    B = A if B is None else B
+    dA = sg.DeviceCSR.from_host(A)
+    dB = dA if B is A else sg.DeviceCSR.from_host(B)
+    p = sg.Product(dA, dB, opts=opts(**kw) if kw else None)
+    try:
+        _, nnz = p.symbolic()
+        rp = torch.empty(A.rows + 1, dtype=torch.int64).pin_memory()
+        col = torch.empty(max(nnz, 1), dtype=torch.int32).pin_memory()
+        val = torch.empty(max(nnz, 1), dtype=torch.float64).pin_memory()
+        p.numeric_host(col, val, rp, window_nnz=window)
+        if case == "recompute":
+            assert p.stats().resident == 0
+    finally:
+        p.close()
+    compare_full(A, B, rp.numpy(), col.numpy()[:nnz], val.numpy()[:nnz], threads=16)
