@@ -244,33 +244,27 @@ __device__ __forceinline__ int64_t expand_chunk(const Group<WARP>& g, const Smem
 }
 
 // ---- outputs -----------------------------------------------------------------------------
-// Block-wide exclusive prefix of the set-bit counts of `words` bitmap words, written to pre[];
-// returns the total.  Each warp owns a contiguous run of words (read lane-strided, so without
-// bank conflicts) and scans it with shuffles; one barrier exchanges the warp totals.
-// `tmp` holds 32 unsigned.  Ends with a barrier.
-__device__ unsigned block_word_prefix(const Group<false>& g, const uint32_t* bits, int64_t words,
-                                      int32_t* pre, unsigned* tmp) {
+// Block-wide exclusive prefix of n unsigned counters, in place.  Each warp owns a contiguous run
+// of counters (read lane-strided, without bank conflicts) and scans it with shuffles; one
+// barrier exchanges the run totals.  `tmp` holds 32 unsigned.  Ends with a barrier.
+__device__ void block_exclusive_scan_inplace(const Group<false>& g, unsigned* a, int64_t n, unsigned* tmp) {
   const int nwarps = g.size >> 5, warp = g.lane >> 5, l = g.lane & 31;
-  const int64_t per = ceil_div(ceil_div(words, nwarps), 32) * 32;
-  const int64_t wb = warp * per, we = min(words, wb + per);
+  const int64_t per = ceil_div(ceil_div(n, nwarps), 32) * 32;
+  const int64_t wb = warp * per, we = min(n, wb + per);
   unsigned c = 0;
-  for (int64_t w = wb + l; w < we; w += 32) c += __popc(bits[w]);
+  for (int64_t i = wb + l; i < we; i += 32) c += a[i];
   c = warp_sum(c);
   if (l == 0) tmp[warp] = c;
   __syncthreads();
-  const unsigned mine = l < warp ? tmp[l] : 0u;
-  const unsigned all = l < nwarps ? tmp[l] : 0u;
-  unsigned run = warp_sum(mine);
-  const unsigned total = warp_sum(all);
-  for (int64_t w0 = wb; w0 < we; w0 += 32) {
-    const int64_t w = w0 + l;
-    const unsigned x = w < we ? __popc(bits[w]) : 0u;
+  unsigned run = warp_sum(l < warp ? tmp[l] : 0u);
+  for (int64_t i0 = wb; i0 < we; i0 += 32) {
+    const int64_t i = i0 + l;
+    const unsigned x = i < we ? a[i] : 0u;
     const unsigned incl = warp_incl_scan(x);
-    if (w < we) pre[w] = static_cast<int32_t>(run + incl - x);
+    if (i < we) a[i] = run + incl - x;
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
   __syncthreads();
-  return total;
 }
 
 // Compact the occupied slots of a block's hash table to [0, n) in place; returns n.  The order
@@ -318,13 +312,16 @@ __device__ int64_t block_compact(const Group<false>& g, const Smem& s, int64_t s
   return written;
 }
 
-// Ordered write of the `n` compacted entries [0, n) of a block's hash table without sorting:
-// the unused part of the table becomes a column bitmap (keys region: bit words, values
-// region: their exclusive prefix) covering a window of 32 * (slots - n) columns; the window
-// slides over the row's column range [lo, hi], and an entry's output position is the number
-// of set bits below its column.  slots >= 2n, so every window covers at least 32n columns.
-__device__ void block_rank_emit(const Group<false>& g, const Smem& s, int64_t slots, int64_t n, int64_t expected,
-                                int32_t col_base, int32_t* c_col, double* c_val, uint32_t* err) {
+// Ordered write of the `n` compacted entries [0, n) of a block's hash table without sorting, in
+// a number of barriers independent of the row's column span.  When the span [lo, hi] fits one
+// bitmap in the free part of the keys region, an entry's rank is the number of set bits below
+// its column.  Otherwise: a counting sort of the entries into B >= n buckets of equal column
+// width (B = the largest power of two not above the free slots, counters in the free keys
+// region) and a rank inside the bucket by comparison with its few members.  Either way the
+// entry index is scattered to its rank (index arrays in the free part of the values region:
+// slots >= 2n leaves 2n free words there) and the write of C is coalesced.
+__device__ void block_bucket_emit(const Group<false>& g, const Smem& s, int64_t slots, int64_t n, int64_t expected,
+                                  int32_t col_base, int32_t* c_col, double* c_val, uint32_t* err) {
   if (n != expected) {
     if (g.lane == 0) set_error(err, kErrRowOverflow);
     return;
@@ -363,32 +360,63 @@ __device__ void block_rank_emit(const Group<false>& g, const Smem& s, int64_t sl
   lo = red[64];
   hi = red[65];
   __syncthreads();
-  uint32_t* bits = reinterpret_cast<uint32_t*>(s.keys + n);        // slots - n words
-  int32_t* pre = reinterpret_cast<int32_t*>(s.vals + n);           // 2 (slots - n) words available
-  const int64_t nw_max = slots - n;
-  int64_t base = 0;
-  for (int64_t ws = lo; ws <= hi; ws += 32 * nw_max) {
-    const int64_t nwin = min(nw_max, (static_cast<int64_t>(hi) - ws) / 32 + 1);
-    for (int64_t w = g.lane; w < nwin; w += g.size) bits[w] = 0u;
+  const int64_t span_words = (static_cast<int64_t>(hi) - lo) / 32 + 1;
+  if (span_words <= slots - n) {
+    // the row's column span fits one bitmap in the free keys region: rank = set bits below the
+    // column (prefix of the word popcounts in the free values region)
+    uint32_t* bits = reinterpret_cast<uint32_t*>(s.keys + n);        // span_words
+    unsigned* pre = reinterpret_cast<unsigned*>(s.vals) + 2 * n;     // span_words
+    int32_t* inv = reinterpret_cast<int32_t*>(pre + span_words);     // n (2n + span_words + n <= 2 slots)
+    for (int64_t w = g.lane; w < span_words; w += g.size) bits[w] = 0u;
     __syncthreads();
     for (int64_t i = g.lane; i < n; i += g.size) {
-      const int64_t c = static_cast<int64_t>(s.keys[i]) - ws;
-      if (c >= 0 && c < 32 * nwin) atomicOr(&bits[c >> 5], 1u << (c & 31));
+      const int32_t c = s.keys[i] - lo;
+      atomicOr(&bits[c >> 5], 1u << (c & 31));
     }
     __syncthreads();
-    const int64_t run = block_word_prefix(g, bits, nwin, pre, reinterpret_cast<unsigned*>(s.tmp));
+    for (int64_t w = g.lane; w < span_words; w += g.size) pre[w] = __popc(bits[w]);
+    __syncthreads();
+    block_exclusive_scan_inplace(g, pre, span_words, reinterpret_cast<unsigned*>(s.tmp));
     for (int64_t i = g.lane; i < n; i += g.size) {
-      const int32_t k = s.keys[i];
-      const int64_t c = static_cast<int64_t>(k) - ws;
-      if (c >= 0 && c < 32 * nwin) {
-        const uint32_t word = bits[c >> 5];
-        const int64_t r = base + pre[c >> 5] + __popc(word & ((1u << (c & 31)) - 1u));
-        c_col[r] = k + col_base;
-        c_val[r] = s.vals[i];
-      }
+      const int32_t c = s.keys[i] - lo;
+      inv[pre[c >> 5] + __popc(bits[c >> 5] & ((1u << (c & 31)) - 1u))] = static_cast<int32_t>(i);
     }
-    base += run;
     __syncthreads();
+    for (int64_t r = g.lane; r < n; r += g.size) {
+      const int32_t i = inv[r];
+      c_col[r] = s.keys[i] + col_base;
+      c_val[r] = s.vals[i];
+    }
+    return;
+  }
+  int64_t nb = 1;  // buckets
+  while (nb * 2 <= slots - n) nb *= 2;
+  int shift = 0;    // bucket of a key: (key - lo) >> shift < nb
+  while (((static_cast<int64_t>(hi) - lo) >> shift) >= nb) ++shift;
+  unsigned* cnt = reinterpret_cast<unsigned*>(s.keys + n);      // nb counters
+  int32_t* order = reinterpret_cast<int32_t*>(s.vals) + 2 * n;  // n entry indices, bucket by bucket
+  int32_t* inv = order + n;                                     // n: entry index of each output position
+  for (int64_t b = g.lane; b < nb; b += g.size) cnt[b] = 0u;
+  __syncthreads();
+  for (int64_t i = g.lane; i < n; i += g.size) atomicAdd(&cnt[(s.keys[i] - lo) >> shift], 1u);
+  __syncthreads();
+  block_exclusive_scan_inplace(g, cnt, nb, reinterpret_cast<unsigned*>(s.tmp));  // cnt[b]: start of bucket b
+  for (int64_t i = g.lane; i < n; i += g.size)
+    order[atomicAdd(&cnt[(s.keys[i] - lo) >> shift], 1u)] = static_cast<int32_t>(i);  // cnt[b]: end of bucket b
+  __syncthreads();
+  for (int64_t i = g.lane; i < n; i += g.size) {
+    const int32_t k = s.keys[i];
+    const int64_t bk = (k - lo) >> shift;
+    const unsigned b0 = bk > 0 ? cnt[bk - 1] : 0u, b1 = cnt[bk];
+    unsigned r = b0;
+    for (unsigned j = b0; j < b1; ++j) r += s.keys[order[j]] < k ? 1u : 0u;  // columns are distinct
+    inv[r] = static_cast<int32_t>(i);
+  }
+  __syncthreads();
+  for (int64_t r = g.lane; r < n; r += g.size) {
+    const int32_t i = inv[r];
+    c_col[r] = s.keys[i] + col_base;
+    c_val[r] = s.vals[i];
   }
 }
 
@@ -401,7 +429,7 @@ __device__ void hash_emit(const Group<WARP>& g, const Smem& s, int64_t slots, in
                           uint32_t* err) {
   if constexpr (!WARP) {
     const int64_t m = block_compact(g, s, slots);
-    block_rank_emit(g, s, slots, m, expected, col_base, c_col, c_val, err);
+    block_bucket_emit(g, s, slots, m, expected, col_base, c_col, c_val, err);
     return;
   }
   int64_t written = 0;
