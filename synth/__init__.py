@@ -23,6 +23,9 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
+import concurrent.futures
+import os
+
 import numpy as np
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -156,25 +159,39 @@ def rmat_edges(scale: int, n_edges: int, a: float, b: float, c: float, seed: int
                block: int = 1 << 22):
     """R-MAT edge list: for every edge and every level (most significant bit first) one
     uniform draw u picks quadrant (0,0) if u < a, (0,1) if u < a+b, (1,0) if u < a+b+c,
-    else (1,1)."""
+    else (1,1).  Blocks of edges are independent (counter-based draws), so they are generated
+    by a thread pool (numpy releases the GIL on these array operations); the result does not
+    depend on the number of threads."""
     rows = np.empty(n_edges, dtype=np.int64)
     cols = np.empty(n_edges, dtype=np.int64)
     ab, abc = a + b, a + b + c
-    for e0 in range(0, n_edges, block):
+    key = _key(seed, STREAM_STRUCT)
+
+    def one(e0):
         e1 = min(n_edges, e0 + block)
         ne = e1 - e0
         r = np.zeros(ne, dtype=np.int64)
         cc = np.zeros(ne, dtype=np.int64)
-        base = np.arange(e0, e1, dtype=np.uint64) * np.uint64(scale)
-        for lvl in range(scale):
-            # draw index = edge * scale + level
-            u = to_unit(_fin((base + np.uint64(lvl + 1)) * _GAMMA + _key(seed, STREAM_STRUCT)))
-            rbit = (u >= ab).astype(np.int64)
-            cbit = (((u >= a) & (u < ab)) | (u >= abc)).astype(np.int64)
-            r = (r << 1) | rbit
-            cc = (cc << 1) | cbit
+        with np.errstate(over="ignore"):
+            base = np.arange(e0, e1, dtype=np.uint64) * np.uint64(scale)
+            for lvl in range(scale):
+                # draw index = edge * scale + level
+                u = to_unit(_fin((base + np.uint64(lvl + 1)) * _GAMMA + key))
+                rbit = (u >= ab).astype(np.int64)
+                cbit = (((u >= a) & (u < ab)) | (u >= abc)).astype(np.int64)
+                r = (r << 1) | rbit
+                cc = (cc << 1) | cbit
         rows[e0:e1] = r
         cols[e0:e1] = cc
+
+    starts = list(range(0, n_edges, block))
+    workers = max(1, min(len(starts), os.cpu_count() or 1, 16))
+    if workers == 1:
+        for e0 in starts:
+            one(e0)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, starts))
     return rows, cols
 
 

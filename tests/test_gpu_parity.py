@@ -231,3 +231,58 @@ def test_numeric_host_windows(gpu_lib, case, window):
     finally:
         p.close()
     compare_full(A, B, rp.numpy(), col.numpy()[:nnz], val.numpy()[:nnz], threads=16)
+
+
+def test_config4_row_windows(gpu_lib):
+    """R-MAT scale 21, edge factor 32: C (about 6e10 entries) fits neither the device nor the
+    test host.  The symbolic phase runs at full size (heavy batches recomputed, not resident);
+    the numeric phase runs in row windows (spgemm_numeric_rows) -- the heaviest rows, a middle
+    block and the last block.  Every window row is checked against C x = A (B x); every window
+    row with at most 2e6 intermediate products against the oracle."""
+    import torch
+    import sparse_gemm_irregular_gb300 as sg
+    A = synth.config(4)
+    ip = oracle.row_ip(A, A)
+    dA = sg.DeviceCSR.from_host(A)
+    p = sg.Product(dA, dA)
+    try:
+        rp, nnz = p.symbolic()
+        st = p.stats()
+        assert st.rows_heavy > 0 and st.resident == 0
+        rp_h = rp.cpu().numpy()
+        del rp
+        row_nnz = np.diff(rp_h)
+        assert rp_h[0] == 0 and rp_h[-1] == nnz and np.all(row_nnz >= 0) and np.all(row_nnz <= ip)
+        x = synth.uniform(11, synth.STREAM_SAMPLE, 0, A.cols, 0.0, 1.0)
+        brow = np.repeat(np.arange(A.rows), np.diff(A.row_ptr))
+        bx = np.bincount(brow, weights=A.val * x[A.col], minlength=A.rows)  # B x (B = A)
+        m = A.rows
+        checked = 0
+        for rb, re in [(0, 32), (m // 2, m // 2 + 8192), (m - 8192, m)]:
+            cnt = int(rp_h[re] - rp_h[rb])
+            col = torch.empty(max(cnt, 1), dtype=torch.int32, device="cuda")
+            val = torch.empty(max(cnt, 1), dtype=torch.float64, device="cuda")
+            p.numeric_rows(rb, re, col, val)
+            torch.cuda.synchronize()
+            c = col.cpu().numpy()[:cnt]
+            v = val.cpu().numpy()[:cnt]
+            del col, val
+            lrp = rp_h[rb:re + 1] - rp_h[rb]
+            rid = np.repeat(np.arange(re - rb), np.diff(lrp))
+            # sorted, unique columns in every row
+            same_row = rid[1:] == rid[:-1]
+            assert np.all(c[1:][same_row] > c[:-1][same_row])
+            # C x = A (B x), all values nonnegative
+            y = np.bincount(rid, weights=v * x[c], minlength=re - rb)
+            a0, a1 = A.row_ptr[rb], A.row_ptr[re]
+            arid = np.repeat(np.arange(re - rb), np.diff(A.row_ptr[rb:re + 1]))
+            ref = np.bincount(arid, weights=A.val[a0:a1] * bx[A.col[a0:a1]], minlength=re - rb)
+            assert np.all(np.abs(y - ref) <= 1e-11 * ref + 1e-300)
+            rows = np.arange(rb, re)
+            small = rows[ip[rows] <= 2_000_000]
+            compare_rows(A, A, rp_h - rp_h[rb], c, v, small, threads=16)
+            checked += len(small)
+        assert checked > 10000
+    finally:
+        p.close()
+        release_device_memory()
