@@ -77,14 +77,15 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 256, 512])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
-    row, thousands of light rows in every ladder bin -- compared in full (multisplit path,
-    direct split, bulk-copy staged multisplit)."""
+    row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
+    full (multisplit path, plain shared atomics in the multisplit, dense chunks in L2, direct
+    split, bulk-copy staged multisplit)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
-    assert st.rows_heavy > 0 and st.rows_light > 0
+    assert st.rows_heavy > 0 and st.rows_light > 0 and st.dense_elems > 0
     compare_full(A, A, rp, col, val, threads=16)
 
 
