@@ -64,6 +64,9 @@ extern "C" {
                                          bulk copies (one 1024-thread block per SM, double
                                          buffered) instead of the register-tiled kernel (two
                                          512-thread blocks per SM); slower on the R-MAT cases */
+#define SPGEMM_FLAG_FUSED_HIST 1024    /* level-0 histogram counted per product inside the outer
+                                         product (warp match + global atomics) instead of from
+                                         per-B-row chunk counts summed over the rows of A */
 #define SPGEMM_FLAG_DIRECT_SPLIT 256  /* one-level plans: the outer product writes straight into
                                          C^_reord (counts from per-B-row chunk histograms), so C^
                                          is never stored and level 0 needs no multisplit pass */

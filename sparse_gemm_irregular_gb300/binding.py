@@ -27,6 +27,7 @@ FLAG_NO_MATCH = 64
 FLAG_DENSE_L2 = 128
 FLAG_DIRECT_SPLIT = 256
 FLAG_TMA_SPLIT = 512
+FLAG_FUSED_HIST = 1024
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",
           "light_numeric", "chunk_numeric", "chunk_dense"]

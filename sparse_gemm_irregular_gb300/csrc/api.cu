@@ -261,12 +261,29 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr, un
   int2* part;
   SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(hb.elems, kOpTile)));
   launch_partition(slice_off, kc, hb.elems, kOpTile, part, h->st);
+  const spgemm_plan& P = h->plan;
+  const int shift0 = ilog2_i64(P.chunk_width * P.chunks_required / P.v_chunks[0]);
+  const int64_t v0 = P.v_chunks[0];
+  unsigned long long* op_counts = counts0;
+  // (bounded memory: the per-B-row counts take k * v0 int32; beyond 8 GB count per product)
+  if (counts0 && !(h->opt.flags & SPGEMM_FLAG_FUSED_HIST) && kc * v0 <= (int64_t(1) << 31)) {
+    // Level-0 histogram by factorisation: the products of A[r, k] fall in the chunks that row k
+    // of B touches, so counts0[r, c] = sum over the entries (r, k) of (entries of B row k in
+    // chunk c).  Per-B-row chunk counts, then one coalesced read per entry of A: work in the
+    // entries of A and B instead of in the products.
+    PhaseTimer t(h, 4);
+    int32_t* bh;
+    SG_ALLOC(bh, int32_t, kc * v0);
+    cudaMemsetAsync(bh, 0, sizeof(int32_t) * kc * v0, h->st);
+    launch_b_chunk_hist(h->B, colcnt, shift0, v0, bh, h->d_err, h->st);
+    launch_row_chunk_counts(h->A, rows, R, bh, v0, counts0, h->st);
+    ws_free(h, bh);
+    op_counts = nullptr;
+  }
   {
     PhaseTimer t(h, 3);
-    const spgemm_plan& P = h->plan;
-    const int shift0 = ilog2_i64(P.chunk_width * P.chunks_required / P.v_chunks[0]);
     launch_outer_product(colptr, csc_row, csc_val, slice_off, part, hb.elems, h->B, cursor, h->d_chat_col,
-                         vals ? h->d_chat_val : nullptr, vals, counts0, shift0, P.v_chunks[0], h->d_err, h->st);
+                         vals ? h->d_chat_val : nullptr, vals, op_counts, shift0, v0, h->d_err, h->st);
   }
   ws_free(h, part);
   ws_free(h, colcnt);

@@ -313,24 +313,30 @@ void launch_b_chunk_hist(const spgemm_csr& B, const int32_t* colcnt, int shift, 
 }
 
 // counts[r * v + c] = sum over the entries A[row r, k] of bh[k * v + c]: the level-0 histogram of
-// C^ without forming C^.  One thread per (heavy row, chunk).
+// C^ without forming C^ (every product of A[r, k] with row k of B lands in the chunks that row k
+// of B touches).  One warp per heavy row, lane c for chunk c (chunks in groups of 32): the
+// counts of one entry are one coalesced read of bh.
 __global__ void k_row_chunk_counts(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
                                    const int32_t* __restrict__ rows, int64_t nrows, const int32_t* __restrict__ bh,
                                    int64_t v, unsigned long long* __restrict__ counts) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= nrows * v) return;
-  const int64_t r = t / v, c = t % v;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (r >= nrows) return;
   const int64_t row = rows[r];
-  unsigned long long sum = 0;
-  for (int64_t e = arp[row]; e < arp[row + 1]; ++e) sum += static_cast<unsigned long long>(bh[acol[e] * v + c]);
-  counts[t] = sum;
+  const int64_t e0 = arp[row], e1 = arp[row + 1];
+  for (int64_t c0 = 0; c0 < v; c0 += 32) {
+    const int64_t c = c0 + lane_id();
+    unsigned long long sum = 0;
+    if (c < v)
+      for (int64_t e = e0; e < e1; ++e) sum += static_cast<unsigned long long>(bh[static_cast<int64_t>(acol[e]) * v + c]);
+    if (c < v) counts[r * v + c] = sum;
+  }
 }
 void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int32_t* bh, int64_t v,
                              unsigned long long* counts, cudaStream_t s) {
   if (nrows == 0) return;
   note_launch();
-  k_row_chunk_counts<<<static_cast<unsigned>(ceil_div(nrows * v, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows,
-                                                                                     nrows, bh, v, counts);
+  k_row_chunk_counts<<<static_cast<unsigned>(ceil_div(nrows * 32, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows,
+                                                                                      nrows, bh, v, counts);
 }
 
 // Outer product writing straight into C^_reord: the same static partition as Algorithm 4, but each

@@ -50,6 +50,9 @@ FORCED = [
     # bulk-copy staged multisplit: two levels, and four levels with recompute batches
     dict(flags=512, tau=16, chunk_width=32, chunks_max=4),
     dict(flags=512 | 16, tau=8, chunk_width=32, chunks_max=2, heavy_batch_elems=700),
+    # level-0 histogram counted per product inside the outer product
+    dict(flags=1024, tau=16, chunk_width=32, chunks_max=4),
+    dict(flags=1024 | 16, tau=8, chunk_width=32, chunks_max=2, heavy_batch_elems=700),
 ]
 
 
@@ -77,12 +80,12 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
     row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
     full (multisplit path, plain shared atomics in the multisplit, dense chunks in L2, direct
-    split, bulk-copy staged multisplit)."""
+    split, bulk-copy staged multisplit, per-product level-0 histogram)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
     assert st.rows_heavy > 0 and st.rows_light > 0 and st.dense_elems > 0
