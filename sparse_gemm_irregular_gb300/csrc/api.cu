@@ -273,11 +273,16 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr, un
     // entries of A and B instead of in the products.
     PhaseTimer t(h, 4);
     int32_t* bh;
+    int64_t* hrp;
     SG_ALLOC(bh, int32_t, kc * v0);
+    SG_ALLOC(hrp, int64_t, R + 1);
     cudaMemsetAsync(bh, 0, sizeof(int32_t) * kc * v0, h->st);
     launch_b_chunk_hist(h->B, colcnt, shift0, v0, bh, h->d_err, h->st);
-    launch_row_chunk_counts(h->A, rows, R, bh, v0, counts0, h->st);
+    launch_heavy_row_len(h->A, rows, R, hrp, h->st);
+    SG_TRY(scan(h, hrp, hrp, R));
+    launch_row_chunk_counts(h->A, rows, R, hrp, nnzh, bh, v0, counts0, h->st);
     ws_free(h, bh);
+    ws_free(h, hrp);
     op_counts = nullptr;
   }
   {
@@ -517,9 +522,15 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   SG_ALLOC(rptr, int64_t, nout + 1);
   SG_ALLOC(out_row, int32_t, nout);
   SG_ALLOC(out_base, int32_t, nout);
+  int64_t* hrp;
+  SG_ALLOC(hrp, int64_t, R + 1);
   cudaMemsetAsync(bh, 0, sizeof(int32_t) * kc * v, h->st);
+  cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
   launch_b_chunk_hist(h->B, colcnt, shift, v, bh, h->d_err, h->st);
-  launch_row_chunk_counts(h->A, rows, R, bh, v, counts, h->st);
+  launch_heavy_row_len(h->A, rows, R, hrp, h->st);
+  SG_TRY(scan(h, hrp, hrp, R));
+  launch_row_chunk_counts(h->A, rows, R, hrp, nnzh, bh, v, counts, h->st);
+  ws_free(h, hrp);
   launch_reord_meta(counts, R, v, nullptr, nullptr, nullptr, width, rptr, out_row, out_base, h->st);
   SG_TRY(scan(h, rptr, rptr, nout));
   launch_copy_i64(rptr, cursor, nout, h->st);

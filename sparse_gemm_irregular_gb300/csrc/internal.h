@@ -125,8 +125,13 @@ void launch_gather_rows(const int32_t* src, int32_t* io, int64_t n, cudaStream_t
 void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t tile, int2* part, cudaStream_t s);
 void launch_b_chunk_hist(const spgemm_csr& B, const int32_t* colcnt, int shift, int64_t v, int32_t* bh, uint32_t* err,
                          cudaStream_t s);
-void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int32_t* bh, int64_t v,
-                             unsigned long long* counts, cudaStream_t s);
+// counts[r * v + c] = sum of bh[k * v + c] over the entries (r, k) of the heavy rows; hrp is the
+// prefix of the heavy rows' lengths (launch_heavy_row_len + scan), entries = hrp[nrows]; counts
+// must be zeroed.
+void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int64_t* hrp,
+                             int64_t entries, const int32_t* bh, int64_t v, unsigned long long* counts,
+                             cudaStream_t s);
+void launch_heavy_row_len(const spgemm_csr& A, const int32_t* rows, int64_t nrows, int64_t* len, cudaStream_t s);
 void launch_outer_direct(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
                          const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
                          const int32_t* xmap, unsigned long long* cursor, int32_t* out_col, double* out_val,

@@ -314,29 +314,57 @@ void launch_b_chunk_hist(const spgemm_csr& B, const int32_t* colcnt, int shift, 
 
 // counts[r * v + c] = sum over the entries A[row r, k] of bh[k * v + c]: the level-0 histogram of
 // C^ without forming C^ (every product of A[r, k] with row k of B lands in the chunks that row k
-// of B touches).  One warp per heavy row, lane c for chunk c (chunks in groups of 32): the
-// counts of one entry are one coalesced read of bh.
+// of B touches) -- a sparse (heavy rows of A) times dense (k x v) product.  The entries of the
+// heavy rows, in row order (prefix hrp), are split evenly over warps, so the longest rows of a
+// power-law A do not serialise on one warp.  Lane c of a warp sums chunk c (chunks in groups of
+// 32) while the row stays the same and adds the partial sum to the counter when it changes.
+__global__ void k_heavy_row_len(const int64_t* __restrict__ arp, const int32_t* __restrict__ rows, int64_t nrows,
+                                int64_t* __restrict__ len) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r < nrows) len[r] = arp[rows[r] + 1] - arp[rows[r]];
+}
+
+constexpr int64_t kCountRun = 256;  // entries per warp
+
 __global__ void k_row_chunk_counts(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
-                                   const int32_t* __restrict__ rows, int64_t nrows, const int32_t* __restrict__ bh,
-                                   int64_t v, unsigned long long* __restrict__ counts) {
-  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (r >= nrows) return;
-  const int64_t row = rows[r];
-  const int64_t e0 = arp[row], e1 = arp[row + 1];
+                                   const int32_t* __restrict__ rows, int64_t nrows, const int64_t* __restrict__ hrp,
+                                   const int32_t* __restrict__ bh, int64_t v, unsigned long long* __restrict__ counts) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t total = hrp[nrows];
+  const int64_t x0 = w * kCountRun;
+  if (x0 >= total) return;
+  const int64_t x1 = min(total, x0 + kCountRun);
+  const int64_t r0 = upper_bound_minus1(hrp, int64_t(0), nrows + 1, x0);  // row holding entry x0
   for (int64_t c0 = 0; c0 < v; c0 += 32) {
     const int64_t c = c0 + lane_id();
+    int64_t r = r0;
+    int64_t e = arp[rows[r]] + (x0 - hrp[r]);
     unsigned long long sum = 0;
-    if (c < v)
-      for (int64_t e = e0; e < e1; ++e) sum += static_cast<unsigned long long>(bh[static_cast<int64_t>(acol[e]) * v + c]);
-    if (c < v) counts[r * v + c] = sum;
+    for (int64_t x = x0; x < x1; ++x, ++e) {
+      while (x >= hrp[r + 1]) {  // row change: flush the partial sum of row r
+        if (sum && c < v) atomicAdd(&counts[r * v + c], sum);
+        sum = 0;
+        ++r;
+        e = arp[rows[r]];
+      }
+      if (c < v) sum += static_cast<unsigned long long>(__ldg(&bh[static_cast<int64_t>(__ldg(&acol[e])) * v + c]));
+    }
+    if (sum && c < v) atomicAdd(&counts[r * v + c], sum);
   }
 }
-void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int32_t* bh, int64_t v,
-                             unsigned long long* counts, cudaStream_t s) {
+void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t nrows, const int64_t* hrp,
+                             int64_t entries, const int32_t* bh, int64_t v, unsigned long long* counts,
+                             cudaStream_t s) {
+  if (nrows == 0 || entries == 0) return;
+  note_launch();
+  const int64_t warps = ceil_div(entries, kCountRun);
+  k_row_chunk_counts<<<static_cast<unsigned>(ceil_div(warps * 32, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows,
+                                                                                      nrows, hrp, bh, v, counts);
+}
+void launch_heavy_row_len(const spgemm_csr& A, const int32_t* rows, int64_t nrows, int64_t* len, cudaStream_t s) {
   if (nrows == 0) return;
   note_launch();
-  k_row_chunk_counts<<<static_cast<unsigned>(ceil_div(nrows * 32, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows,
-                                                                                      nrows, bh, v, counts);
+  k_heavy_row_len<<<static_cast<unsigned>(ceil_div(nrows, 256)), 256, 0, s>>>(A.row_ptr, rows, nrows, len);
 }
 
 // Outer product writing straight into C^_reord: the same static partition as Algorithm 4, but each
