@@ -51,7 +51,8 @@ extern "C" {
 
 /* ---- option flags (spgemm_options.flags) ------------------------------------------ */
 #define SPGEMM_FLAG_ALL_HEAVY 1       /* route every non-empty row through the heavy path   */
-#define SPGEMM_FLAG_ALL_LIGHT 2       /* route every row through the light path (needs IP <= tau) */
+#define SPGEMM_FLAG_ALL_LIGHT 2       /* keep every row with IP <= tau light even when ALL_HEAVY is
+                                         set; rows above tau are always heavy (no light table fits) */
 #define SPGEMM_FLAG_NO_DENSE_LIGHT 4  /* light rows never use the shortened dense accumulator */
 #define SPGEMM_FLAG_VALIDATE 8        /* check A and B (row_ptr monotone, columns in range)  */
 #define SPGEMM_FLAG_RECOMPUTE 16      /* never keep C^_reord between symbolic and numeric    */

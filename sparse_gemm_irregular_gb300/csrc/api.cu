@@ -914,6 +914,12 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
     return fail(rc);
   }
   h->lad = make_ladder(h->plan.tau);
+  // the largest light bin's hash table must fit one block's shared memory (this also keeps the
+  // products of a light row, at most tau, far below 2^31)
+  if (light_smem_bytes(h->lad.slots[h->lad.n - 1], h->lad.tpr[h->lad.n - 1], false, true) > static_cast<size_t>(optin)) {
+    set_last_error("tau too large: the light-row hash table does not fit in shared memory");
+    return fail(SPGEMM_ERR_INVALID_ARG);
+  }
   h->rule.n = h->lad.n;
   for (int i = 0; i < h->lad.n; ++i) {
     h->rule.upper[i] = h->lad.upper[i];

@@ -60,11 +60,24 @@ __device__ __forceinline__ int64_t group_scan(const Group<WARP>& g, int64_t v, i
   }
 }
 
+// 32-bit variant (tmp reinterpreted as 33 int32).
+template <bool WARP>
+__device__ __forceinline__ int group_scan_i32(const Group<WARP>& g, int v, int64_t* tmp, int* total) {
+  if (WARP) {
+    const int x = warp_incl_scan(v);
+    *total = __shfl_sync(0xffffffffu, x, 31);
+    return x;
+  } else {
+    return block_incl_scan(v, reinterpret_cast<int*>(tmp), total);
+  }
+}
+
 // Shared-memory layout of one group.
 struct Smem {
   double* av;        // [batch] A values of the staged entries
   int64_t* bstart;   // [batch] first B index of the staged entries
-  int64_t* incl;     // [batch] inclusive prefix of their B row lengths
+  int32_t* incl;     // [batch] inclusive prefix of their B row lengths (a light row has at most
+                     //         tau products, far below 2^31)
   int64_t* tmp;      // [33] scan scratch
   double* vals;      // [slots] (numeric)
   int32_t* keys;     // [slots] hash keys, or dense bitmap words
@@ -77,7 +90,7 @@ __host__ __device__ inline int batch_of(int size) { return size < kMaxBatch ? si
 __host__ __device__ inline size_t group_bytes(int64_t slots, int size, bool dense, bool numeric,
                                               bool rows) {
   size_t b = align16(33 * sizeof(int64_t));
-  if (rows) b += align16(batch_of(size) * (sizeof(double) + 2 * sizeof(int64_t)));
+  if (rows) b += align16(batch_of(size) * (sizeof(double) + sizeof(int64_t) + sizeof(int32_t)));
   if (numeric) b += align16(static_cast<size_t>(slots) * sizeof(double));
   b += dense ? align16(((slots + 31) / 32) * sizeof(int32_t))
              : align16(static_cast<size_t>(slots) * sizeof(int32_t));
@@ -93,8 +106,8 @@ __device__ __forceinline__ Smem carve(char* p, int64_t slots, int size, bool den
     const int nb = batch_of(size);
     s.av = reinterpret_cast<double*>(p);
     s.bstart = reinterpret_cast<int64_t*>(p + nb * sizeof(double));
-    s.incl = reinterpret_cast<int64_t*>(p + nb * (sizeof(double) + sizeof(int64_t)));
-    p += align16(nb * (sizeof(double) + 2 * sizeof(int64_t)));
+    s.incl = reinterpret_cast<int32_t*>(p + nb * (sizeof(double) + sizeof(int64_t)));
+    p += align16(nb * (sizeof(double) + sizeof(int64_t) + sizeof(int32_t)));
   } else {
     s.av = nullptr;
     s.bstart = nullptr;
@@ -172,28 +185,28 @@ __device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& 
   const int nb = batch_of(g.size);
   for (int64_t eb = a0; eb < a1; eb += nb) {
     const int nent = static_cast<int>(min(static_cast<int64_t>(nb), a1 - eb));
-    int64_t len = 0;
+    int len = 0;
     if (g.lane < nent) {
       const int64_t e = eb + g.lane;
       const int32_t k = p.acol[e];
       const int64_t b0 = p.brp[k];
-      len = p.brp[k + 1] - b0;
+      len = static_cast<int>(p.brp[k + 1] - b0);
       s.av[g.lane] = NUMERIC ? p.aval[e] : 0.0;
       s.bstart[g.lane] = b0;
     }
-    int64_t total;
-    const int64_t incl = group_scan<WARP>(g, g.lane < nb ? len : 0, s.tmp, &total);
+    int total;
+    const int incl = group_scan_i32<WARP>(g, g.lane < nb ? len : 0, s.tmp, &total);
     if (g.lane < nent) s.incl[g.lane] = incl;
     g.sync();
     int j = 0;
     // kExpandUnroll products per thread per step: their B loads are all issued before the
     // first accumulator update, so each thread keeps several L2 requests in flight
-    for (int64_t f0 = g.lane; f0 < total; f0 += kExpandUnroll * g.size) {
+    for (int f0 = g.lane; f0 < total; f0 += kExpandUnroll * g.size) {
       int32_t col[kExpandUnroll];
       double bv[kExpandUnroll], av[kExpandUnroll];
 #pragma unroll
       for (int u = 0; u < kExpandUnroll; ++u) {
-        const int64_t f = f0 + static_cast<int64_t>(u) * g.size;
+        const int f = f0 + u * g.size;
         col[u] = kEmptyKey;
         if (f < total) {
           // staged entry j holds flattened positions [incl[j-1], incl[j])
@@ -205,7 +218,7 @@ __device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& 
             }
             j = lo;
           }
-          const int64_t before = j > 0 ? s.incl[j - 1] : 0;
+          const int before = j > 0 ? s.incl[j - 1] : 0;
           const int64_t q = s.bstart[j] + (f - before);
           col[u] = p.bcol[q];
           if (NUMERIC) {

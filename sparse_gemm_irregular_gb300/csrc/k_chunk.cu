@@ -212,15 +212,21 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
   if (MODE != 1) g.sync();
   const int32_t* col = p.cs.col + start;
   const double* val = p.cs.val + start;
+  // element offsets inside a chunk are 32-bit (a chunk of 2^31 or more elements is rejected)
+  if (cnt > 0x7fffffffLL) {
+    if (g.lane == 0) set_error(p.err, kErrBounds);
+    return;
+  }
+  const int n32 = static_cast<int>(cnt);
 
   if (MODE == 0) {
     constexpr int U = 8;
-    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
+    for (int f0 = 0; f0 < n32; f0 += g.size * U) {
       uint32_t cr[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
-        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
-        cr[j] = f < cnt ? static_cast<uint32_t>(__ldcs(col + f)) : 0xffffffffu;
+        const int f = f0 + j * g.size + g.lane;
+        cr[j] = f < n32 ? static_cast<uint32_t>(__ldcs(col + f)) : 0xffffffffu;
       }
 #pragma unroll
       for (int j = 0; j < U; ++j) {
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
     }
     g.sync();
     int64_t n = 0;
-    for (int64_t w = g.lane; w < words; w += g.size) n += __popc(s.bits[w]);
+    for (int w = g.lane; w < static_cast<int>(words); w += g.size) n += __popc(s.bits[w]);
     int64_t tot;
     ck_scan<WARP>(g, n, s.tmp, &tot);
     if (g.lane == 0) p.cs.nnz[q] = tot;
@@ -250,15 +256,15 @@ __global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
     for (uint32_t j = g.lane; j < slots; j += g.size) s.vals[j] = 0.0;
     g.sync();
     constexpr int U = 4;
-    for (int64_t f0 = 0; f0 < cnt; f0 += static_cast<int64_t>(g.size) * U) {
+    for (int f0 = 0; f0 < n32; f0 += g.size * U) {
       int32_t cr[U];
       double vr[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
-        const int64_t f = f0 + static_cast<int64_t>(j) * g.size + g.lane;
+        const int f = f0 + j * g.size + g.lane;
         cr[j] = -1;
         vr[j] = 0.0;
-        if (f < cnt) {
+        if (f < n32) {
           cr[j] = __ldcs(col + f);
           vr[j] = __ldcs(val + f);
         }
@@ -334,6 +340,11 @@ __device__ __forceinline__ void dense_fetch(const CkParams& p, int* next, DenseJ
   }
   j->start = p.cs.start[q];
   j->cnt = p.cs.cnt[q];
+  if (j->cnt > 0x7fffffffLL) {  // element offsets inside a chunk are 32-bit
+    set_error(p.err, kErrBounds);
+    j->state = 2;
+    return;
+  }
   j->out = p.sink.row_ptr[grow] + p.cs.out[q] - p.sink.row_ptr[p.sink.row_begin];
   j->expected = p.cs.nnz[q];
   j->base = p.cs.base[q];
@@ -371,23 +382,33 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
     else jobs[1].state = 0;
   }
   __syncthreads();
-  // streaming registers: batch b of the current chunk is loaded while batch b-1 is added
+  // streaming registers: batch b of the current chunk is loaded while batch b-1 is added.  A
+  // chunk is a base pointer pair and a 32-bit count held in registers, so the per-element work
+  // is 32-bit offset arithmetic (no rereads of the shared descriptors).
   constexpr int U = 4;
   int32_t cr[U];
   double vr[U];
-  auto load_batch = [&](const DenseJob& jb, int64_t f0) {
+  auto load_batch = [&](const int32_t* bc, const double* bv, int n, int f0) {
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      const int64_t f = f0 + static_cast<int64_t>(j) * nt + t;
+      const int f = f0 + j * nt + t;
       cr[j] = -1;
-      vr[j] = 0.0;
-      if (jb.state == 1 && f < jb.cnt) {
-        cr[j] = __ldcs(p.cs.col + jb.start + f);
-        vr[j] = __ldcs(p.cs.val + jb.start + f);
+      if (f < n) {
+        cr[j] = __ldcs(bc + f);
+        vr[j] = __ldcs(bv + f);
       }
     }
   };
-  if (warp > 0) load_batch(jobs[0], 0);
+  auto chunk_of = [&](const DenseJob& jb, const int32_t*& bc, const double*& bv, int& n) {
+    n = jb.state == 1 ? static_cast<int>(jb.cnt) : 0;
+    bc = p.cs.col + (jb.state == 1 ? jb.start : 0);
+    bv = p.cs.val + (jb.state == 1 ? jb.start : 0);
+  };
+  const int32_t* ccol;
+  const double* cval;
+  int ccnt;
+  chunk_of(jobs[0], ccol, cval, ccnt);
+  if (warp > 0) load_batch(ccol, cval, ccnt, 0);
   for (int it = 0;; ++it) {
     const DenseJob job = jobs[it % 3];
     if (job.state == 0) break;
@@ -398,10 +419,12 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
         else jobs[(it + 2) % 3].state = 0;
       }
     } else {
-      const DenseJob nxt = jobs[(it + 1) % 3];
-      const int64_t step = static_cast<int64_t>(nt) * U;
-      const int64_t cnt = job.state == 1 ? job.cnt : 0;
-      for (int64_t f0 = 0; f0 < (cnt > 0 ? cnt : 1); f0 += step) {
+      const int32_t* ncol;
+      const double* nval;
+      int ncnt;
+      chunk_of(jobs[(it + 1) % 3], ncol, nval, ncnt);
+      const int step = nt * U;
+      for (int f0 = 0; f0 < (ccnt > 0 ? ccnt : 1); f0 += step) {
         int32_t c2[U];
         double v2[U];
 #pragma unroll
@@ -410,8 +433,8 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
           v2[j] = vr[j];
         }
         // next batch of this chunk, or the first batch of the next chunk
-        if (f0 + step < cnt) load_batch(job, f0 + step);
-        else load_batch(nxt, 0);
+        if (f0 + step < ccnt) load_batch(ccol, cval, ccnt, f0 + step);
+        else load_batch(ncol, nval, ncnt, 0);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
           const int32_t c = c2[j];
@@ -430,6 +453,9 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
           }
         }
       }
+      ccol = ncol;
+      cval = nval;
+      ccnt = ncnt;
     }
     if (L2) __threadfence_block();
     __syncthreads();

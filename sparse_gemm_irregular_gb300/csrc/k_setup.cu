@@ -61,7 +61,8 @@ void launch_brow_minmax(const spgemm_csr& B, int32_t* bmin, int32_t* bmax, cudaS
 // ---- IP per row, span, bin ---------------------------------------------------------------
 __device__ __forceinline__ uint8_t classify_row(int64_t ip, int64_t span, const BinRule& r) {
   if (ip == 0) return kBinEmpty;
-  if (!r.all_light && (r.all_heavy || ip > r.tau)) return static_cast<uint8_t>(2 * r.n);
+  // rows above tau cannot fit a light table: heavy even when all_light is set
+  if (ip > r.tau || (r.all_heavy && !r.all_light)) return static_cast<uint8_t>(2 * r.n);
   int L = 0;
   while (L < r.n - 1 && ip > r.upper[L]) ++L;
   const bool dense = !r.no_dense && span <= r.slots[L];
