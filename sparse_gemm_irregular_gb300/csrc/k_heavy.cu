@@ -233,12 +233,33 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     e = lo;
   }
   if (!HIST) {
-    for (; p < n; p += blockDim.x) {
-      while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
-      const int64_t src = src_delta[e] + p;
-      const int64_t dst = dst_delta[e] + p;
-      out_col[dst] = bcol[src];
-      if (VALS) out_val[dst] = __ldg(&cval[a_first + e]) * bval[src];
+    // kOpUnroll elements per thread per step: all their gathers are issued before the stores
+    constexpr int kOpUnroll = 4;
+    for (; p < n; p += kOpUnroll * blockDim.x) {
+      int64_t dst[kOpUnroll];
+      int32_t c[kOpUnroll];
+      double a[kOpUnroll], b[kOpUnroll];
+#pragma unroll
+      for (int u = 0; u < kOpUnroll; ++u) {
+        const int32_t q = p + u * static_cast<int32_t>(blockDim.x);
+        dst[u] = -1;
+        if (q < n) {
+          while (e + 1 < nent && seg_start[e + 1] <= q) ++e;
+          const int64_t src = src_delta[e] + q;
+          dst[u] = dst_delta[e] + q;
+          c[u] = bcol[src];
+          if (VALS) {
+            a[u] = __ldg(&cval[a_first + e]);
+            b[u] = bval[src];
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kOpUnroll; ++u) {
+        if (dst[u] < 0) continue;
+        out_col[dst[u]] = c[u];
+        if (VALS) out_val[dst[u]] = a[u] * b[u];
+      }
     }
     return;
   }
