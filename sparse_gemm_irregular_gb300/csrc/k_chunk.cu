@@ -484,18 +484,38 @@ __global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, 
       const int64_t n_out = total < job.expected ? total : job.expected;
       int32_t* c_col = p.sink.c_col + job.out;
       double* c_val = p.sink.c_val + job.out;
-      for (int64_t k = g.lane; k < total; k += g.size) {
-        int lo = 0, hi = static_cast<int>(words) - 1;
-        while (lo < hi) {  // last word whose prefix is <= k: it holds bit number k
-          const int mid = (lo + hi + 1) >> 1;
-          if (s.pre[mid] <= k) lo = mid; else hi = mid - 1;
+      // four output positions per thread per step, their binary searches (last word whose
+      // prefix is <= k: it holds bit number k) run in lockstep so the shared loads overlap
+      int steps = 0;
+      while ((int64_t(1) << steps) < words) ++steps;
+      const int nw = static_cast<int>(words);
+      for (int k0 = g.lane; k0 < static_cast<int>(total); k0 += 4 * g.size) {
+        int lo[4], hi[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          lo[u] = 0;
+          hi[u] = k0 + u * g.size < static_cast<int>(total) ? nw - 1 : 0;
         }
-        const int32_t idx = lo * 32 + nth_set_bit(s.bits[lo], static_cast<int>(k - s.pre[lo]));
-        if (k < n_out) {
-          c_col[k] = idx + job.base;
-          c_val[k] = L2 ? __ldcg(&acc[idx]) : acc[idx];
+        for (int st = 0; st < steps; ++st) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (lo[u] < hi[u]) {
+              const int mid = (lo[u] + hi[u] + 1) >> 1;
+              if (s.pre[mid] <= k0 + u * g.size) lo[u] = mid; else hi[u] = mid - 1;
+            }
+          }
         }
-        if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = k0 + u * g.size;
+          if (k >= static_cast<int>(total)) continue;
+          const int32_t idx = lo[u] * 32 + nth_set_bit(s.bits[lo[u]], k - s.pre[lo[u]]);
+          if (k < n_out) {
+            c_col[k] = idx + job.base;
+            c_val[k] = L2 ? __ldcg(&acc[idx]) : acc[idx];
+          }
+          if (L2) __stcg(&acc[idx], 0.0); else acc[idx] = 0.0;  // leave the array zeroed
+        }
       }
       __syncthreads();
       for (int64_t w = g.lane; w < words; w += g.size) s.bits[w] = 0u;
