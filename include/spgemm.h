@@ -62,10 +62,9 @@ extern "C" {
 #define SPGEMM_FLAG_DENSE_L2 128      /* heavy dense chunks sum with L2 reductions into a global
                                          per-SM array instead of shared-memory atomics */
 #define SPGEMM_FLAG_TMA_SPLIT 512     /* multisplit: tiles of C^ staged in shared memory by
-                                         bulk copies (one 1024-thread block per SM, double
-                                         buffered) instead of the register-tiled kernel (two
-                                         512-thread blocks per SM); slower on the R-MAT cases */
-#define SPGEMM_FLAG_FUSED_HIST 1024    /* level-0 histogram counted per product inside the outer
+                                         bulk copies (two stages per block) instead of held in
+                                         registers; slower on the R-MAT cases */
+#define SPGEMM_FLAG_FUSED_HIST 1024   /* level-0 histogram counted per product inside the outer
                                          product (warp match + global atomics) instead of from
                                          per-B-row chunk counts summed over the rows of A */
 #define SPGEMM_FLAG_DIRECT_SPLIT 256  /* one-level plans: the outer product writes straight into

@@ -1,14 +1,16 @@
 // C ABI and orchestration of the gMAGNUS pipeline (gMAGNUS page, Algorithm 3).
 //
 //   create    : planner, IP per row + bins (light ladder / heavy), one synchronisation.
-//   symbolic  : light rows (hash / shortened dense symbolic), heavy batches (CSC -> outer
-//               product -> levels of histogram + partition + multisplit -> chunk symbolic),
-//               scan of C.row_ptr, one synchronisation for nnz(C).
-//   numeric   : light rows (accumulate + sort + write), heavy batches (chunk accumulate +
-//               sorted write at the final positions).  The expansion is kept from symbolic
+//   symbolic  : light rows (hash / shortened dense symbolic), heavy batches (CSC -> level-0
+//               histogram from per-B-row chunk counts -> outer product -> levels of histogram +
+//               partition + multisplit -> chunk symbolic), scan of C.row_ptr, one
+//               synchronisation for nnz(C).
+//   numeric   : light rows (accumulate + ordered write), heavy batches (chunk accumulate +
+//               ordered write at the final positions).  The expansion is kept from symbolic
 //               to numeric when the whole heavy part fits one batch ("resident"), otherwise
 //               it is recomputed batch by batch (the device cannot hold C^ of every heavy row
-//               of the largest products).
+//               of the largest products).  numeric_rows computes a row window;
+//               numeric_host streams row windows into host memory.
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
