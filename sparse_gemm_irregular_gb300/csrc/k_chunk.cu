@@ -30,17 +30,15 @@ constexpr int kHubBits = 16;
 constexpr int kHubSlots = 1 + kHubBits + kHubBits * (kHubBits - 1) / 2;  // 137
 static_assert(kHubSlots == kChunkHubSlots, "hub slot count");
 
+// Branch-free (lanes of a warp that hit hubs and lanes that do not take the same path):
+// 0 for column 0, 1 + i for 2^i, 1 + kHubBits + j(j-1)/2 + i for 2^i + 2^j (i < j), else -1.
 __device__ __forceinline__ int hub_index(uint32_t c) {
-  if (c >= (1u << kHubBits)) return -1;
   const int pc = __popc(c);
-  if (pc == 0) return 0;
-  if (pc == 1) return 1 + (__ffs(c) - 1);
-  if (pc == 2) {
-    const int i = __ffs(c) - 1;
-    const int j = 31 - __clz(c);
-    return 1 + kHubBits + j * (j - 1) / 2 + i;
-  }
-  return -1;
+  const int i = __ffs(c) - 1;      // lowest set bit (-1 for c = 0)
+  const int j = 31 - __clz(c);     // highest set bit
+  const int two = 1 + kHubBits + ((j * (j - 1)) >> 1) + i;
+  const int idx = pc == 0 ? 0 : (pc == 1 ? 1 + i : two);
+  return (pc <= 2 && c < (1u << kHubBits)) ? idx : -1;
 }
 
 __host__ __device__ inline uint32_t hub_column(int idx) {
