@@ -70,6 +70,7 @@ extern "C" {
 #define SPGEMM_FLAG_DIRECT_SPLIT 256  /* one-level plans: the outer product writes straight into
                                          C^_reord (counts from per-B-row chunk histograms), so C^
                                          is never stored and level 0 needs no multisplit pass */
+#define SPGEMM_FLAG_NO_GRAPH 2048    /* never capture or replay the numeric phase as a CUDA graph */
 
 /* A CSR matrix in device memory, borrowed by the library (never written or freed). */
 typedef struct {
@@ -126,7 +127,7 @@ typedef struct {
   int64_t dense_elems;       /* C^_reord elements summed on the dense accumulator       */
   int64_t dense_nnz;         /* entries of C those dense chunks produce                 */
   int32_t resident;          /* 1: C^_reord kept from symbolic to numeric               */
-  int32_t reserved;
+  int32_t numeric_graph;     /* 1: the last numeric call replayed a captured CUDA graph */
 } spgemm_stats;
 
 typedef struct spgemm_ctx* spgemm_handle;
@@ -156,7 +157,12 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz);
 
 /* Numeric phase: writes C.col_idx (device, c_nnz int32) and C.vals (device, c_nnz fp64),
  * caller-owned, each row sorted by column, at the positions of the row_ptr from
- * spgemm_symbolic (which must still hold those values).  May be called more than once. */
+ * spgemm_symbolic (which must still hold those values).  May be called more than once.  When
+ * no C^_reord is kept from symbolic (stats.resident == 0: no heavy row, or SPGEMM_FLAG_RECOMPUTE)
+ * every call reads the current values of A and B, so their values (never their structure) may
+ * change between calls.  A call repeating the previous one's arguments is captured into a CUDA
+ * graph, and later repeats replay it (stats.numeric_graph), when the phase needs no host
+ * synchronisation: no heavy row, or C^_reord resident.  SPGEMM_FLAG_NO_GRAPH turns this off. */
 int spgemm_numeric(spgemm_handle h, int32_t* c_col_idx, double* c_vals);
 
 /* Numeric phase for rows [row_begin, row_end) only, written at offset 0 = row_ptr[row_begin]

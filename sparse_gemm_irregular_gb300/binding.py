@@ -28,6 +28,7 @@ FLAG_DENSE_L2 = 128
 FLAG_DIRECT_SPLIT = 256
 FLAG_TMA_SPLIT = 512
 FLAG_FUSED_HIST = 1024
+FLAG_NO_GRAPH = 2048
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",
           "light_numeric", "chunk_numeric", "chunk_dense"]
@@ -62,7 +63,7 @@ class spgemm_stats(ctypes.Structure):
                 ("rows_dense_light", _i64), ("c_nnz", _i64), ("heavy_batches", _i64),
                 ("levels_run", _i64), ("final_chunks", _i64), ("chunks_dense", _i64),
                 ("chat_bytes", _i64), ("c_nnz_heavy", _i64), ("dense_elems", _i64), ("dense_nnz", _i64),
-                ("resident", _i32), ("reserved", _i32)]
+                ("resident", _i32), ("numeric_graph", _i32)]
 
 
 EXPORTS = {

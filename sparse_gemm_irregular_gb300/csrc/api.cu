@@ -69,6 +69,7 @@ cudaMemPool_t device_pool(int dev) {
 
 void* ws_alloc(spgemm_ctx* h, size_t bytes) {
   void* p = nullptr;
+  if (h->capturing) return nullptr;  // a captured phase must not allocate: the capture is dropped
   if (bytes == 0) bytes = 16;
   if (cudaMallocFromPoolAsync(&p, bytes, h->pool, h->st) != cudaSuccess) {
     cudaGetLastError();
@@ -806,10 +807,86 @@ int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, doubl
   return SPGEMM_OK;
 }
 
+void drop_numeric_graph(spgemm_ctx* h) {
+  if (h->num_exec) cudaGraphExecDestroy(h->num_exec);
+  h->num_exec = nullptr;
+  h->num_launches = 0;
+}
+
+// Capture the numeric phase of rows [rb, re) into h->num_exec; false (nothing enqueued, the
+// stream out of capture) when the capture fails, so the caller runs the phase eagerly.
+// The legacy default stream cannot be captured, so the phase is enqueued on a private
+// non-blocking stream while the capture is open; the graph is then launched on the caller's.
+bool capture_numeric(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
+  if (!h->st_graph && cudaStreamCreateWithFlags(&h->st_graph, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    h->st_graph = nullptr;
+    return false;
+  }
+  if (cudaStreamBeginCapture(h->st_graph, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const long long before = launch_count();
+  cudaStream_t caller = h->st;
+  h->st = h->st_graph;
+  h->capturing = true;
+  const int rc = numeric_enqueue(h, rb, re, c_col, c_val);
+  h->capturing = false;
+  if (rc != SPGEMM_OK) join_light(h);  // keep the light stream joined; the capture is dropped
+  h->st = caller;
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(h->st_graph, &g);
+  const long long launched = launch_count() - before;
+  g_launches.fetch_sub(launched, std::memory_order_relaxed);  // counted again at each replay
+  cudaGraphExec_t ex = nullptr;
+  const bool ok = rc == SPGEMM_OK && e == cudaSuccess && g &&
+                  cudaGraphInstantiate(&ex, g, 0) == cudaSuccess;
+  if (g) cudaGraphDestroy(g);
+  if (!ok) {
+    if (ex) cudaGraphExecDestroy(ex);
+    cudaGetLastError();
+    // the phase then runs eagerly; the reason stays readable through spgemm_last_error
+    set_last_error(std::string("numeric graph capture dropped (ran eagerly): ") +
+                   (rc != SPGEMM_OK ? "phase failed under capture" : cudaGetErrorString(e)));
+    return false;
+  }
+  h->num_exec = ex;
+  h->num_launches = launched;
+  return true;
+}
+
+// Numeric phase of rows [rb, re), synchronised.  A repeated call (same rows, same output
+// arrays) is captured once into a CUDA graph and replayed from then on, when the phase needs no
+// host synchronisation and no allocation: no heavy batch, or the one batch's C^_reord kept from
+// the symbolic phase.  Replays cut the launch cost that dominates small products.
 int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
   if (h->state < 2) {
     set_last_error("numeric called before symbolic");
     return SPGEMM_ERR_BAD_STATE;
+  }
+  h->last_graph = false;
+  const bool graphable = !h->timing && !(h->opt.flags & SPGEMM_FLAG_NO_GRAPH) &&
+                         (h->batches.empty() || h->resident);
+  if (graphable) {
+    SG_TRY(numeric_bins(h));  // its one synchronisation stays outside any capture
+    const bool same = rb == h->num_rb && re == h->num_re && c_col == h->num_col && c_val == h->num_val;
+    if (!same) {
+      drop_numeric_graph(h);
+      h->num_rb = rb;
+      h->num_re = re;
+      h->num_col = c_col;
+      h->num_val = c_val;
+      h->num_calls = 0;
+    }
+    if (!h->num_exec && h->num_calls >= 1) capture_numeric(h, rb, re, c_col, c_val);
+    if (h->num_exec) {
+      SG_TRY(check_cuda(cudaGraphLaunch(h->num_exec, h->st), "numeric graph launch"));
+      g_launches.fetch_add(h->num_launches, std::memory_order_relaxed);
+      h->last_graph = true;
+      return sync_and_check(h, "numeric");
+    }
+    ++h->num_calls;
   }
   SG_TRY(numeric_enqueue(h, rb, re, c_col, c_val));
   return sync_and_check(h, "numeric");
@@ -1224,6 +1301,7 @@ int spgemm_numeric_host(spgemm_handle h, int64_t* c_row_ptr, int32_t* c_col_idx,
 int spgemm_get_stats(spgemm_handle h, spgemm_stats* out) {
   if (!h || !out) return SPGEMM_ERR_INVALID_ARG;
   *out = h->stats;
+  out->numeric_graph = h->last_graph ? 1 : 0;
   return SPGEMM_OK;
 }
 
@@ -1249,6 +1327,8 @@ int spgemm_destroy(spgemm_handle h) {
   if (!h) return SPGEMM_OK;
   drain_timers(h);
   if (h->st_light) cudaStreamSynchronize(h->st_light);
+  drop_numeric_graph(h);
+  if (h->st_graph) cudaStreamDestroy(h->st_graph);
   for (void* p : h->allocs) cudaFreeAsync(p, h->st);
   h->allocs.clear();
   cudaStreamSynchronize(h->st);

@@ -265,6 +265,18 @@ struct spgemm_ctx {
 
   // phase timing (slots: see spgemm_get_phase_times)
   bool timing = false;
+
+  // numeric phase replayed from a CUDA graph: captured on the second call with the same row
+  // range and output arrays, when that phase enqueues no host synchronisation and no allocation
+  cudaGraphExec_t num_exec = nullptr;
+  cudaStream_t st_graph = nullptr;  // capture stream (the caller's may be the legacy default stream)
+  int64_t num_rb = -1, num_re = -1;
+  int32_t* num_col = nullptr;
+  double* num_val = nullptr;
+  int num_calls = 0;           // eager calls with the current key
+  long long num_launches = 0;  // kernel launches the graph holds
+  bool capturing = false;      // ws_alloc refuses while a capture is open
+  bool last_graph = false;     // the last numeric call ran from the graph
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[sg::kPhaseSlots];
   double phase_ms[sg::kPhaseSlots] = {0};
   int64_t phase_n[sg::kPhaseSlots] = {0};

@@ -290,3 +290,57 @@ def test_config4_row_windows(gpu_lib):
     finally:
         p.close()
         release_device_memory()
+
+
+@pytest.mark.parametrize("case", ["light", "resident", "recompute", "no_graph"])
+def test_numeric_repeat_graph(gpu_lib, case):
+    """Repeated numeric calls into the same arrays: the second call is captured into a CUDA graph
+    and later calls replay it, where the phase has no host synchronisation (no heavy row, or
+    C^_reord resident).  Without a resident C^_reord each call reads the current values of A and
+    B, so new values (same structure) give the oracle's product of the new values."""
+    import torch
+    import sparse_gemm_irregular_gb300 as sg
+    if case == "light":
+        A, kw = synth.uniform_rows(2048, 8, seed=3), None
+    elif case == "resident":
+        A, kw = synth.rmat(12, 16, seed=8), dict(tau=512, chunk_width=256)
+    elif case == "recompute":
+        A, kw = synth.rmat(11, 16, seed=9), dict(tau=256, chunk_width=128, heavy_batch_elems=20000, flags=16)
+    else:
+        A, kw = synth.uniform_rows(2048, 8, seed=4), dict(flags=sg.binding.FLAG_NO_GRAPH)
+    dA = sg.DeviceCSR.from_host(A)
+    p = sg.Product(dA, dA, opts=opts(**kw) if kw else None)
+    try:
+        rp, nnz = p.symbolic()
+        st0 = p.stats()
+        if case == "resident":
+            assert st0.resident == 1 and st0.rows_heavy > 0
+        if case == "recompute":
+            assert st0.resident == 0 and st0.heavy_batches > 1
+        col = torch.empty(max(nnz, 1), dtype=torch.int32, device="cuda")
+        val = torch.empty(max(nnz, 1), dtype=torch.float64, device="cuda")
+        graphed, launches = [], []
+        for call in range(4):
+            if call >= 2 and case != "resident":  # new values, same structure
+                vals = synth.uniform(40 + call, 0, 0, A.nnz, -1.0, 1.0)
+                A = synth.with_values(A, vals)
+                dA.val.copy_(torch.from_numpy(vals))
+            k0 = sg.spgemm_kernel_launches()
+            p.numeric(col, val)
+            torch.cuda.synchronize()
+            launches.append(sg.spgemm_kernel_launches() - k0)
+            graphed.append(p.stats().numeric_graph)
+            compare_full(A, A, rp.cpu().numpy(), col.cpu().numpy()[:nnz], val.cpu().numpy()[:nnz])
+        expect = [0, 1, 1, 1] if case in ("light", "resident") else [0, 0, 0, 0]
+        assert graphed == expect, sg.spgemm_last_error()
+        # the first call also bins the light rows by their exact size (once per handle); a replay
+        # counts the kernels its graph holds
+        assert launches[1] == launches[2] == launches[3] > 0 and launches[0] >= launches[1]
+        # other output arrays: a new key, so the next call runs eagerly again
+        col2, val2 = torch.empty_like(col), torch.empty_like(val)
+        p.numeric(col2, val2)
+        assert p.stats().numeric_graph == 0
+        torch.cuda.synchronize()
+        compare_full(A, A, rp.cpu().numpy(), col2.cpu().numpy()[:nnz], val2.cpu().numpy()[:nnz])
+    finally:
+        p.close()
