@@ -204,8 +204,10 @@ int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_
 long long spgemm_kernel_launches(void);
 
 /* Device workspace comes from a stream-ordered memory pool (one per device) that keeps freed
- * memory cached for the next product.  This returns the cached memory to the device; call it
- * when no product is running.  Always SPGEMM_OK. */
+ * memory cached for the next product, and the library's internal streams and events are kept
+ * for reuse by later handles.  This returns the cached memory to the device and destroys the
+ * kept streams and events; call it when no product is running (and before any device reset).
+ * Always SPGEMM_OK. */
 int spgemm_release_memory(void);
 
 /* Release the workspace (stream-ordered on the handle's stream) and the handle.  NULL is ok. */

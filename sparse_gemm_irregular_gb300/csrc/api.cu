@@ -86,6 +86,83 @@ void ws_free(spgemm_ctx* h, void* p) {
   cudaFreeAsync(p, h->st);
 }
 
+// Streams and events outlive their handles: a process-wide free list per device, so that small
+// products do not pay for creating and destroying them.  A pooled stream is idle when returned
+// (its handle synchronised it).
+static std::mutex g_sp_mu;
+static std::vector<cudaStream_t> g_sp_streams[64];
+static std::vector<cudaEvent_t> g_sp_events[64];
+
+cudaStream_t pooled_stream(int dev) {
+  {
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    if (dev >= 0 && dev < 64 && !g_sp_streams[dev].empty()) {
+      cudaStream_t s = g_sp_streams[dev].back();
+      g_sp_streams[dev].pop_back();
+      return s;
+    }
+  }
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return s;
+}
+
+cudaEvent_t pooled_event(int dev) {
+  {
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    if (dev >= 0 && dev < 64 && !g_sp_events[dev].empty()) {
+      cudaEvent_t e = g_sp_events[dev].back();
+      g_sp_events[dev].pop_back();
+      return e;
+    }
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+void return_stream(int dev, cudaStream_t s) {
+  if (!s) return;
+  std::lock_guard<std::mutex> lock(g_sp_mu);
+  if (dev >= 0 && dev < 64) g_sp_streams[dev].push_back(s);
+  else cudaStreamDestroy(s);
+}
+
+void return_event(int dev, cudaEvent_t e) {
+  if (!e) return;
+  std::lock_guard<std::mutex> lock(g_sp_mu);
+  if (dev >= 0 && dev < 64) g_sp_events[dev].push_back(e);
+  else cudaEventDestroy(e);
+}
+
+// Page-locked status block of the calling thread: the device error word, nnz(C) and the numeric
+// bin starts land here by asynchronous copies, so one synchronisation reads them all.  The calls
+// of one thread are sequential, so one block per thread suffices.  Null if it cannot be had.
+struct HostStatus {
+  uint32_t err;
+  uint32_t pad;
+  int64_t nnz;
+  int64_t starts[kMaxLadder + 1];
+};
+
+HostStatus* host_status() {
+  thread_local HostStatus* hs = nullptr;
+  thread_local bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    if (cudaMallocHost(&p, sizeof(HostStatus)) == cudaSuccess) hs = static_cast<HostStatus*>(p);
+    else cudaGetLastError();
+  }
+  return hs;
+}
+
 Ladder make_ladder(int64_t tau) {
   Ladder L;
   int64_t u = 32;
@@ -153,10 +230,18 @@ int scan(spgemm_ctx* h, const int64_t* in, int64_t* out, int64_t n) {
 }
 
 int sync_and_check(spgemm_ctx* h, const char* where) {
-  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), where));
-  SG_TRY(check_cuda(cudaGetLastError(), where));
   uint32_t err = 0;
-  SG_TRY(check_cuda(cudaMemcpy(&err, h->d_err, sizeof(err), cudaMemcpyDeviceToHost), where));
+  HostStatus* hs = host_status();
+  if (hs) {  // the error word rides on the same synchronisation
+    SG_TRY(check_cuda(cudaMemcpyAsync(&hs->err, h->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, h->st), where));
+    SG_TRY(check_cuda(cudaStreamSynchronize(h->st), where));
+    SG_TRY(check_cuda(cudaGetLastError(), where));
+    err = hs->err;
+  } else {
+    SG_TRY(check_cuda(cudaStreamSynchronize(h->st), where));
+    SG_TRY(check_cuda(cudaGetLastError(), where));
+    SG_TRY(check_cuda(cudaMemcpy(&err, h->d_err, sizeof(err), cudaMemcpyDeviceToHost), where));
+  }
   if (err) {
     char buf[160];
     snprintf(buf, sizeof(buf), "%s: device check failed (flags 0x%x)", where, err);
@@ -706,14 +791,17 @@ void join_light(spgemm_ctx* h) {
   cudaStreamWaitEvent(h->st, h->ev_join, 0);
 }
 
-// Numeric bins of the light hash rows by their exact nnz (once per handle, after symbolic).
-int numeric_bins(spgemm_ctx* h) {
-  if (!h->nbin_start.empty()) return SPGEMM_OK;
+// Numeric bins of the light hash rows by their exact nnz, from the row_ptr of C.  Enqueued at the
+// end of the symbolic phase with the bin starts copied into `starts` (page-locked) and read after
+// that phase's synchronisation; `starts` null: a synchronous pass of its own.
+int numeric_bins_enqueue(spgemm_ctx* h, const int64_t* c_row_ptr, int64_t* starts_host) {
   const int nl = h->lad.n;
   int64_t nh = 0;
   for (int L = 0; L < nl; ++L) nh += h->bin_start[2 * L + 1] - h->bin_start[2 * L];
-  h->nbin_start.assign(nl + 1, 0);
-  if (nh == 0) return SPGEMM_OK;
+  if (nh == 0) {
+    h->nbin_start.assign(nl + 1, 0);
+    return SPGEMM_OK;
+  }
   int32_t* all;
   uint8_t* bin;
   int64_t *cnt, *starts;
@@ -730,21 +818,33 @@ int numeric_bins(spgemm_ctx* h) {
                            h->st);
     off += c;
   }
-  launch_nnz_bins(all, nh, h->c_row_ptr, h->rule, bin, h->st);
+  launch_nnz_bins(all, nh, c_row_ptr, h->rule, bin, h->st);
   launch_bin_count(bin, nh, nl, cnt, h->st);
   SG_TRY(scan(h, cnt, cnt, nl * nblk));
   // the scatter writes positions into the concatenated list; map them back to row ids
   launch_bin_scatter(bin, nh, nl, cnt, h->d_nrows, h->st);
   launch_gather_rows(all, h->d_nrows, nh, h->st);
   launch_bin_starts(cnt, nblk, nl, starts, h->st);
-  SG_TRY(check_cuda(cudaMemcpyAsync(h->nbin_start.data(), starts, sizeof(int64_t) * (nl + 1), cudaMemcpyDeviceToHost,
-                                    h->st), "copy numeric bins"));
-  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "numeric bins"));
+  if (starts_host) {
+    SG_TRY(check_cuda(cudaMemcpyAsync(starts_host, starts, sizeof(int64_t) * (nl + 1), cudaMemcpyDeviceToHost,
+                                      h->st), "copy numeric bins"));
+  } else {
+    h->nbin_start.assign(nl + 1, 0);
+    SG_TRY(check_cuda(cudaMemcpyAsync(h->nbin_start.data(), starts, sizeof(int64_t) * (nl + 1),
+                                      cudaMemcpyDeviceToHost, h->st), "copy numeric bins"));
+    SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "numeric bins"));
+  }
   ws_free(h, all);
   ws_free(h, bin);
   ws_free(h, cnt);
   ws_free(h, starts);
   return SPGEMM_OK;
+}
+
+// Numeric bins, if the symbolic phase did not leave them.
+int numeric_bins(spgemm_ctx* h) {
+  if (!h->nbin_start.empty()) return SPGEMM_OK;
+  return numeric_bins_enqueue(h, h->c_row_ptr, nullptr);
 }
 
 void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
@@ -1017,9 +1117,10 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
     return fail(SPGEMM_ERR_OUT_OF_MEMORY);
   }
   cudaMemsetAsync(h->d_err, 0, sizeof(uint32_t), h->st);
-  if (cudaStreamCreateWithFlags(&h->st_light, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+  h->st_light = pooled_stream(dev);
+  h->ev_fork = pooled_event(dev);
+  h->ev_join = pooled_event(dev);
+  if (!h->st_light || !h->ev_fork || !h->ev_join) {
     delete tsetup;
     set_last_error("stream or event creation failed");
     return fail(SPGEMM_ERR_CUDA);
@@ -1187,10 +1288,24 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     PhaseTimer t(h, 9);
     SG_TRY(scan(h, c_row_ptr, c_row_ptr, h->m));
   }
+  // nnz(C) and the numeric bins of the light rows come back with the one synchronisation
   int64_t nnz = 0;
-  SG_TRY(check_cuda(cudaMemcpyAsync(&nnz, c_row_ptr + h->m, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
-                    "copy nnz"));
-  SG_TRY(sync_and_check(h, "symbolic"));
+  HostStatus* hs = host_status();
+  bool bins_pending = false;
+  if (hs) {
+    h->nbin_start.clear();
+    SG_TRY(numeric_bins_enqueue(h, c_row_ptr, hs->starts));
+    bins_pending = h->nbin_start.empty();
+    SG_TRY(check_cuda(cudaMemcpyAsync(&hs->nnz, c_row_ptr + h->m, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                      "copy nnz"));
+    SG_TRY(sync_and_check(h, "symbolic"));
+    nnz = hs->nnz;
+    if (bins_pending) h->nbin_start.assign(hs->starts, hs->starts + h->lad.n + 1);
+  } else {
+    SG_TRY(check_cuda(cudaMemcpyAsync(&nnz, c_row_ptr + h->m, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                      "copy nnz"));
+    SG_TRY(sync_and_check(h, "symbolic"));
+  }
   *c_nnz = nnz;
   h->stats.c_nnz = nnz;
   h->stats.c_nnz_heavy = 0;
@@ -1337,17 +1452,26 @@ int spgemm_destroy(spgemm_handle h) {
     if (h->ev_copied[b]) cudaEventDestroy(h->ev_copied[b]);
   }
   if (h->st_copy) cudaStreamDestroy(h->st_copy);
-  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-  if (h->ev_join) cudaEventDestroy(h->ev_join);
-  if (h->st_light) cudaStreamDestroy(h->st_light);
+  return_event(h->device, h->ev_fork);
+  return_event(h->device, h->ev_join);
+  return_stream(h->device, h->st_light);  // synchronised above
   delete h;
   return SPGEMM_OK;
 }
 
 int spgemm_release_memory(void) {
-  std::lock_guard<std::mutex> lock(g_pool_mu);
-  for (int d = 0; d < 64; ++d)
-    if (g_pool[d]) cudaMemPoolTrimTo(g_pool[d], 0);
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    for (int d = 0; d < 64; ++d)
+      if (g_pool[d]) cudaMemPoolTrimTo(g_pool[d], 0);
+  }
+  std::lock_guard<std::mutex> lock(g_sp_mu);
+  for (int d = 0; d < 64; ++d) {
+    for (cudaStream_t st : g_sp_streams[d]) cudaStreamDestroy(st);
+    for (cudaEvent_t e : g_sp_events[d]) cudaEventDestroy(e);
+    g_sp_streams[d].clear();
+    g_sp_events[d].clear();
+  }
   return SPGEMM_OK;
 }
 

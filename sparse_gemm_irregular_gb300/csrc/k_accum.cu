@@ -417,13 +417,17 @@ __device__ void block_bucket_emit(const Group<false>& g, const Smem& s, int64_t 
   for (int64_t i = g.lane; i < n; i += g.size)
     order[atomicAdd(&cnt[(s.keys[i] - lo) >> shift], 1u)] = static_cast<int32_t>(i);  // cnt[b]: end of bucket b
   __syncthreads();
-  for (int64_t i = g.lane; i < n; i += g.size) {
+  // rank inside the bucket, taken in bucket order: the lanes of a warp mostly share one bucket,
+  // so they run the same number of comparisons and read the same members (broadcast loads); in
+  // entry order one dense bucket would hold back every warp that has one of its members
+  for (int64_t p = g.lane; p < n; p += g.size) {
+    const int32_t i = order[p];
     const int32_t k = s.keys[i];
     const int64_t bk = (k - lo) >> shift;
     const unsigned b0 = bk > 0 ? cnt[bk - 1] : 0u, b1 = cnt[bk];
     unsigned r = b0;
     for (unsigned j = b0; j < b1; ++j) r += s.keys[order[j]] < k ? 1u : 0u;  // columns are distinct
-    inv[r] = static_cast<int32_t>(i);
+    inv[r] = i;
   }
   __syncthreads();
   for (int64_t r = g.lane; r < n; r += g.size) {
