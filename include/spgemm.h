@@ -89,8 +89,29 @@ typedef struct {
   int64_t heavy_batch_elems; /* most heavy intermediate products expanded at once          */
   int64_t smem_bytes;        /* shared-memory budget s_LM per thread block                 */
   int32_t flags;             /* SPGEMM_FLAG_* */
+  int32_t workflow;          /* SPGEMM_WORKFLOW_*: how the light rows are sized (0: exact symbolic) */
+  int32_t hll_registers;     /* estimated workflow: 32 or 64 registers per sketch (0: by the
+                                expansion ratio, 32 below 48 products per entry of A, else 64) */
   int32_t reserved;
+  double hll_coef;           /* estimated workflow: capacity = ceil(coef * estimate) (0: 2.0 with
+                                32 registers, 1.5 with 64) */
 } spgemm_options;
+
+/* Light-row sizing (Ocean page, Table 1 and the estimation-based workflow).  SYMBOLIC counts
+ * every light row exactly before the numeric phase.  UPPER_BOUND and ESTIMATE skip that count:
+ * the light rows are accumulated during spgemm_symbolic into temporary slots of a capacity --
+ * the row's intermediate-product count (a bound), or a HyperLogLog estimate times a coefficient
+ * -- and their exact sizes come out of that pass; rows that do not fit their estimated slot are
+ * accumulated again with the bound.  spgemm_numeric then copies them to their final positions.
+ * The light rows' values are therefore read during spgemm_symbolic.  AUTO applies the page's
+ * selection: UPPER_BOUND when the average row has fewer than 64 intermediate products, ESTIMATE
+ * when the expansion ratio (products per entry of A) and the sampled compression ratio
+ * (products per entry of C, from HyperLogLog estimates of 3% of the rows, 600 to 10,000) are
+ * both at least 8, else SYMBOLIC.  Heavy rows always take the exact multisplit path. */
+#define SPGEMM_WORKFLOW_SYMBOLIC 0
+#define SPGEMM_WORKFLOW_UPPER_BOUND 1
+#define SPGEMM_WORKFLOW_ESTIMATE 2
+#define SPGEMM_WORKFLOW_AUTO 3
 
 #define SPGEMM_MAX_LEVELS 8
 
@@ -128,6 +149,9 @@ typedef struct {
   int64_t dense_nnz;         /* entries of C those dense chunks produce                 */
   int32_t resident;          /* 1: C^_reord kept from symbolic to numeric               */
   int32_t numeric_graph;     /* 1: the last numeric call replayed a captured CUDA graph */
+  int64_t rows_overflow;     /* estimated workflow: light rows that exceeded their slot    */
+  int32_t workflow;          /* SPGEMM_WORKFLOW_* the symbolic phase ran (after AUTO)      */
+  int32_t hll_registers;     /* registers per sketch (estimated workflow), else 0          */
 } spgemm_stats;
 
 typedef struct spgemm_ctx* spgemm_handle;
@@ -159,8 +183,9 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz);
  * caller-owned, each row sorted by column, at the positions of the row_ptr from
  * spgemm_symbolic (which must still hold those values).  May be called more than once.  When
  * no C^_reord is kept from symbolic (stats.resident == 0: no heavy row, or SPGEMM_FLAG_RECOMPUTE)
- * every call reads the current values of A and B, so their values (never their structure) may
- * change between calls.  A call repeating the previous one's arguments is captured into a CUDA
+ * and the light rows were sized exactly (stats.workflow == SPGEMM_WORKFLOW_SYMBOLIC), every call
+ * reads the current values of A and B, so their values (never their structure) may change
+ * between calls.  A call repeating the previous one's arguments is captured into a CUDA
  * graph, and later repeats replay it (stats.numeric_graph), when the phase needs no host
  * synchronisation: no heavy row, or C^_reord resident.  SPGEMM_FLAG_NO_GRAPH turns this off. */
 int spgemm_numeric(spgemm_handle h, int32_t* c_col_idx, double* c_vals);
@@ -231,6 +256,19 @@ int spgemm_destroy(spgemm_handle h);
  * (cudaGetSymbolAddress, with that device current), so make that first call before any
  * stream capture.  Every call on a device shares the one array: calls that overlap on the
  * GPU (other streams, other host threads) race and give wrong results; serialise them. */
+/* HyperLogLog output-size estimates for every row of C = A * B (Ocean page: HyperLogLog
+ * background, construct-and-merge of Figure 3).  One sketch of `registers` (32 or 64) one-byte
+ * registers per row of B: a column's 32-bit hash (MurmurHash3 finaliser) picks its register by
+ * the low bits and offers 1 + the leading zeros of the other bits; row i's sketch is the
+ * element-wise maximum over the rows of B that row i of A selects; its estimate is the
+ * HyperLogLog harmonic-mean estimate with linear counting below 5m/2.  Writes cap[i] =
+ * min(IP_i, ceil(coef * estimate_i)) (0 for rows without products) into the DEVICE array cap (A.rows
+ * int64).  A and B are device CSR with A.cols == B.rows.  Enqueued on `stream`; scratch is
+ * allocated and freed stream-ordered.  Errors: INVALID_ARG (null pointers, shape mismatch,
+ * registers not 32 or 64, coef <= 0), OUT_OF_MEMORY, CUDA. */
+int spgemm_hll_estimate(const spgemm_csr* A, const spgemm_csr* B, int32_t registers, double coef,
+                        int64_t* cap, void* stream);
+
 int spgemm_symbolic_noalloc(int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
                             const spgemm_csr* B, int64_t* c_row_ptr, int64_t* c_nnz, void* stream);
 

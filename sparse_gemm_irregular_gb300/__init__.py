@@ -10,14 +10,14 @@ from dataclasses import dataclass
 
 from . import binding
 from .binding import (SpgemmError, load, options, spgemm_create, spgemm_destroy, spgemm_get_phase_times,
-                      spgemm_numeric_host,
+                      spgemm_hll_estimate, spgemm_numeric_host,
                       spgemm_get_plan, spgemm_get_stats, spgemm_kernel_launches, spgemm_last_error, spgemm_numeric,
                       spgemm_numeric_rows, spgemm_plan_params, spgemm_release_memory, spgemm_strerror,
                       spgemm_symbolic)
 
 __all__ = [
     "DeviceCSR", "multiply", "Product", "SpgemmError", "load", "options", "spgemm_create",
-    "spgemm_destroy", "spgemm_get_phase_times", "spgemm_get_plan", "spgemm_get_stats",
+    "spgemm_destroy", "spgemm_get_phase_times", "spgemm_get_plan", "spgemm_get_stats", "spgemm_hll_estimate",
     "spgemm_kernel_launches",
     "spgemm_last_error", "spgemm_numeric", "spgemm_numeric_rows", "spgemm_plan_params",
     "spgemm_release_memory",

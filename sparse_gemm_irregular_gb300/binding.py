@@ -29,6 +29,7 @@ FLAG_DIRECT_SPLIT = 256
 FLAG_TMA_SPLIT = 512
 FLAG_FUSED_HIST = 1024
 FLAG_NO_GRAPH = 2048
+WORKFLOW_SYMBOLIC, WORKFLOW_UPPER_BOUND, WORKFLOW_ESTIMATE, WORKFLOW_AUTO = 0, 1, 2, 3
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",
           "light_numeric", "chunk_numeric", "chunk_dense"]
@@ -47,7 +48,7 @@ class spgemm_csr(ctypes.Structure):
 class spgemm_options(ctypes.Structure):
     _fields_ = [("tau", _i64), ("chunk_width", _i64), ("chunks_max", _i64),
                 ("heavy_batch_elems", _i64), ("smem_bytes", _i64), ("flags", _i32),
-                ("reserved", _i32)]
+                ("workflow", _i32), ("hll_registers", _i32), ("reserved", _i32), ("hll_coef", ctypes.c_double)]
 
 
 class spgemm_plan(ctypes.Structure):
@@ -63,7 +64,8 @@ class spgemm_stats(ctypes.Structure):
                 ("rows_dense_light", _i64), ("c_nnz", _i64), ("heavy_batches", _i64),
                 ("levels_run", _i64), ("final_chunks", _i64), ("chunks_dense", _i64),
                 ("chat_bytes", _i64), ("c_nnz_heavy", _i64), ("dense_elems", _i64), ("dense_nnz", _i64),
-                ("resident", _i32), ("numeric_graph", _i32)]
+                ("resident", _i32), ("numeric_graph", _i32), ("rows_overflow", _i64), ("workflow", _i32),
+                ("hll_registers", _i32)]
 
 
 EXPORTS = {
@@ -79,6 +81,7 @@ EXPORTS = {
     "spgemm_get_phase_times": (ctypes.c_int, [_vp, _vp, _vp, _i32]),
     "spgemm_kernel_launches": (ctypes.c_longlong, []),
     "spgemm_symbolic_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "spgemm_hll_estimate": (ctypes.c_int, [_vp, _vp, _i32, ctypes.c_double, _vp, _vp]),
     "spgemm_release_memory": (ctypes.c_int, []),
     "spgemm_destroy": (ctypes.c_int, [_vp]),
     "spgemm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -190,6 +193,12 @@ def spgemm_symbolic_noalloc(m, k, n, A: spgemm_csr, B: spgemm_csr, c_row_ptr: in
     _check(load().spgemm_symbolic_noalloc(m, k, n, ctypes.byref(A), ctypes.byref(B), _vp(c_row_ptr),
                                           ctypes.byref(nnz), _vp(stream)), "spgemm_symbolic_noalloc")
     return nnz.value
+
+
+def spgemm_hll_estimate(A: spgemm_csr, B: spgemm_csr, registers: int, coef: float, cap: int, stream: int = 0):
+    """HyperLogLog capacity of every row of A*B into the device array ``cap`` (see spgemm.h)."""
+    _check(load().spgemm_hll_estimate(ctypes.byref(A), ctypes.byref(B), registers, coef, _vp(cap), _vp(stream)),
+           "spgemm_hll_estimate")
 
 
 def spgemm_destroy(h):

@@ -841,9 +841,10 @@ int numeric_bins_enqueue(spgemm_ctx* h, const int64_t* c_row_ptr, int64_t* start
   return SPGEMM_OK;
 }
 
-// Numeric bins, if the symbolic phase did not leave them.
+// Numeric bins, if the symbolic phase did not leave them (exact workflow only: the estimated
+// workflows accumulate the light rows during the symbolic phase).
 int numeric_bins(spgemm_ctx* h) {
-  if (!h->nbin_start.empty()) return SPGEMM_OK;
+  if (!h->nbin_start.empty() || h->workflow != SPGEMM_WORKFLOW_SYMBOLIC) return SPGEMM_OK;
   return numeric_bins_enqueue(h, h->c_row_ptr, nullptr);
 }
 
@@ -867,6 +868,250 @@ void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
   }
 }
 
+// ---- estimated light-row sizing (Ocean page: Table 1, the estimation-based workflow) -------
+
+// Stable split of a row list by a per-item bin in [0, nb): `out` receives the rows bin by bin,
+// `starts` (host, nb + 1) the bin boundaries.  Synchronises to read them.
+int split_rows(spgemm_ctx* h, const int32_t* rows, int64_t n, const uint8_t* bin, int nb, int32_t* out,
+               std::vector<int64_t>& starts) {
+  starts.assign(nb + 1, 0);
+  if (n == 0) return SPGEMM_OK;
+  const int64_t nblk = bin_blocks(n);
+  int64_t *cnt, *st;
+  SG_ALLOC(cnt, int64_t, nb * nblk + 1);
+  SG_ALLOC(st, int64_t, nb + 1);
+  launch_bin_count(bin, n, nb, cnt, h->st);
+  SG_TRY(scan(h, cnt, cnt, nb * nblk));
+  launch_bin_scatter(bin, n, nb, cnt, out, h->st);  // item index at its position
+  launch_gather_rows(rows, out, n, h->st);           // item index -> row id
+  launch_bin_starts(cnt, nblk, nb, st, h->st);
+  SG_TRY(check_cuda(cudaMemcpyAsync(starts.data(), st, sizeof(int64_t) * (nb + 1), cudaMemcpyDeviceToHost, h->st),
+                    "copy split"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "split"));
+  ws_free(h, cnt);
+  ws_free(h, st);
+  return SPGEMM_OK;
+}
+
+int ensure_sketch(spgemm_ctx* h) {
+  if (h->d_sketch) return SPGEMM_OK;
+  SG_ALLOC(h->d_sketch, uint8_t, std::max<int64_t>(h->B.rows, 1) * h->hll_m);
+  launch_hll_sketch(h->B, h->hll_m, h->d_sketch, h->st);
+  return SPGEMM_OK;
+}
+
+// The workflow of the light rows (Table 1 of the Ocean page for SPGEMM_WORKFLOW_AUTO): the
+// upper bound when the average row has fewer than 64 products; HyperLogLog estimates when the
+// expansion ratio (products per entry of A) and the compression ratio (products per entry of
+// C) of a row sample -- 3% of the rows, at least 600 and at most 10,000, evenly spaced -- are
+// both at least 8; else the exact symbolic pass.
+int choose_workflow(spgemm_ctx* h) {
+  const int64_t ipt = h->stats.ip_total;
+  const double er = h->A.nnz > 0 ? static_cast<double>(ipt) / static_cast<double>(h->A.nnz) : 0.0;
+  h->hll_m = h->opt.hll_registers ? h->opt.hll_registers : (er < 48.0 ? 32 : 64);
+  h->hll_coef = h->opt.hll_coef > 0.0 ? h->opt.hll_coef : (h->hll_m == 32 ? 2.0 : 1.5);
+  int wf = h->opt.workflow;
+  if (wf == SPGEMM_WORKFLOW_AUTO) {
+    if (h->m > 0 && static_cast<double>(ipt) / static_cast<double>(h->m) < 64.0) {
+      wf = SPGEMM_WORKFLOW_UPPER_BOUND;
+    } else if (er < 8.0) {
+      wf = SPGEMM_WORKFLOW_SYMBOLIC;
+    } else {
+      const int64_t want = std::min<int64_t>(
+          h->m, std::max<int64_t>(600, std::min<int64_t>(10000, (3 * h->m + 50) / 100)));
+      std::vector<int32_t> rows(want);
+      for (int64_t j = 0; j < want; ++j) rows[j] = static_cast<int32_t>(j * h->m / want);
+      int32_t* d_rows;
+      int64_t *d_ipv, *d_capv;
+      double* d_est;
+      SG_ALLOC(d_rows, int32_t, want);
+      SG_ALLOC(d_ipv, int64_t, want);
+      SG_ALLOC(d_capv, int64_t, h->m);
+      SG_ALLOC(d_est, double, want);
+      SG_TRY(check_cuda(cudaMemcpyAsync(d_rows, rows.data(), sizeof(int32_t) * want, cudaMemcpyHostToDevice, h->st),
+                        "copy sample"));
+      SG_TRY(ensure_sketch(h));
+      launch_hll_rows(h->A, d_rows, want, h->d_ip, h->d_sketch, h->hll_m, h->hll_coef, d_capv, d_est, h->st);
+      launch_gather_ip(d_rows, want, h->d_ip, d_ipv, h->st);
+      std::vector<double> est(want);
+      std::vector<int64_t> ipv(want);
+      SG_TRY(check_cuda(cudaMemcpyAsync(est.data(), d_est, sizeof(double) * want, cudaMemcpyDeviceToHost, h->st),
+                        "copy sample estimates"));
+      SG_TRY(check_cuda(cudaMemcpyAsync(ipv.data(), d_ipv, sizeof(int64_t) * want, cudaMemcpyDeviceToHost, h->st),
+                        "copy sample products"));
+      SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "workflow sample"));
+      double sip = 0.0, sest = 0.0;
+      for (int64_t j = 0; j < want; ++j)
+        if (ipv[j] > 0) {
+          sip += static_cast<double>(ipv[j]);
+          sest += est[j];
+        }
+      const double cr = sest > 0.0 ? sip / sest : 0.0;
+      wf = cr >= 8.0 ? SPGEMM_WORKFLOW_ESTIMATE : SPGEMM_WORKFLOW_SYMBOLIC;
+      ws_free(h, d_rows);
+      ws_free(h, d_ipv);
+      ws_free(h, d_capv);
+      ws_free(h, d_est);
+    }
+  }
+  h->workflow = wf;
+  h->stats.workflow = wf;
+  h->stats.hll_registers = wf == SPGEMM_WORKFLOW_ESTIMATE ? h->hll_m : 0;
+  return SPGEMM_OK;
+}
+
+// One pass of the light rows into temporary slots: the hash rows listed per ladder level
+// (`hrows`, `hstart`), the dense rows from the create bins; every row gets its nnz in `rp` and
+// est_nnz, or is marked as overflowed.
+void est_pass(spgemm_ctx* h, const int32_t* hrows, const std::vector<int64_t>& hstart, bool dense_rows,
+              const EstSink& es, int64_t* rp) {
+  Sink sk{};
+  sk.row_nnz = rp;
+  sk.row_begin = 0;
+  sk.row_end = h->m;
+  for (int L = 0; L < h->lad.n; ++L) {
+    for (int d = 0; d < 2; ++d) {
+      if (d == 1 && !dense_rows) continue;
+      RowJob job;
+      if (d == 0) {
+        job.rows = hrows + hstart[L];
+        job.count = hstart[L + 1] - hstart[L];
+      } else {
+        job.rows = h->d_rows + h->bin_start[2 * L + 1];
+        job.count = h->bin_start[2 * L + 2] - h->bin_start[2 * L + 1];
+      }
+      job.slots = h->lad.slots[L];
+      job.tpr = h->lad.tpr[L];
+      job.dense = d == 1;
+      launch_light(h->A, h->B, h->d_span_lo, job, true, sk, h->d_err, h->st, &es);
+    }
+  }
+}
+
+// Light rows under SPGEMM_WORKFLOW_UPPER_BOUND / _ESTIMATE: capacities, one accumulation pass
+// into temporary slots (their exact sizes come out of it), and for the rows that did not fit a
+// second pass with the IP bound as capacity.  Runs on the handle's stream.
+int est_light(spgemm_ctx* h, int64_t* rp) {
+  const int nl = h->lad.n;
+  const int64_t nlight = h->bin_start[2 * nl];  // light rows: d_rows[0, nlight), bins 0 .. 2nl-1
+  if (nlight == 0) return SPGEMM_OK;
+  PhaseTimer t(h, 1);
+  const bool est = h->workflow == SPGEMM_WORKFLOW_ESTIMATE;
+  SG_ALLOC(h->d_est_nnz, int64_t, h->m);
+  SG_ALLOC(h->d_row_tmp, int64_t, h->m);
+  const int64_t* cap = h->d_ip;
+  if (est) {
+    SG_TRY(ensure_sketch(h));
+    SG_ALLOC(h->d_cap, int64_t, h->m);
+    launch_copy_i64(h->d_ip, h->d_cap, h->m, h->st);  // dense rows keep the IP bound
+    for (int L = 0; L < nl; ++L)
+      launch_hll_rows(h->A, h->d_rows + h->bin_start[2 * L], h->bin_start[2 * L + 1] - h->bin_start[2 * L],
+                      h->d_ip, h->d_sketch, h->hll_m, h->hll_coef, h->d_cap, nullptr, h->st);
+    cap = h->d_cap;
+  }
+  // slots in light-row order
+  int64_t* off;
+  SG_ALLOC(off, int64_t, nlight + 1);
+  launch_gather_ip(h->d_rows, nlight, cap, off, h->st);
+  SG_TRY(scan(h, off, off, nlight));
+  launch_scatter_off(h->d_rows, nlight, off, 0, h->d_row_tmp, h->st);
+  int64_t total = 0;
+  SG_TRY(check_cuda(cudaMemcpyAsync(&total, off + nlight, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy slot total"));
+  // hash rows of pass 1: the create bins (IP levels), or re-binned by their capacity
+  std::vector<int64_t> hstart(nl + 1, 0);
+  const int32_t* hrows = h->d_rows;
+  int32_t* all = nullptr;
+  int32_t* binned = nullptr;
+  int64_t nh = 0;
+  for (int L = 0; L < nl; ++L) nh += h->bin_start[2 * L + 1] - h->bin_start[2 * L];
+  if (est && nh > 0) {
+    uint8_t* bin;
+    SG_ALLOC(all, int32_t, nh);
+    SG_ALLOC(binned, int32_t, nh);
+    SG_ALLOC(bin, uint8_t, nh);
+    int64_t o = 0;
+    for (int L = 0; L < nl; ++L) {
+      const int64_t c = h->bin_start[2 * L + 1] - h->bin_start[2 * L];
+      if (c) cudaMemcpyAsync(all + o, h->d_rows + h->bin_start[2 * L], sizeof(int32_t) * c, cudaMemcpyDeviceToDevice,
+                             h->st);
+      o += c;
+    }
+    launch_val_bins(all, nh, h->d_cap, h->rule, bin, h->st);
+    SG_TRY(split_rows(h, all, nh, bin, nl, binned, hstart));
+    ws_free(h, bin);
+    hrows = binned;
+  } else {
+    SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "slot total"));
+  }
+  SG_ALLOC(h->d_tmp_col[0], int32_t, std::max<int64_t>(total, 1));
+  SG_ALLOC(h->d_tmp_val[0], double, std::max<int64_t>(total, 1));
+  EstSink es{cap, h->d_row_tmp, h->d_tmp_col[0], h->d_tmp_val[0], h->d_est_nnz};
+  if (est && nh > 0) {
+    est_pass(h, hrows, hstart, true, es, rp);
+  } else {  // the create lists: level L's hash rows, then its dense rows
+    Sink sk{};
+    sk.row_nnz = rp;
+    sk.row_begin = 0;
+    sk.row_end = h->m;
+    for (int L = 0; L < nl; ++L)
+      for (int d = 0; d < 2; ++d) {
+        RowJob job;
+        job.rows = h->d_rows + h->bin_start[2 * L + d];
+        job.count = h->bin_start[2 * L + d + 1] - h->bin_start[2 * L + d];
+        job.slots = h->lad.slots[L];
+        job.tpr = h->lad.tpr[L];
+        job.dense = d == 1;
+        launch_light(h->A, h->B, h->d_span_lo, job, true, sk, h->d_err, h->st, &es);
+      }
+  }
+  ws_free(h, off);
+  h->d_est_list[0] = h->d_rows;
+  h->est_count[0] = nlight;
+  h->est_count[1] = 0;
+  h->stats.rows_overflow = 0;
+  if (!est) return SPGEMM_OK;
+  // rows that overflowed their estimated slot: a second pass with the IP bound
+  uint8_t* ob;
+  int32_t* split;
+  std::vector<int64_t> os;
+  SG_ALLOC(ob, uint8_t, nlight);
+  SG_ALLOC(split, int32_t, nlight);
+  launch_overflow_bins(h->d_rows, nlight, h->d_est_nnz, ob, h->st);
+  SG_TRY(split_rows(h, h->d_rows, nlight, ob, 2, split, os));
+  ws_free(h, ob);
+  const int64_t nover = os[2] - os[1];
+  h->d_est_list[0] = split;
+  h->est_count[0] = os[1];
+  h->stats.rows_overflow = nover;
+  if (nover == 0) return SPGEMM_OK;
+  const int32_t* over = split + os[1];
+  int64_t* off2;
+  SG_ALLOC(off2, int64_t, nover + 1);
+  launch_gather_ip(over, nover, h->d_ip, off2, h->st);
+  SG_TRY(scan(h, off2, off2, nover));
+  launch_scatter_off(over, nover, off2, 0, h->d_row_tmp, h->st);
+  int64_t total2 = 0;
+  SG_TRY(check_cuda(cudaMemcpyAsync(&total2, off2 + nover, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy fallback total"));
+  uint8_t* lb;
+  int32_t* obinned;
+  std::vector<int64_t> ostart;
+  SG_ALLOC(lb, uint8_t, nover);
+  SG_ALLOC(obinned, int32_t, nover);
+  launch_val_bins(over, nover, h->d_ip, h->rule, lb, h->st);
+  SG_TRY(split_rows(h, over, nover, lb, nl, obinned, ostart));  // synchronises: total2 is in
+  ws_free(h, lb);
+  ws_free(h, off2);
+  SG_ALLOC(h->d_tmp_col[1], int32_t, std::max<int64_t>(total2, 1));
+  SG_ALLOC(h->d_tmp_val[1], double, std::max<int64_t>(total2, 1));
+  EstSink es2{h->d_ip, h->d_row_tmp, h->d_tmp_col[1], h->d_tmp_val[1], h->d_est_nnz};
+  est_pass(h, obinned, ostart, false, es2, rp);
+  h->d_est_list[1] = obinned;
+  h->est_count[1] = nover;
+  return SPGEMM_OK;
+}
+
 // Enqueue the numeric phase of rows [rb, re) on the handle's stream, written at offset 0 =
 // row_ptr[rb] of c_col / c_val; no synchronisation.
 int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double* c_val) {
@@ -876,11 +1121,17 @@ int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, doubl
   sk.c_val = c_val;
   sk.row_begin = rb;
   sk.row_end = re;
-  SG_TRY(numeric_bins(h));
-  fork_light(h);
-  {
+  if (h->workflow == SPGEMM_WORKFLOW_SYMBOLIC) {
+    SG_TRY(numeric_bins(h));
+    fork_light(h);
     PhaseTimer t(h, 10, h->st_light);
     light_pass(h, true, sk);
+  } else {
+    fork_light(h);
+    PhaseTimer t(h, 10);
+    for (int b = 0; b < 2; ++b)  // light rows: temporary slots -> final positions
+      launch_copy_rows(h->d_est_list[b], h->est_count[b], h->d_row_tmp, h->c_row_ptr, rb, re, h->d_tmp_col[b],
+                       h->d_tmp_val[b], c_col, c_val, h->st);
   }
   for (auto& hb : h->batches) {
     if (hb.row_hi < rb || hb.row_lo >= re) continue;
@@ -1048,6 +1299,12 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
   h->B = *B;
   h->st = static_cast<cudaStream_t>(stream);
   if (opt) h->opt = *opt;
+  if (h->opt.workflow < SPGEMM_WORKFLOW_SYMBOLIC || h->opt.workflow > SPGEMM_WORKFLOW_AUTO ||
+      (h->opt.hll_registers != 0 && !hll_registers_ok(h->opt.hll_registers)) || !(h->opt.hll_coef >= 0.0)) {
+    delete h;
+    set_last_error("invalid workflow, register count or coefficient");
+    return SPGEMM_ERR_INVALID_ARG;
+  }
   const char* tenv = getenv("SPGEMM_TIMING");
   h->timing = (tenv && tenv[0] == '1') || (h->opt.flags & SPGEMM_FLAG_TIMING);
   int rc = SPGEMM_OK;
@@ -1254,8 +1511,10 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
   sk.row_nnz = c_row_ptr;
   sk.row_begin = 0;
   sk.row_end = h->m;
+  SG_TRY(choose_workflow(h));
+  if (h->workflow != SPGEMM_WORKFLOW_SYMBOLIC) SG_TRY(est_light(h, c_row_ptr));
   fork_light(h);
-  {
+  if (h->workflow == SPGEMM_WORKFLOW_SYMBOLIC) {
     PhaseTimer t(h, 1, h->st_light);
     light_pass(h, false, sk);
   }
@@ -1294,8 +1553,8 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
   bool bins_pending = false;
   if (hs) {
     h->nbin_start.clear();
-    SG_TRY(numeric_bins_enqueue(h, c_row_ptr, hs->starts));
-    bins_pending = h->nbin_start.empty();
+    if (h->workflow == SPGEMM_WORKFLOW_SYMBOLIC) SG_TRY(numeric_bins_enqueue(h, c_row_ptr, hs->starts));
+    bins_pending = h->nbin_start.empty() && h->workflow == SPGEMM_WORKFLOW_SYMBOLIC;
     SG_TRY(check_cuda(cudaMemcpyAsync(&hs->nnz, c_row_ptr + h->m, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
                       "copy nnz"));
     SG_TRY(sync_and_check(h, "symbolic"));
@@ -1437,6 +1696,31 @@ int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_
 }
 
 long long spgemm_kernel_launches(void) { return launch_count(); }
+
+int spgemm_hll_estimate(const spgemm_csr* A, const spgemm_csr* B, int32_t registers, double coef, int64_t* cap,
+                        void* stream) {
+  g_last_error.clear();
+  if (!A || !B || !cap || A->rows < 0 || B->rows < 0 || A->cols != B->rows || !hll_registers_ok(registers) ||
+      !(coef > 0.0))
+    return SPGEMM_ERR_INVALID_ARG;
+  if (A->rows == 0) return SPGEMM_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* sk = nullptr;
+  int64_t* ip = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&sk), std::max<int64_t>(B->rows, 1) * registers, st) != cudaSuccess ||
+      cudaMallocAsync(reinterpret_cast<void**>(&ip), sizeof(int64_t) * A->rows, st) != cudaSuccess) {
+    cudaGetLastError();
+    if (sk) cudaFreeAsync(sk, st);
+    set_last_error("sketch allocation failed");
+    return SPGEMM_ERR_OUT_OF_MEMORY;
+  }
+  launch_hll_sketch(*B, registers, sk, st);
+  launch_row_products(*A, *B, ip, st);
+  launch_hll_rows(*A, nullptr, A->rows, ip, sk, registers, coef, cap, nullptr, st);
+  cudaFreeAsync(sk, st);
+  cudaFreeAsync(ip, st);
+  return check_cuda(cudaGetLastError(), "hll estimate");
+}
 
 int spgemm_destroy(spgemm_handle h) {
   if (!h) return SPGEMM_OK;

@@ -103,13 +103,45 @@ struct Sink {            // where results go
   double* c_val;
   int64_t row_begin, row_end;  // numeric row window; output index 0 = row_ptr[row_begin]
 };
+struct EstSink {          // estimated workflows (numeric pass run before the row sizes are known)
+  const int64_t* cap;      // per global row: output capacity (an estimate, or the IP bound)
+  const int64_t* row_tmp;  // per global row: offset of its slot in the temporary output
+  int32_t* tmp_col;
+  double* tmp_val;
+  int64_t* est_nnz;        // out per global row: nnz, or -1 when the row overflowed its capacity
+};
+// est != null: numeric rows write sorted into their temporary slot and their nnz into
+// sink.row_nnz, or mark themselves in est_nnz when they do not fit.
 void launch_light(const spgemm_csr& A, const spgemm_csr& B, const int32_t* span_lo,
                   const RowJob& job, bool numeric, const Sink& sink, uint32_t* err,
-                  cudaStream_t s);
+                  cudaStream_t s, const EstSink* est = nullptr);
 void launch_chunks(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t slots, int tpr,
                    bool dense, int64_t dense_width, bool numeric, const Sink& sink,
                    uint32_t* err, cudaStream_t s);
 size_t light_smem_bytes(int64_t slots, int tpr, bool dense, bool numeric);
+
+// ---- estimated light-row sizing (k_estimate.cu) ------------------------------------------
+bool hll_registers_ok(int m);
+// one sketch of m one-byte registers per row of B (out: B.rows * m bytes)
+void launch_hll_sketch(const spgemm_csr& B, int m, uint8_t* out, cudaStream_t s);
+// capacity of the listed rows of A*B (all rows if rows == nullptr): cap[row] = min(ip[row],
+// ceil(coef * estimate)); est_out[i] (optional) = the raw estimate of the i-th listed row
+void launch_hll_rows(const spgemm_csr& A, const int32_t* rows, int64_t n, const int64_t* ip, const uint8_t* sk,
+                     int m, double coef, int64_t* cap, double* est_out, cudaStream_t s);
+// intermediate products of every row of A*B
+void launch_row_products(const spgemm_csr& A, const spgemm_csr& B, int64_t* ip, cudaStream_t s);
+// bin[i] = ladder level of val[rows[i]]
+void launch_val_bins(const int32_t* rows, int64_t n, const int64_t* val, const BinRule& rule, uint8_t* bin,
+                     cudaStream_t s);
+// bin[i] = 1 if est_nnz[rows[i]] < 0 (the row overflowed its slot), else 0
+void launch_overflow_bins(const int32_t* rows, int64_t n, const int64_t* est_nnz, uint8_t* bin, cudaStream_t s);
+// dst[rows[i]] = base + off[i]
+void launch_scatter_off(const int32_t* rows, int64_t n, const int64_t* off, int64_t base, int64_t* dst,
+                        cudaStream_t s);
+// listed rows inside [row_begin, row_end): temporary slot -> final position
+void launch_copy_rows(const int32_t* rows, int64_t n, const int64_t* row_tmp, const int64_t* row_ptr,
+                      int64_t row_begin, int64_t row_end, const int32_t* tcol, const double* tval, int32_t* ccol,
+                      double* cval, cudaStream_t s);
 
 // ---- heavy pipeline (k_heavy.cu) ---------------------------------------------------------
 void launch_gather_ip(const int32_t* heavy_rows, int64_t nrows, const int64_t* ip, int64_t* out,
@@ -277,6 +309,19 @@ struct spgemm_ctx {
   long long num_launches = 0;  // kernel launches the graph holds
   bool capturing = false;      // ws_alloc refuses while a capture is open
   bool last_graph = false;     // the last numeric call ran from the graph
+
+  // light rows sized by their IP bound or by HyperLogLog estimates (SPGEMM_WORKFLOW_*)
+  int workflow = 0;            // the workflow the symbolic phase ran
+  int hll_m = 0;               // registers per sketch
+  double hll_coef = 0.0;
+  uint8_t* d_sketch = nullptr; // one sketch per row of B
+  int64_t* d_cap = nullptr;    // per row: capacity of its temporary slot
+  int64_t* d_row_tmp = nullptr;// per row: offset of its slot
+  int64_t* d_est_nnz = nullptr;// per row: nnz, or -1 (overflowed)
+  int32_t* d_tmp_col[2] = {nullptr, nullptr};  // temporary output: first pass, fallback pass
+  double* d_tmp_val[2] = {nullptr, nullptr};
+  int32_t* d_est_list[2] = {nullptr, nullptr}; // rows held by each temporary output
+  int64_t est_count[2] = {0, 0};
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[sg::kPhaseSlots];
   double phase_ms[sg::kPhaseSlots] = {0};
   int64_t phase_n[sg::kPhaseSlots] = {0};

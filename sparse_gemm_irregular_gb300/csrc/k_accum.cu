@@ -37,6 +37,8 @@ struct AccParams {
   Sink sink;
   uint32_t* err;
   int has_vals;        // chunk source carries values
+  EstSink est;         // estimated workflows: capacities and the temporary output (numeric rows)
+  int est_on;
 };
 
 template <bool WARP>
@@ -78,7 +80,7 @@ struct Smem {
   int64_t* bstart;   // [batch] first B index of the staged entries
   int32_t* incl;     // [batch] inclusive prefix of their B row lengths (a light row has at most
                      //         tau products, far below 2^31)
-  int64_t* tmp;      // [33] scan scratch
+  int64_t* tmp;      // [34] scan scratch; word 33: overflow flag of the estimated workflows
   double* vals;      // [slots] (numeric)
   int32_t* keys;     // [slots] hash keys, or dense bitmap words
 };
@@ -89,7 +91,7 @@ __host__ __device__ inline int batch_of(int size) { return size < kMaxBatch ? si
 
 __host__ __device__ inline size_t group_bytes(int64_t slots, int size, bool dense, bool numeric,
                                               bool rows) {
-  size_t b = align16(33 * sizeof(int64_t));
+  size_t b = align16(34 * sizeof(int64_t));
   if (rows) b += align16(batch_of(size) * (sizeof(double) + sizeof(int64_t) + sizeof(int32_t)));
   if (numeric) b += align16(static_cast<size_t>(slots) * sizeof(double));
   b += dense ? align16(((slots + 31) / 32) * sizeof(int32_t))
@@ -101,7 +103,7 @@ __device__ __forceinline__ Smem carve(char* p, int64_t slots, int size, bool den
                                       bool rows) {
   Smem s;
   s.tmp = reinterpret_cast<int64_t*>(p);
-  p += align16(33 * sizeof(int64_t));
+  p += align16(34 * sizeof(int64_t));
   if (rows) {
     const int nb = batch_of(size);
     s.av = reinterpret_cast<double*>(p);
@@ -176,10 +178,12 @@ __device__ __forceinline__ void acc_clear(const Group<WARP>& g, const Smem& s, i
 
 // ---- sources -----------------------------------------------------------------------------
 // Expand row `row` of A*B into the accumulator; returns this thread's count of new columns.
+// `ierr` receives hash-table overflows: the global error word, or (estimated workflows) the
+// row's own flag, which also ends the expansion early.
 template <bool WARP, bool NUMERIC, bool DENSE>
 __device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& s,
                                               const AccParams& p, int64_t row, int32_t base,
-                                              uint32_t slots) {
+                                              uint32_t slots, uint32_t* ierr) {
   int64_t fresh = 0;
   const int64_t a0 = p.arp[row], a1 = p.arp[row + 1];
   const int nb = batch_of(g.size);
@@ -202,6 +206,7 @@ __device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& 
     // kExpandUnroll products per thread per step: their B loads are all issued before the
     // first accumulator update, so each thread keeps several L2 requests in flight
     for (int f0 = g.lane; f0 < total; f0 += kExpandUnroll * g.size) {
+      if (ierr != p.err && *reinterpret_cast<volatile uint32_t*>(ierr) != 0u) break;  // row overflowed
       int32_t col[kExpandUnroll];
       double bv[kExpandUnroll], av[kExpandUnroll];
 #pragma unroll
@@ -232,7 +237,7 @@ __device__ __forceinline__ int64_t expand_row(const Group<WARP>& g, const Smem& 
         if (col[u] == kEmptyKey) continue;
         const double v = NUMERIC ? av[u] * bv[u] : 0.0;
         if (DENSE) fresh += dense_insert<NUMERIC>(s, slots, col[u] - base, v, p.err);
-        else fresh += hash_insert<NUMERIC>(s, slots, col[u], v, p.err);
+        else fresh += hash_insert<NUMERIC>(s, slots, col[u], v, ierr);
       }
     }
     g.sync();
@@ -572,13 +577,16 @@ __global__ void __launch_bounds__(1024) k_accum(AccParams p) {
     grow = p.list[item];
     if (DENSE) acc_base = p.span_lo[grow];
   }
-  if (NUMERIC && (grow < p.sink.row_begin || grow >= p.sink.row_end)) return;
+  const bool est = !CHUNK && NUMERIC && p.est_on;
+  if (NUMERIC && !est && (grow < p.sink.row_begin || grow >= p.sink.row_end)) return;
 
+  uint32_t* const flag = reinterpret_cast<uint32_t*>(s.tmp + 33);
+  if (g.lane == 0) *flag = 0u;
   acc_clear<WARP, NUMERIC, DENSE>(g, s, p.slots);
   g.sync();
   int64_t fresh;
   if (CHUNK) fresh = expand_chunk<WARP, NUMERIC, DENSE>(g, s, p, cstart, ccnt, slots);
-  else fresh = expand_row<WARP, NUMERIC, DENSE>(g, s, p, grow, acc_base, slots);
+  else fresh = expand_row<WARP, NUMERIC, DENSE>(g, s, p, grow, acc_base, slots, est ? flag : p.err);
   g.sync();
   int64_t n;
   group_scan<WARP>(g, fresh, s.tmp, &n);
@@ -587,6 +595,23 @@ __global__ void __launch_bounds__(1024) k_accum(AccParams p) {
       if (CHUNK) p.cs.nnz[q] = n;
       else p.sink.row_nnz[grow] = n;
     }
+    return;
+  }
+  if (est) {
+    // estimated workflows: the row fits its capacity, or it is marked for the fallback pass
+    g.sync();
+    const bool over = *reinterpret_cast<volatile uint32_t*>(flag) != 0u || n > p.est.cap[grow];
+    if (over) {
+      if (g.lane == 0) p.est.est_nnz[grow] = -1;
+      return;  // uniform per group
+    }
+    if (g.lane == 0) {
+      p.est.est_nnz[grow] = n;
+      p.sink.row_nnz[grow] = n;
+    }
+    const int64_t o = p.est.row_tmp[grow];
+    if (DENSE) dense_emit<WARP>(g, s, p.slots, n, acc_base, p.est.tmp_col + o, p.est.tmp_val + o, p.err);
+    else hash_emit<WARP>(g, s, p.slots, n, n, 0, p.est.tmp_col + o, p.est.tmp_val + o, p.err);
     return;
   }
   const int64_t rp0 = p.sink.row_ptr[grow];
@@ -650,9 +675,13 @@ static void dispatch(const AccParams& p, int tpr, bool dense, bool numeric, cuda
 
 void launch_light(const spgemm_csr& A, const spgemm_csr& B, const int32_t* span_lo,
                   const RowJob& job, bool numeric, const Sink& sink, uint32_t* err,
-                  cudaStream_t s) {
+                  cudaStream_t s, const EstSink* est) {
   if (job.count == 0) return;
   AccParams p{};
+  if (est) {
+    p.est = *est;
+    p.est_on = 1;
+  }
   p.arp = A.row_ptr;
   p.acol = A.col_idx;
   p.aval = A.vals;
