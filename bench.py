@@ -227,7 +227,10 @@ def main():
     ap.add_argument("--rmat-scale", type=int, default=0,
                     help="replace the workload by a seeded R-MAT of this scale (small cases for profiling)")
     ap.add_argument("--edge-factor", type=int, default=16)
-    ap.add_argument("--no-variants", action="store_true", help="skip the direct-split variant measurement")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the variant measurements (direct split, upper-bound and estimated light rows)")
+    ap.add_argument("--workflow", type=int, default=0,
+                    help="light-row sizing: 0 exact symbolic, 1 IP upper bound, 2 HyperLogLog, 3 automatic")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -256,9 +259,10 @@ def main():
     dA = sg.DeviceCSR.from_host(A)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
-    timing = sg.options(flags=sg.binding.FLAG_TIMING | args.flags, chunk_width=args.chunk_width, tau=args.tau)
-    plain = (sg.options(flags=args.flags, chunk_width=args.chunk_width, tau=args.tau)
-             if (args.flags or args.chunk_width or args.tau) else None)
+    timing = sg.options(flags=sg.binding.FLAG_TIMING | args.flags, chunk_width=args.chunk_width, tau=args.tau,
+                        workflow=args.workflow)
+    plain = (sg.options(flags=args.flags, chunk_width=args.chunk_width, tau=args.tau, workflow=args.workflow)
+             if (args.flags or args.chunk_width or args.tau or args.workflow) else None)
 
     def step(opts=None, keep=False):
         p = sg.Product(dA, dA, stream=stream, opts=opts)
@@ -334,6 +338,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg_name, "m": A.rows, "nnz_A": A.nnz, "ip_total": ip, "nnz_C": c_nnz,
                    "rows_heavy": st.rows_heavy, "ip_heavy": st.ip_heavy,
+                   "light_rows": ("exact symbolic", "IP upper bound", "HyperLogLog estimate")[st.workflow],
                    "l2": "512 MiB buffer written between timed steps (outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_roofline": {"compulsory_bytes": comp, "frac": hbm_frac, "peak_gbs": peak,
@@ -345,28 +350,34 @@ def main():
         "step_ms": step_ms,
     }
 
-    # the same product on the direct-split path (SPGEMM_FLAG_DIRECT_SPLIT), measured the same way
+    # the same product on other paths, measured the same way: the direct split of level 0
+    # (SPGEMM_FLAG_DIRECT_SPLIT) and the light rows sized by their IP bound or by HyperLogLog
+    # estimates instead of the exact symbolic pass (SPGEMM_WORKFLOW_UPPER_BOUND / _ESTIMATE)
     if not args.no_variants:
-        vopt = sg.options(flags=sg.binding.FLAG_TIMING | sg.binding.FLAG_DIRECT_SPLIT | args.flags,
-                          chunk_width=args.chunk_width, tau=args.tau)
-        for _ in range(2):
-            step(vopt)
-        torch.cuda.synchronize()
-        vms, vph = [], {}
-        for i in range(args.steps):
-            flush.fill_(float(i))
-            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_.record(stream)
-            _, ph = step(vopt)
-            b_.record(stream)
+        result["variants"] = {}
+        for name, vflags, vwf in (("direct_split", sg.binding.FLAG_DIRECT_SPLIT, args.workflow),
+                                  ("upper_bound", 0, sg.binding.WORKFLOW_UPPER_BOUND),
+                                  ("estimate", 0, sg.binding.WORKFLOW_ESTIMATE)):
+            vopt = sg.options(flags=sg.binding.FLAG_TIMING | vflags | args.flags, chunk_width=args.chunk_width,
+                              tau=args.tau, workflow=vwf)
+            for _ in range(2):
+                step(vopt)
             torch.cuda.synchronize()
-            vms.append(a_.elapsed_time(b_))
-            for k_, (ms, n_) in ph.items():
-                vph[k_] = vph.get(k_, 0.0) + ms
-        result["variants"] = {"direct_split": {
-            "value": 2.0 * ip * args.steps * world / (sum(vms) / 1e3) / 1e9, "unit": UNIT,
-            "ms_per_step": sum(vms) / args.steps,
-            "phases_ms_per_step": {k_: v / args.steps for k_, v in vph.items() if v > 0}}}
+            vms, vph = [], {}
+            for i in range(args.steps):
+                flush.fill_(float(i))
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                _, ph = step(vopt)
+                b_.record(stream)
+                torch.cuda.synchronize()
+                vms.append(a_.elapsed_time(b_))
+                for k_, (ms, n_) in ph.items():
+                    vph[k_] = vph.get(k_, 0.0) + ms
+            result["variants"][name] = {
+                "value": 2.0 * ip * args.steps * world / (sum(vms) / 1e3) / 1e9, "unit": UNIT,
+                "ms_per_step": sum(vms) / args.steps,
+                "phases_ms_per_step": {k_: v / args.steps for k_, v in vph.items() if v > 0}}
 
     # end to end through the public API with host buffers
     if not args.no_e2e:

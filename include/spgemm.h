@@ -106,7 +106,7 @@ typedef struct {
  * The light rows' values are therefore read during spgemm_symbolic.  AUTO applies the page's
  * selection: UPPER_BOUND when the average row has fewer than 64 intermediate products, ESTIMATE
  * when the expansion ratio (products per entry of A) and the sampled compression ratio
- * (products per entry of C, from HyperLogLog estimates of 3% of the rows, 600 to 10,000) are
+ * (products per entry of C, from HyperLogLog estimates of 3% of the light rows, 600 to 10,000) are
  * both at least 8, else SYMBOLIC.  Heavy rows always take the exact multisplit path. */
 #define SPGEMM_WORKFLOW_SYMBOLIC 0
 #define SPGEMM_WORKFLOW_UPPER_BOUND 1

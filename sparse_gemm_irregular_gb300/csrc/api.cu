@@ -903,8 +903,10 @@ int ensure_sketch(spgemm_ctx* h) {
 // The workflow of the light rows (Table 1 of the Ocean page for SPGEMM_WORKFLOW_AUTO): the
 // upper bound when the average row has fewer than 64 products; HyperLogLog estimates when the
 // expansion ratio (products per entry of A) and the compression ratio (products per entry of
-// C) of a row sample -- 3% of the rows, at least 600 and at most 10,000, evenly spaced -- are
-// both at least 8; else the exact symbolic pass.
+// C) of a row sample -- 3% of the light rows, at least 600 and at most 10,000, evenly spaced --
+// are both at least 8; else the exact symbolic pass.  The sample holds light rows only: the
+// workflow sizes only those, and a heavy row's sketch merge would be one warp's long serial
+// loop.
 int choose_workflow(spgemm_ctx* h) {
   const int64_t ipt = h->stats.ip_total;
   const double er = h->A.nnz > 0 ? static_cast<double>(ipt) / static_cast<double>(h->A.nnz) : 0.0;
@@ -916,11 +918,12 @@ int choose_workflow(spgemm_ctx* h) {
       wf = SPGEMM_WORKFLOW_UPPER_BOUND;
     } else if (er < 8.0) {
       wf = SPGEMM_WORKFLOW_SYMBOLIC;
-    } else {
+    } else if (h->bin_start[2 * h->lad.n] > 0) {
+      const int64_t nlight = h->bin_start[2 * h->lad.n];  // d_rows[0, nlight): the light rows
       const int64_t want = std::min<int64_t>(
-          h->m, std::max<int64_t>(600, std::min<int64_t>(10000, (3 * h->m + 50) / 100)));
-      std::vector<int32_t> rows(want);
-      for (int64_t j = 0; j < want; ++j) rows[j] = static_cast<int32_t>(j * h->m / want);
+          nlight, std::max<int64_t>(600, std::min<int64_t>(10000, (3 * nlight + 50) / 100)));
+      std::vector<int32_t> rows(want);  // positions in the light list, then row ids
+      for (int64_t j = 0; j < want; ++j) rows[j] = static_cast<int32_t>(j * nlight / want);
       int32_t* d_rows;
       int64_t *d_ipv, *d_capv;
       double* d_est;
@@ -930,6 +933,7 @@ int choose_workflow(spgemm_ctx* h) {
       SG_ALLOC(d_est, double, want);
       SG_TRY(check_cuda(cudaMemcpyAsync(d_rows, rows.data(), sizeof(int32_t) * want, cudaMemcpyHostToDevice, h->st),
                         "copy sample"));
+      launch_gather_rows(h->d_rows, d_rows, want, h->st);
       SG_TRY(ensure_sketch(h));
       launch_hll_rows(h->A, d_rows, want, h->d_ip, h->d_sketch, h->hll_m, h->hll_coef, d_capv, d_est, h->st);
       launch_gather_ip(d_rows, want, h->d_ip, d_ipv, h->st);
@@ -952,6 +956,8 @@ int choose_workflow(spgemm_ctx* h) {
       ws_free(h, d_ipv);
       ws_free(h, d_capv);
       ws_free(h, d_est);
+    } else {
+      wf = SPGEMM_WORKFLOW_SYMBOLIC;  // no light rows to size
     }
   }
   h->workflow = wf;
@@ -1066,9 +1072,16 @@ int est_light(spgemm_ctx* h, int64_t* rp) {
       }
   }
   ws_free(h, off);
+  // the copy-out lists: rows of the warp bins (short), of the block bins (long), fallback rows
+  int wide_level = nl;  // first ladder level served by blocks
+  for (int L = nl - 1; L >= 0; --L)
+    if (h->lad.tpr[L] > 32) wide_level = L;
+  const int64_t split_at = h->bin_start[2 * wide_level];
   h->d_est_list[0] = h->d_rows;
-  h->est_count[0] = nlight;
-  h->est_count[1] = 0;
+  h->est_count[0] = split_at;
+  h->d_est_list[1] = h->d_rows + split_at;
+  h->est_count[1] = nlight - split_at;
+  h->est_count[2] = 0;
   h->stats.rows_overflow = 0;
   if (!est) return SPGEMM_OK;
   // rows that overflowed their estimated slot: a second pass with the IP bound
@@ -1077,15 +1090,17 @@ int est_light(spgemm_ctx* h, int64_t* rp) {
   std::vector<int64_t> os;
   SG_ALLOC(ob, uint8_t, nlight);
   SG_ALLOC(split, int32_t, nlight);
-  launch_overflow_bins(h->d_rows, nlight, h->d_est_nnz, ob, h->st);
-  SG_TRY(split_rows(h, h->d_rows, nlight, ob, 2, split, os));
+  launch_overflow_bins(h->d_rows, nlight, h->d_est_nnz, h->d_bin, 2 * wide_level, ob, h->st);
+  SG_TRY(split_rows(h, h->d_rows, nlight, ob, 3, split, os));
   ws_free(h, ob);
-  const int64_t nover = os[2] - os[1];
+  const int64_t nover = os[3] - os[2];
   h->d_est_list[0] = split;
   h->est_count[0] = os[1];
+  h->d_est_list[1] = split + os[1];
+  h->est_count[1] = os[2] - os[1];
   h->stats.rows_overflow = nover;
   if (nover == 0) return SPGEMM_OK;
-  const int32_t* over = split + os[1];
+  const int32_t* over = split + os[2];
   int64_t* off2;
   SG_ALLOC(off2, int64_t, nover + 1);
   launch_gather_ip(over, nover, h->d_ip, off2, h->st);
@@ -1107,8 +1122,8 @@ int est_light(spgemm_ctx* h, int64_t* rp) {
   SG_ALLOC(h->d_tmp_val[1], double, std::max<int64_t>(total2, 1));
   EstSink es2{h->d_ip, h->d_row_tmp, h->d_tmp_col[1], h->d_tmp_val[1], h->d_est_nnz};
   est_pass(h, obinned, ostart, false, es2, rp);
-  h->d_est_list[1] = obinned;
-  h->est_count[1] = nover;
+  h->d_est_list[2] = obinned;
+  h->est_count[2] = nover;
   return SPGEMM_OK;
 }
 
@@ -1129,9 +1144,9 @@ int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, doubl
   } else {
     fork_light(h);
     PhaseTimer t(h, 10);
-    for (int b = 0; b < 2; ++b)  // light rows: temporary slots -> final positions
-      launch_copy_rows(h->d_est_list[b], h->est_count[b], h->d_row_tmp, h->c_row_ptr, rb, re, h->d_tmp_col[b],
-                       h->d_tmp_val[b], c_col, c_val, h->st);
+    for (int b = 0; b < 3; ++b)  // light rows: temporary slots -> final positions
+      launch_copy_rows(h->d_est_list[b], h->est_count[b], h->d_row_tmp, h->c_row_ptr, rb, re,
+                       h->d_tmp_col[b == 2 ? 1 : 0], h->d_tmp_val[b == 2 ? 1 : 0], c_col, c_val, b > 0, h->st);
   }
   for (auto& hb : h->batches) {
     if (hb.row_hi < rb || hb.row_lo >= re) continue;

@@ -133,15 +133,18 @@ void launch_row_products(const spgemm_csr& A, const spgemm_csr& B, int64_t* ip, 
 // bin[i] = ladder level of val[rows[i]]
 void launch_val_bins(const int32_t* rows, int64_t n, const int64_t* val, const BinRule& rule, uint8_t* bin,
                      cudaStream_t s);
-// bin[i] = 1 if est_nnz[rows[i]] < 0 (the row overflowed its slot), else 0
-void launch_overflow_bins(const int32_t* rows, int64_t n, const int64_t* est_nnz, uint8_t* bin, cudaStream_t s);
+// bin[i] = 2 if est_nnz[rows[i]] < 0 (the row overflowed its slot), else 1 if its create bin is
+// at least wide_from (a block bin), else 0
+void launch_overflow_bins(const int32_t* rows, int64_t n, const int64_t* est_nnz, const uint8_t* create_bin,
+                          int wide_from, uint8_t* bin, cudaStream_t s);
 // dst[rows[i]] = base + off[i]
 void launch_scatter_off(const int32_t* rows, int64_t n, const int64_t* off, int64_t base, int64_t* dst,
                         cudaStream_t s);
-// listed rows inside [row_begin, row_end): temporary slot -> final position
+// listed rows inside [row_begin, row_end): temporary slot -> final position (wide: 32 lanes
+// per row, else 8)
 void launch_copy_rows(const int32_t* rows, int64_t n, const int64_t* row_tmp, const int64_t* row_ptr,
                       int64_t row_begin, int64_t row_end, const int32_t* tcol, const double* tval, int32_t* ccol,
-                      double* cval, cudaStream_t s);
+                      double* cval, bool wide, cudaStream_t s);
 
 // ---- heavy pipeline (k_heavy.cu) ---------------------------------------------------------
 void launch_gather_ip(const int32_t* heavy_rows, int64_t nrows, const int64_t* ip, int64_t* out,
@@ -320,8 +323,10 @@ struct spgemm_ctx {
   int64_t* d_est_nnz = nullptr;// per row: nnz, or -1 (overflowed)
   int32_t* d_tmp_col[2] = {nullptr, nullptr};  // temporary output: first pass, fallback pass
   double* d_tmp_val[2] = {nullptr, nullptr};
-  int32_t* d_est_list[2] = {nullptr, nullptr}; // rows held by each temporary output
-  int64_t est_count[2] = {0, 0};
+  // rows to copy out: rows of the warp bins and of the block bins from the first temporary
+  // output, the fallback rows from the second
+  const int32_t* d_est_list[3] = {nullptr, nullptr, nullptr};
+  int64_t est_count[3] = {0, 0, 0};
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[sg::kPhaseSlots];
   double phase_ms[sg::kPhaseSlots] = {0};
   int64_t phase_n[sg::kPhaseSlots] = {0};

@@ -120,9 +120,11 @@ __global__ void k_val_bins(const int32_t* __restrict__ rows, int64_t n, const in
 }
 
 __global__ void k_overflow_bins(const int32_t* __restrict__ rows, int64_t n, const int64_t* __restrict__ est_nnz,
-                                uint8_t* __restrict__ bin) {
+                                const uint8_t* __restrict__ create_bin, int wide_from, uint8_t* __restrict__ bin) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < n) bin[i] = est_nnz[rows[i]] < 0 ? 1 : 0;
+  if (i >= n) return;
+  const int32_t row = rows[i];
+  bin[i] = est_nnz[row] < 0 ? 2 : (create_bin[row] >= wide_from ? 1 : 0);
 }
 
 __global__ void k_scatter_off(const int32_t* __restrict__ rows, int64_t n, const int64_t* __restrict__ off,
@@ -131,23 +133,25 @@ __global__ void k_scatter_off(const int32_t* __restrict__ rows, int64_t n, const
   if (i < n) dst[rows[i]] = base + off[i];
 }
 
-// One warp per listed row: rows inside [row_begin, row_end) move from their temporary slot to
-// their final position (row_ptr[row] - row_ptr[row_begin]); the copy is coalesced.
+// Rows inside [row_begin, row_end) move from their temporary slot to their final position
+// (row_ptr[row] - row_ptr[row_begin]), LANES lanes per listed row: 8 for the rows of the warp
+// bins (short rows still fill the warp), 32 for the rows of the block bins (long rows).
+template <int LANES>
 __global__ void __launch_bounds__(256) k_copy_rows(const int32_t* __restrict__ rows, int64_t n,
                                                    const int64_t* __restrict__ row_tmp,
                                                    const int64_t* __restrict__ row_ptr, int64_t row_begin,
                                                    int64_t row_end, const int32_t* __restrict__ tcol,
                                                    const double* __restrict__ tval, int32_t* __restrict__ ccol,
                                                    double* __restrict__ cval) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * 8 + w;
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / LANES;
+  const int gl = threadIdx.x % LANES;
   if (i >= n) return;
   const int64_t row = rows[i];
   if (row < row_begin || row >= row_end) return;
   const int64_t d = row_ptr[row] - row_ptr[row_begin];
   const int64_t len = row_ptr[row + 1] - row_ptr[row];
   const int64_t src = row_tmp[row];
-  for (int64_t j = lane; j < len; j += 32) {
+  for (int64_t j = gl; j < len; j += LANES) {
     ccol[d + j] = tcol[src + j];
     cval[d + j] = tval[src + j];
   }
@@ -204,10 +208,12 @@ void launch_val_bins(const int32_t* rows, int64_t n, const int64_t* val, const B
   k_val_bins<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(rows, n, val, rule, bin);
 }
 
-void launch_overflow_bins(const int32_t* rows, int64_t n, const int64_t* est_nnz, uint8_t* bin, cudaStream_t s) {
+void launch_overflow_bins(const int32_t* rows, int64_t n, const int64_t* est_nnz, const uint8_t* create_bin,
+                          int wide_from, uint8_t* bin, cudaStream_t s) {
   if (n == 0) return;
   note_launch();
-  k_overflow_bins<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(rows, n, est_nnz, bin);
+  k_overflow_bins<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(rows, n, est_nnz, create_bin, wide_from,
+                                                                          bin);
 }
 
 void launch_scatter_off(const int32_t* rows, int64_t n, const int64_t* off, int64_t base, int64_t* dst,
@@ -219,11 +225,15 @@ void launch_scatter_off(const int32_t* rows, int64_t n, const int64_t* off, int6
 
 void launch_copy_rows(const int32_t* rows, int64_t n, const int64_t* row_tmp, const int64_t* row_ptr,
                       int64_t row_begin, int64_t row_end, const int32_t* tcol, const double* tval, int32_t* ccol,
-                      double* cval, cudaStream_t s) {
+                      double* cval, bool wide, cudaStream_t s) {
   if (n == 0) return;
   note_launch();
-  k_copy_rows<<<static_cast<unsigned>(ceil_div(n, 8)), 256, 0, s>>>(rows, n, row_tmp, row_ptr, row_begin, row_end,
-                                                                     tcol, tval, ccol, cval);
+  if (wide)
+    k_copy_rows<32><<<static_cast<unsigned>(ceil_div(n, 8)), 256, 0, s>>>(rows, n, row_tmp, row_ptr, row_begin,
+                                                                          row_end, tcol, tval, ccol, cval);
+  else
+    k_copy_rows<8><<<static_cast<unsigned>(ceil_div(n, 32)), 256, 0, s>>>(rows, n, row_tmp, row_ptr, row_begin,
+                                                                          row_end, tcol, tval, ccol, cval);
 }
 
 }  // namespace sg
