@@ -10,7 +10,11 @@
 //               to numeric when the whole heavy part fits one batch ("resident"), otherwise
 //               it is recomputed batch by batch (the device cannot hold C^ of every heavy row
 //               of the largest products).  numeric_rows computes a row window;
-//               numeric_host streams row windows into host memory.
+//               numeric_host streams row windows into host memory.  A repeated numeric call
+//               replays a CUDA graph captured on its second occurrence.
+//   light-row workflows (Ocean page, Table 1): the exact symbolic pass above, or the light rows
+//               accumulated during symbolic into slots sized by their IP bound or by HyperLogLog
+//               estimates (with a fallback pass for rows that overflow), copied out in numeric.
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
