@@ -269,6 +269,20 @@ int spgemm_destroy(spgemm_handle h);
 int spgemm_hll_estimate(const spgemm_csr* A, const spgemm_csr* B, int32_t registers, double coef,
                         int64_t* cap, void* stream);
 
+/* Markov-clustering step after the expansion C = M * M (Trident page, section 5.7): normalize
+ * the columns of C, prune the entries below `threshold`, square the remaining entries.  An
+ * entry (i, j) is kept when C[i,j] / colsum_j >= threshold; its new value is
+ * (C[i,j] / colsum_j)^2; rows keep C's column order.  C is device CSR (any row order inside
+ * rows).  Symbolic part: writes col_sums (device, C.cols doubles; fp64 sums, order not fixed),
+ * out_row_ptr (device, C.rows + 1) and *out_nnz (host); synchronises `stream`.  Numeric part:
+ * writes out_col / out_val (device, *out_nnz entries, caller-owned) at out_row_ptr, using the
+ * col_sums of the symbolic part.  Errors: INVALID_ARG (null pointers, threshold < 0),
+ * OUT_OF_MEMORY (scan scratch), CUDA. */
+int spgemm_mcl_prune_symbolic(const spgemm_csr* C, double threshold, double* col_sums, int64_t* out_row_ptr,
+                              int64_t* out_nnz, void* stream);
+int spgemm_mcl_prune_numeric(const spgemm_csr* C, double threshold, const double* col_sums,
+                             const int64_t* out_row_ptr, int32_t* out_col, double* out_val, void* stream);
+
 int spgemm_symbolic_noalloc(int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
                             const spgemm_csr* B, int64_t* c_row_ptr, int64_t* c_nnz, void* stream);
 

@@ -10,7 +10,8 @@ from dataclasses import dataclass
 
 from . import binding
 from .binding import (SpgemmError, load, options, spgemm_create, spgemm_destroy, spgemm_get_phase_times,
-                      spgemm_hll_estimate, spgemm_numeric_host,
+                      spgemm_hll_estimate, spgemm_mcl_prune_numeric, spgemm_mcl_prune_symbolic,
+                      spgemm_numeric_host,
                       spgemm_get_plan, spgemm_get_stats, spgemm_kernel_launches, spgemm_last_error, spgemm_numeric,
                       spgemm_numeric_rows, spgemm_plan_params, spgemm_release_memory, spgemm_strerror,
                       spgemm_symbolic)
@@ -18,6 +19,7 @@ from .binding import (SpgemmError, load, options, spgemm_create, spgemm_destroy,
 __all__ = [
     "DeviceCSR", "multiply", "Product", "SpgemmError", "load", "options", "spgemm_create",
     "spgemm_destroy", "spgemm_get_phase_times", "spgemm_get_plan", "spgemm_get_stats", "spgemm_hll_estimate",
+    "spgemm_mcl_prune_symbolic", "spgemm_mcl_prune_numeric", "mcl_iteration",
     "spgemm_kernel_launches",
     "spgemm_last_error", "spgemm_numeric", "spgemm_numeric_rows", "spgemm_plan_params",
     "spgemm_release_memory",
@@ -135,3 +137,27 @@ def multiply(A: DeviceCSR, B: DeviceCSR, stream=None, opts=None) -> DeviceCSR:
     finally:
         p.close()
     return DeviceCSR(A.rows, B.cols, row_ptr, col, val)
+
+
+def mcl_iteration(M: DeviceCSR, threshold: float = 0.002, stream=None, opts=None) -> DeviceCSR:
+    """One Markov-clustering iteration (Trident page, section 5.7): the expansion M * M on the
+    library's SpGEMM, then column normalization, pruning below ``threshold`` and the element-wise
+    square, all on the device.  Returns the new matrix."""
+    import torch
+    p = Product(M, M, stream=stream, opts=opts)
+    try:
+        p.symbolic()
+        col, val = p.numeric()
+        C = DeviceCSR(M.rows, M.cols, p.row_ptr, col, val)
+    finally:
+        p.close()
+    dev = M.row_ptr.device
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    sums = torch.empty(max(M.cols, 1), dtype=torch.float64, device=dev)
+    rp = torch.empty(M.rows + 1, dtype=torch.int64, device=dev)
+    cd = C.desc()
+    nnz = spgemm_mcl_prune_symbolic(cd, threshold, sums.data_ptr(), rp.data_ptr(), st)
+    oc = torch.empty(max(nnz, 1), dtype=torch.int32, device=dev)
+    ov = torch.empty(max(nnz, 1), dtype=torch.float64, device=dev)
+    spgemm_mcl_prune_numeric(cd, threshold, sums.data_ptr(), rp.data_ptr(), oc.data_ptr(), ov.data_ptr(), st)
+    return DeviceCSR(M.rows, M.cols, rp, oc[:nnz], ov[:nnz])

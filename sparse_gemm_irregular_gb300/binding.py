@@ -82,6 +82,8 @@ EXPORTS = {
     "spgemm_kernel_launches": (ctypes.c_longlong, []),
     "spgemm_symbolic_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "spgemm_hll_estimate": (ctypes.c_int, [_vp, _vp, _i32, ctypes.c_double, _vp, _vp]),
+    "spgemm_mcl_prune_symbolic": (ctypes.c_int, [_vp, ctypes.c_double, _vp, _vp, _vp, _vp]),
+    "spgemm_mcl_prune_numeric": (ctypes.c_int, [_vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp]),
     "spgemm_release_memory": (ctypes.c_int, []),
     "spgemm_destroy": (ctypes.c_int, [_vp]),
     "spgemm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -199,6 +201,20 @@ def spgemm_hll_estimate(A: spgemm_csr, B: spgemm_csr, registers: int, coef: floa
     """HyperLogLog capacity of every row of A*B into the device array ``cap`` (see spgemm.h)."""
     _check(load().spgemm_hll_estimate(ctypes.byref(A), ctypes.byref(B), registers, coef, _vp(cap), _vp(stream)),
            "spgemm_hll_estimate")
+
+
+def spgemm_mcl_prune_symbolic(C: spgemm_csr, threshold: float, col_sums: int, out_row_ptr: int, stream: int = 0) -> int:
+    """Column sums and the pruned row offsets of a Markov-clustering step; returns the pruned nnz."""
+    nnz = _i64(0)
+    _check(load().spgemm_mcl_prune_symbolic(ctypes.byref(C), threshold, _vp(col_sums), _vp(out_row_ptr),
+                                            ctypes.byref(nnz), _vp(stream)), "spgemm_mcl_prune_symbolic")
+    return nnz.value
+
+
+def spgemm_mcl_prune_numeric(C: spgemm_csr, threshold: float, col_sums: int, out_row_ptr: int, out_col: int,
+                             out_val: int, stream: int = 0):
+    _check(load().spgemm_mcl_prune_numeric(ctypes.byref(C), threshold, _vp(col_sums), _vp(out_row_ptr),
+                                           _vp(out_col), _vp(out_val), _vp(stream)), "spgemm_mcl_prune_numeric")
 
 
 def spgemm_destroy(h):

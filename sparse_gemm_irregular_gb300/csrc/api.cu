@@ -1716,6 +1716,49 @@ int spgemm_get_phase_times(spgemm_handle h, double* t, int64_t* launches, int32_
 
 long long spgemm_kernel_launches(void) { return launch_count(); }
 
+namespace {
+bool csr_ok(const spgemm_csr* C) {
+  return C && C->rows >= 0 && C->cols >= 0 && C->nnz >= 0 && C->row_ptr && (C->nnz == 0 || (C->col_idx && C->vals));
+}
+}  // namespace
+
+int spgemm_mcl_prune_symbolic(const spgemm_csr* C, double threshold, double* col_sums, int64_t* out_row_ptr,
+                              int64_t* out_nnz, void* stream) {
+  g_last_error.clear();
+  if (!csr_ok(C) || !out_row_ptr || !out_nnz || (C->cols > 0 && !col_sums) || !(threshold >= 0.0))
+    return SPGEMM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (C->cols > 0) cudaMemsetAsync(col_sums, 0, sizeof(double) * C->cols, st);
+  launch_col_sums(*C, col_sums, st);
+  cudaMemsetAsync(out_row_ptr, 0, sizeof(int64_t) * (C->rows + 1), st);
+  launch_keep_count(*C, col_sums, threshold, out_row_ptr, st);
+  int64_t* scratch = nullptr;
+  const int64_t need = std::max<int64_t>(scan_scratch_elems(C->rows), 1);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), sizeof(int64_t) * need, st) != cudaSuccess) {
+    cudaGetLastError();
+    set_last_error("scan scratch allocation failed");
+    return SPGEMM_ERR_OUT_OF_MEMORY;
+  }
+  scan_excl_i64(out_row_ptr, out_row_ptr, C->rows, scratch, st);
+  cudaFreeAsync(scratch, st);
+  int64_t nnz = 0;
+  SG_TRY(check_cuda(cudaMemcpyAsync(&nnz, out_row_ptr + C->rows, sizeof(int64_t), cudaMemcpyDeviceToHost, st),
+                    "copy pruned nnz"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(st), "mcl prune symbolic"));
+  *out_nnz = nnz;
+  return SPGEMM_OK;
+}
+
+int spgemm_mcl_prune_numeric(const spgemm_csr* C, double threshold, const double* col_sums,
+                             const int64_t* out_row_ptr, int32_t* out_col, double* out_val, void* stream) {
+  g_last_error.clear();
+  if (!csr_ok(C) || !out_row_ptr || (C->nnz > 0 && (!col_sums || !out_col || !out_val)) || !(threshold >= 0.0))
+    return SPGEMM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  launch_keep_write(*C, col_sums, threshold, out_row_ptr, out_col, out_val, st);
+  return check_cuda(cudaGetLastError(), "mcl prune numeric");
+}
+
 int spgemm_hll_estimate(const spgemm_csr* A, const spgemm_csr* B, int32_t registers, double coef, int64_t* cap,
                         void* stream) {
   g_last_error.clear();

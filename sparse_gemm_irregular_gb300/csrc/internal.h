@@ -146,6 +146,12 @@ void launch_copy_rows(const int32_t* rows, int64_t n, const int64_t* row_tmp, co
                       int64_t row_begin, int64_t row_end, const int32_t* tcol, const double* tval, int32_t* ccol,
                       double* cval, bool wide, cudaStream_t s);
 
+// ---- Markov-clustering step (k_mcl.cu) -----------------------------------------------------
+void launch_col_sums(const spgemm_csr& C, double* sums, cudaStream_t s);  // sums zeroed by the caller
+void launch_keep_count(const spgemm_csr& C, const double* sums, double thr, int64_t* counts, cudaStream_t s);
+void launch_keep_write(const spgemm_csr& C, const double* sums, double thr, const int64_t* out_rp, int32_t* out_col,
+                       double* out_val, cudaStream_t s);
+
 // ---- heavy pipeline (k_heavy.cu) ---------------------------------------------------------
 void launch_gather_ip(const int32_t* heavy_rows, int64_t nrows, const int64_t* ip, int64_t* out,
                       cudaStream_t s);

@@ -124,6 +124,24 @@ def csr_from_coo(rows: int, cols: int, r: np.ndarray, c: np.ndarray, v: np.ndarr
     return CSR(rows, cols, rp, cc, np.ascontiguousarray(v, dtype=np.float64))
 
 
+def transpose(m: CSR) -> CSR:
+    """The transpose as CSR (input preparation for products such as A * A^T)."""
+    r = np.repeat(np.arange(m.rows, dtype=np.int64), np.diff(m.row_ptr))
+    return csr_from_coo(m.cols, m.rows, m.col.astype(np.int64), r.astype(np.int32), m.val)
+
+
+def aggregation(n: int, coarse: int, seed: int = 0, per_row: int = 1) -> CSR:
+    """n x coarse restriction-style operator: row i has ``per_row`` distinct columns drawn from
+    [0, coarse), values 1 / per_row (a tall, skinny B for rectangular products A * R)."""
+    cols = np.empty((n, per_row), dtype=np.int64)
+    for j in range(per_row):
+        cols[:, j] = (draws(seed, 11 + j, 0, n) % np.uint64(coarse)).astype(np.int64)
+    r = np.repeat(np.arange(n, dtype=np.int64), per_row)
+    c = cols.reshape(-1)
+    m = csr_from_coo(n, coarse, r, c.astype(np.int32), np.full(n * per_row, 1.0 / per_row), merge=True)
+    return m
+
+
 def uniform_rows(n: int, per_row: int, seed: int = 0, lo: float = -1.0, hi: float = 1.0) -> CSR:
     """n x n, exactly ``per_row`` distinct columns per row chosen uniformly by Floyd's
     algorithm, columns stored sorted, values U[lo, hi)."""

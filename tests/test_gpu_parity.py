@@ -344,3 +344,25 @@ def test_numeric_repeat_graph(gpu_lib, case):
         compare_full(A, A, rp.cpu().numpy(), col2.cpu().numpy()[:nnz], val2.cpu().numpy()[:nnz])
     finally:
         p.close()
+
+
+@pytest.mark.parametrize("case", ["rmat_pair", "a_times_r", "a_times_r_heavy", "a_times_at"])
+def test_general_products(gpu_lib, case):
+    """Products beyond C = A*A: an R-MAT pair A*B with B != A, a rectangular A*R with a tall
+    aggregation operator R, and A*A^T of a rectangular A (heavy path forced on small inputs)."""
+    kw = None
+    if case == "rmat_pair":
+        A, B = synth.rmat(13, 16, seed=1), synth.rmat(13, 16, seed=2)
+    elif case.startswith("a_times_r"):
+        A = synth.rmat(13, 16, seed=3)
+        B = synth.aggregation(A.cols, 700, seed=4, per_row=2)
+        if case.endswith("heavy"):
+            kw = dict(tau=64, chunk_width=64, chunks_max=4)
+    else:
+        A = synth.random_sparse(3000, 5000, 0.004, 6, duplicates=True, empty_rows=True, sort_rows=False)
+        B = synth.transpose(A)
+        kw = dict(tau=128, chunk_width=256)
+    rp, col, val, st = gpu_product(A, B, opts(**kw) if kw else None)
+    compare_full(A, B, rp, col, val, threads=16)
+    if kw:
+        assert st.rows_heavy > 0

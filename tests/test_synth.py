@@ -75,3 +75,17 @@ def test_mcl_column_stochastic():
     assert np.allclose(s, 1.0, rtol=0, atol=1e-12)
     diag = [i in set(M.row(i)[0].tolist()) for i in range(M.rows)]
     assert all(diag)
+
+
+def test_transpose_and_aggregation_helpers():
+    A = synth.random_sparse(30, 40, 0.1, 1, duplicates=True)
+    T = synth.transpose(A)
+    assert (T.rows, T.cols, T.nnz) == (A.cols, A.rows, A.nnz)
+    d = np.zeros((A.rows, A.cols))
+    np.add.at(d, (np.repeat(np.arange(A.rows), np.diff(A.row_ptr)), A.col), A.val)
+    dt = np.zeros((T.rows, T.cols))
+    np.add.at(dt, (np.repeat(np.arange(T.rows), np.diff(T.row_ptr)), T.col), T.val)
+    assert np.array_equal(d.T, dt)
+    R = synth.aggregation(100, 10, seed=2, per_row=2)
+    R.check()
+    assert R.rows == 100 and R.cols == 10 and np.all(np.diff(R.row_ptr) >= 1)
