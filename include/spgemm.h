@@ -71,6 +71,11 @@ extern "C" {
                                          C^_reord (counts from per-B-row chunk histograms), so C^
                                          is never stored and level 0 needs no multisplit pass */
 #define SPGEMM_FLAG_NO_GRAPH 2048    /* never capture or replay the numeric phase as a CUDA graph */
+#define SPGEMM_FLAG_NO_ESC 4096      /* light hash rows with at most 64 intermediate products
+                                        use the shared-memory hash table like longer rows, instead
+                                        of the default expand-sort-compact accumulator held in one
+                                        warp's registers (exact symbolic workflow; narrow rows
+                                        always take the shortened dense accumulator) */
 
 /* A CSR matrix in device memory, borrowed by the library (never written or freed). */
 typedef struct {

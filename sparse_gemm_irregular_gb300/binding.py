@@ -29,6 +29,7 @@ FLAG_DIRECT_SPLIT = 256
 FLAG_TMA_SPLIT = 512
 FLAG_FUSED_HIST = 1024
 FLAG_NO_GRAPH = 2048
+FLAG_NO_ESC = 4096
 WORKFLOW_SYMBOLIC, WORKFLOW_UPPER_BOUND, WORKFLOW_ESTIMATE, WORKFLOW_AUTO = 0, 1, 2, 3
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",

@@ -800,8 +800,8 @@ void join_light(spgemm_ctx* h) {
 // that phase's synchronisation; `starts` null: a synchronous pass of its own.
 int numeric_bins_enqueue(spgemm_ctx* h, const int64_t* c_row_ptr, int64_t* starts_host) {
   const int nl = h->lad.n;
-  int64_t nh = 0;
-  for (int L = 0; L < nl; ++L) nh += h->bin_start[2 * L + 1] - h->bin_start[2 * L];
+  int64_t nh = 0;  // hash rows outside the ESC levels (those keep their IP lists)
+  for (int L = h->esc_levels; L < nl; ++L) nh += h->bin_start[2 * L + 1] - h->bin_start[2 * L];
   if (nh == 0) {
     h->nbin_start.assign(nl + 1, 0);
     return SPGEMM_OK;
@@ -816,7 +816,7 @@ int numeric_bins_enqueue(spgemm_ctx* h, const int64_t* c_row_ptr, int64_t* start
   SG_ALLOC(cnt, int64_t, nl * nblk + 1);
   SG_ALLOC(starts, int64_t, nl + 1);
   int64_t off = 0;
-  for (int L = 0; L < nl; ++L) {
+  for (int L = h->esc_levels; L < nl; ++L) {
     const int64_t c = h->bin_start[2 * L + 1] - h->bin_start[2 * L];
     if (c) cudaMemcpyAsync(all + off, h->d_rows + h->bin_start[2 * L], sizeof(int32_t) * c, cudaMemcpyDeviceToDevice,
                            h->st);
@@ -856,6 +856,13 @@ void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
   for (int L = 0; L < h->lad.n; ++L) {
     for (int d = 0; d < 2; ++d) {
       const int b = 2 * L + d;
+      // short hash rows (IP lists): expand-sort-compact in registers; short rows of narrow span
+      // keep the shortened dense accumulator, which measured faster for them
+      const bool esc = L < h->esc_levels && d == 0;
+      if (esc)
+        launch_esc(h->A, h->B, h->d_rows + h->bin_start[b], h->bin_start[b + 1] - h->bin_start[b], numeric, sk,
+                   h->d_err, h->st_light);
+      if (esc && !numeric) continue;  // numeric: the rows binned here by nnz still follow
       RowJob job;
       if (numeric && d == 0) {  // hash rows: numeric bins by exact size
         job.rows = h->d_nrows + h->nbin_start[L];
@@ -1385,6 +1392,8 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
   h->rule.all_light = (h->opt.flags & SPGEMM_FLAG_ALL_LIGHT) ? 1 : 0;
   h->rule.no_dense = (h->opt.flags & SPGEMM_FLAG_NO_DENSE_LIGHT) ? 1 : 0;
   h->nbins = 2 * h->lad.n + 1;
+  if (!(h->opt.flags & SPGEMM_FLAG_NO_ESC))
+    while (h->esc_levels < h->lad.n && h->lad.upper[h->esc_levels] <= esc_max_products()) ++h->esc_levels;
 
   PhaseTimer* tsetup = new PhaseTimer(h, 0);
   h->d_err = static_cast<uint32_t*>(ws_alloc(h, sizeof(uint32_t)));

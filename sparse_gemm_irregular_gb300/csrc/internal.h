@@ -119,6 +119,11 @@ void launch_chunks(const ChunkSet& cs, const int32_t* list, int64_t count, int64
                    bool dense, int64_t dense_width, bool numeric, const Sink& sink,
                    uint32_t* err, cudaStream_t s);
 size_t light_smem_bytes(int64_t slots, int tpr, bool dense, bool numeric);
+// expand-sort-compact rows of at most esc_max_products() products (k_esc.cu): symbolic writes
+// sink.row_nnz, numeric writes the sorted row at its final position
+int64_t esc_max_products();
+void launch_esc(const spgemm_csr& A, const spgemm_csr& B, const int32_t* rows, int64_t n, bool numeric,
+                const Sink& sink, uint32_t* err, cudaStream_t s);
 
 // ---- estimated light-row sizing (k_estimate.cu) ------------------------------------------
 bool hll_registers_ok(int m);
@@ -318,6 +323,8 @@ struct spgemm_ctx {
   long long num_launches = 0;  // kernel launches the graph holds
   bool capturing = false;      // ws_alloc refuses while a capture is open
   bool last_graph = false;     // the last numeric call ran from the graph
+
+  int esc_levels = 0;           // ladder levels whose light rows take the ESC accumulator
 
   // light rows sized by their IP bound or by HyperLogLog estimates (SPGEMM_WORKFLOW_*)
   int workflow = 0;            // the workflow the symbolic phase ran

@@ -53,6 +53,9 @@ FORCED = [
     # level-0 histogram counted per product inside the outer product
     dict(flags=1024, tau=16, chunk_width=32, chunks_max=4),
     dict(flags=1024 | 16, tau=8, chunk_width=32, chunks_max=2, heavy_batch_elems=700),
+    # short hash rows in the shared hash tables instead of expand-sort-compact
+    dict(flags=4096),
+    dict(flags=4096 | 2 | 4, tau=4096),
 ]
 
 
@@ -80,12 +83,13 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
     row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
     full (multisplit path, plain shared atomics in the multisplit, dense chunks in L2, direct
-    split, bulk-copy staged multisplit, per-product level-0 histogram)."""
+    split, bulk-copy staged multisplit, per-product level-0 histogram, short hash rows in
+    shared hash tables instead of expand-sort-compact)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
     assert st.rows_heavy > 0 and st.rows_light > 0 and st.dense_elems > 0
@@ -366,3 +370,32 @@ def test_general_products(gpu_lib, case):
     compare_full(A, B, rp, col, val, threads=16)
     if kw:
         assert st.rows_heavy > 0
+
+
+@pytest.mark.parametrize("case", ["config1", "band", "random_dup", "long_a_rows"])
+def test_esc_short_rows(gpu_lib, case):
+    """Expand-sort-compact (the default for hash rows of at most 64 products) against the hash
+    tables: config 1 (64 per row), a band (49, shortened dense either way),
+    duplicates and empty rows, and rows of A longer than a warp whose B rows are mostly empty
+    (several staged chunks per row)."""
+    if case == "config1":
+        A = B = synth.config(1)
+    elif case == "band":
+        A = B = synth.banded(20000, 3, seed=2)
+    elif case == "random_dup":
+        A = synth.random_sparse(400, 300, 0.02, 7, duplicates=True, empty_rows=True, sort_rows=False)
+        B = synth.random_sparse(300, 500, 0.01, 8, duplicates=True, empty_rows=True)
+    else:
+        from synth import CSR
+        A = synth.random_sparse(200, 3000, 0.03, 9, duplicates=True)     # ~90 entries per row
+        Bf = synth.random_sparse(3000, 400, 0.004, 10)
+        keep = np.zeros(3000, dtype=bool)
+        keep[::40] = True                                               # most B rows empty
+        lens = np.diff(Bf.row_ptr) * keep
+        rp = np.zeros(3001, np.int64)
+        np.cumsum(lens, out=rp[1:])
+        sel = np.repeat(keep, np.diff(Bf.row_ptr))
+        B = CSR(3000, 400, rp, Bf.col[sel], Bf.val[sel])
+    for kw in (None, opts(flags=4096)):  # expand-sort-compact (default), and hash tables
+        rp, col, val, st = gpu_product(A, B, kw)
+        compare_full(A, B, rp, col, val, threads=8)
