@@ -71,7 +71,10 @@ __global__ void __launch_bounds__(256) k_keep_write(const int64_t* __restrict__ 
 
 void launch_col_sums(const spgemm_csr& C, double* sums, cudaStream_t s) {
   if (C.nnz == 0) return;
-  const int64_t blocks = std::min<int64_t>(ceil_div(C.nnz, 256), 152 * 32);
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = std::min<int64_t>(ceil_div(C.nnz, 256), static_cast<int64_t>(sms) * 8);  // grid-stride
   note_launch();
   k_col_sums<<<static_cast<unsigned>(blocks), 256, 0, s>>>(C.col_idx, C.vals, C.nnz, sums);
 }
