@@ -34,6 +34,22 @@ METRIC = "SpGEMM GFLOP/s (2 x intermediate products / s), 1 x GB300"
 UNIT = "GFLOP/s"
 
 
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest value over the ranks (the slowest replica's time); x itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ip_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job GFLOP/s: every rank's replica does 2 * IP flops per step."""
+    return 2.0 * ip_per_step * steps * world / seconds / 1e9
+
+
 def compulsory_bytes(A, B, c_nnz: int) -> int:
     """bytes(A) + bytes(rows of B that A touches) + bytes(C); bytes(X) = (rows+1)*8 + 12*nnz."""
     touched = np.zeros(B.rows, dtype=bool)
@@ -302,15 +318,11 @@ def main():
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    t_total = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([t_total], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_total = float(t.item())
+    t_total = max_over_ranks(sum(step_ms) / 1e3, world)
 
     ip = st.ip_total
     c_nnz = st.c_nnz
-    value = 2.0 * ip * args.steps * world / t_total / 1e9
+    value = job_rate(ip, args.steps, world, t_total)
     ms_per_step = t_total / args.steps * 1e3
     peak, peak_src = load_peaks()
     comp = compulsory_bytes(A, A, c_nnz)
@@ -374,9 +386,10 @@ def main():
                 vms.append(a_.elapsed_time(b_))
                 for k_, (ms, n_) in ph.items():
                     vph[k_] = vph.get(k_, 0.0) + ms
+            vt = max_over_ranks(sum(vms) / 1e3, world)
             result["variants"][name] = {
-                "value": 2.0 * ip * args.steps * world / (sum(vms) / 1e3) / 1e9, "unit": UNIT,
-                "ms_per_step": sum(vms) / args.steps,
+                "value": job_rate(ip, args.steps, world, vt), "unit": UNIT,
+                "ms_per_step": vt * 1e3 / args.steps,
                 "phases_ms_per_step": {k_: v / args.steps for k_, v in vph.items() if v > 0}}
 
     # end to end through the public API with host buffers
@@ -430,8 +443,8 @@ def e2e(args, A, sg, torch, stream, world):
         d2h = (A.rows + 1) * 8 + nnz * 12
         if i >= warm:
             times.append(t0.elapsed_time(t1) / 1e3)
-    t = sum(times)
-    return {"value": 2.0 * st.ip_total * len(times) * world / t / 1e9, "unit": UNIT,
+    t = max_over_ranks(sum(times), world)
+    return {"value": job_rate(st.ip_total, len(times), world, t), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": len(times), "warmup": warm}
 
 
