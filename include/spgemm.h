@@ -243,24 +243,6 @@ int spgemm_release_memory(void);
 /* Release the workspace (stream-ordered on the handle's stream) and the handle.  NULL is ok. */
 int spgemm_destroy(spgemm_handle h);
 
-/* C.row_ptr and nnz(C) without allocating any device memory.  The paper has no counterpart:
- * this entry point exists for callers that cannot call cudaMalloc (or any allocator) at the
- * point where they need the row sizes of C -- code running inside an allocator or memory
- * manager, loops that forbid allocation after start-up, hosts with a fixed memory budget.
- * Instead of a workspace it uses one static __device__ array of 33,280 bytes that every
- * device which loads this library holds until the process exits.
- *   m, k, n, A, B: as for spgemm_create (A and B in device memory, borrowed);
- *   c_row_ptr:     device, m+1 int64, caller-owned, written with the exclusive scan of the
- *                  distinct column counts of the rows of A*B (identical to spgemm_symbolic);
- *   c_nnz:         host, receives nnz(C);
- *   stream:        cudaStream_t; the call synchronises it before returning.
- * Limits: m <= 16,777,215 rows and at most 2048 intermediate products in every row of A*B;
- * otherwise SPGEMM_ERR_INVALID_ARG (a too-long row is detected on the device, after the
- * kernels ran, and c_row_ptr is then meaningless).  No cudaMalloc, cudaFree or allocating
- * library call is made.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current), so make that first call before any
- * stream capture.  Every call on a device shares the one array: calls that overlap on the
- * GPU (other streams, other host threads) race and give wrong results; serialise them. */
 /* HyperLogLog output-size estimates for every row of C = A * B (Ocean page: HyperLogLog
  * background, construct-and-merge of Figure 3).  One sketch of `registers` (32 or 64) one-byte
  * registers per row of B: a column's 32-bit hash (MurmurHash3 finaliser) picks its register by
@@ -288,6 +270,29 @@ int spgemm_mcl_prune_symbolic(const spgemm_csr* C, double threshold, double* col
 int spgemm_mcl_prune_numeric(const spgemm_csr* C, double threshold, const double* col_sums,
                              const int64_t* out_row_ptr, int32_t* out_col, double* out_val, void* stream);
 
+/* C.row_ptr and nnz(C) without allocating any device memory.  The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc (or any allocator) at the
+ * point where they need the row sizes of C -- code running inside an allocator or memory
+ * manager, loops that forbid allocation after start-up, hosts with a fixed memory budget.
+ * Instead of a workspace it uses one static __device__ array of 33,280 bytes that every
+ * device which loads this library holds until the process exits.
+ *   m, k, n, A, B: as for spgemm_create (A and B in device memory, borrowed);
+ *   c_row_ptr:     device, m+1 int64, caller-owned, written with the exclusive scan of the
+ *                  distinct column counts of the rows of A*B (identical to spgemm_symbolic);
+ *   c_nnz:         host, receives nnz(C);
+ *   stream:        cudaStream_t; the call synchronises it before returning.
+ * Limits: m <= 16,777,215 rows and at most 2048 intermediate products in every row of A*B.
+ * Errors: INVALID_ARG for null pointers, mismatched shapes, more rows than the limit, a row
+ * above the product limit or a row pointer / column index out of range (the last two are
+ * detected on the device after the kernels ran; c_row_ptr is then meaningless); DEVICE when a
+ * row's hash table filled up (not expected within the limits); OVERFLOW for k or n above
+ * 2^31-1; CUDA for a failed runtime call.  No cudaMalloc, cudaFree or allocating library call
+ * is made by the call itself.  With CUDA's lazy module loading, though, the first call on a
+ * device loads this code and its static array into that device's memory and looks up the
+ * array's address (cudaGetSymbolAddress, with that device current): make one warm-up call per
+ * device at start-up (m = 0 is enough), before any stream capture and before entering code
+ * that must not allocate.  Every call on a device shares the one array: calls that overlap on
+ * the GPU (other streams, other host threads) race and give wrong results; serialise them. */
 int spgemm_symbolic_noalloc(int64_t m, int64_t k, int64_t n, const spgemm_csr* A,
                             const spgemm_csr* B, int64_t* c_row_ptr, int64_t* c_nnz, void* stream);
 

@@ -6,7 +6,11 @@
 // allocation after start-up, and hosts that hand the library a fixed memory budget.  The
 // regular spgemm_create / spgemm_symbolic path allocates its workspace (bins, scan scratch,
 // intermediate buffers) with cudaMallocAsync; this entry point instead uses one file-scope
-// __device__ array, reserved once when the library is loaded on a device.
+// __device__ array.  Under CUDA's lazy module loading the array and the four kernels below
+// come into device memory with the first call on each device (that call's symbol lookup and
+// launches load the module), so the first call may itself take device memory: make one
+// warm-up call per device at start-up (m = 0 suffices), before any stream capture and before
+// entering code that must not allocate.  Later calls allocate nothing.
 //
 // Scope and limits:
 //   * every row of A*B may have at most kNaMaxRowIP intermediate products (the warp hash
@@ -37,11 +41,19 @@ static __device__ __align__(256) int64_t g_na_scratch[kNaScratchElems];
 
 constexpr uint32_t kNaErrRowTooLong = 1u;
 constexpr uint32_t kNaErrHashFull = 2u;
+constexpr uint32_t kNaErrBounds = 4u;   // a row pointer or column index outside its range
+
+__device__ __forceinline__ void na_flag(int64_t* scratch, uint32_t bit) {
+  atomicOr(reinterpret_cast<unsigned long long*>(&scratch[kNaMaxTiles + 1]), bit);
+}
 
 // One warp per row: distinct columns of row i of A*B, counted in a shared-memory hash.
+// Malformed input (a row pointer outside [0, nnz] or decreasing, a column outside its range)
+// is skipped and flagged, never read past.
 __global__ void __launch_bounds__(32 * kNaWarps) k_na_row_nnz(
-    const int64_t* __restrict__ arp, const int32_t* __restrict__ acol, const int64_t* __restrict__ brp,
-    const int32_t* __restrict__ bcol, int64_t m, int64_t* __restrict__ out, int64_t* scratch) {
+    const int64_t* __restrict__ arp, const int32_t* __restrict__ acol, int64_t a_nnz, const int64_t* __restrict__ brp,
+    const int32_t* __restrict__ bcol, int64_t b_nnz, int64_t k_dim, int64_t n_dim, int64_t m,
+    int64_t* __restrict__ out, int64_t* scratch) {
   extern __shared__ int32_t na_keys[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -50,15 +62,38 @@ __global__ void __launch_bounds__(32 * kNaWarps) k_na_row_nnz(
   if (row >= m) return;
   int32_t* keys = na_keys + warp * kNaSlots;
   const int64_t a0 = arp[row], a1 = arp[row + 1];
+  if (a0 < 0 || a1 < a0 || a1 > a_nnz) {
+    if (lane == 0) {
+      na_flag(scratch, kNaErrBounds);
+      out[row] = 0;
+    }
+    return;
+  }
+  // B row k as a checked range: empty (and flagged) when k or its row pointers are out of range
+  auto brow = [&](int32_t k, int64_t& b0, int64_t& b1) {
+    b0 = b1 = 0;
+    if (k < 0 || k >= k_dim) {
+      na_flag(scratch, kNaErrBounds);
+      return;
+    }
+    const int64_t s = brp[k], e = brp[k + 1];
+    if (s < 0 || e < s || e > b_nnz) {
+      na_flag(scratch, kNaErrBounds);
+      return;
+    }
+    b0 = s;
+    b1 = e;
+  };
   int64_t ip = 0;
   for (int64_t e = a0 + lane; e < a1; e += 32) {
-    const int32_t k = acol[e];
-    ip += brp[k + 1] - brp[k];
+    int64_t b0, b1;
+    brow(acol[e], b0, b1);
+    ip += b1 - b0;
   }
   ip = sg::warp_sum(ip);
   if (ip > kNaMaxRowIP) {
     if (lane == 0) {
-      atomicOr(reinterpret_cast<unsigned long long*>(&scratch[kNaMaxTiles + 1]), kNaErrRowTooLong);
+      na_flag(scratch, kNaErrRowTooLong);
       out[row] = 0;
     }
     return;
@@ -67,9 +102,14 @@ __global__ void __launch_bounds__(32 * kNaWarps) k_na_row_nnz(
   __syncwarp();
   int64_t fresh = 0;
   for (int64_t e = a0; e < a1; ++e) {
-    const int32_t k = acol[e];
-    for (int64_t q = brp[k] + lane; q < brp[k + 1]; q += 32) {
+    int64_t b0, b1;
+    brow(acol[e], b0, b1);
+    for (int64_t q = b0 + lane; q < b1; q += 32) {
       const int32_t c = bcol[q];
+      if (c < 0 || c >= n_dim) {
+        na_flag(scratch, kNaErrBounds);
+        continue;
+      }
       uint32_t slot = sg::hash_slot(c, kNaSlots);
       bool done = false;
       for (int probe = 0; probe < kNaSlots && !done; ++probe) {
@@ -87,7 +127,7 @@ __global__ void __launch_bounds__(32 * kNaWarps) k_na_row_nnz(
         }
         if (!done) slot = (slot + 1 == kNaSlots) ? 0 : slot + 1;
       }
-      if (!done) atomicOr(reinterpret_cast<unsigned long long*>(&scratch[kNaMaxTiles + 1]), kNaErrHashFull);
+      if (!done) na_flag(scratch, kNaErrHashFull);
     }
   }
   fresh = sg::warp_sum(fresh);
@@ -209,13 +249,16 @@ extern "C" int spgemm_symbolic_noalloc(int64_t m, int64_t k, int64_t n, const sp
                                            static_cast<int>(smem)), "smem attribute");
   if (rc != SPGEMM_OK) return rc;
   const unsigned blocks = static_cast<unsigned>(sg::ceil_div(m > 0 ? m : 1, kNaWarps));
-  k_na_row_nnz<<<blocks, 32 * kNaWarps, smem, st>>>(A->row_ptr, A->col_idx, B->row_ptr, B->col_idx, m,
-                                                      c_row_ptr, scratch);
+  k_na_row_nnz<<<blocks, 32 * kNaWarps, smem, st>>>(A->row_ptr, A->col_idx, A->nnz, B->row_ptr, B->col_idx,
+                                                      B->nnz, k, n, m, c_row_ptr, scratch);
   const int64_t len = m + 1;
   const int64_t nb = sg::ceil_div(len, kNaTile);
   k_na_tile_sums<<<static_cast<unsigned>(nb), kNaScanThreads, 0, st>>>(c_row_ptr, len, scratch);
   k_na_scan_sums<<<1, kNaScanThreads, 0, st>>>(nb, scratch);
   k_na_tile_scan<<<static_cast<unsigned>(nb), kNaScanThreads, 0, st>>>(c_row_ptr, len, scratch);
+  // launch errors of these four kernels, before anything else is enqueued
+  rc = sg::check_cuda(cudaGetLastError(), "spgemm_symbolic_noalloc launch");
+  if (rc != SPGEMM_OK) return rc;
   int64_t flags = 0, nnz = 0;
   rc = sg::check_cuda(cudaMemcpyAsync(&flags, scratch + kNaMaxTiles + 1, sizeof(int64_t),
                                       cudaMemcpyDeviceToHost, st), "copy flags");
@@ -225,8 +268,10 @@ extern "C" int spgemm_symbolic_noalloc(int64_t m, int64_t k, int64_t n, const sp
   if (rc != SPGEMM_OK) return rc;
   rc = sg::check_cuda(cudaStreamSynchronize(st), "spgemm_symbolic_noalloc");
   if (rc != SPGEMM_OK) return rc;
-  rc = sg::check_cuda(cudaGetLastError(), "spgemm_symbolic_noalloc launch");
-  if (rc != SPGEMM_OK) return rc;
+  if (flags & kNaErrBounds) {
+    sg::set_last_error("spgemm_symbolic_noalloc: a row pointer or column index of A or B is out of range");
+    return SPGEMM_ERR_INVALID_ARG;
+  }
   if (flags & kNaErrRowTooLong) {
     sg::set_last_error("spgemm_symbolic_noalloc: a row of A*B has more than 2048 intermediate products");
     return SPGEMM_ERR_INVALID_ARG;

@@ -69,10 +69,53 @@ def test_noalloc_rejects_limits():
         binding.spgemm_symbolic_noalloc(A.rows, A.cols, B.cols, dA.desc(), dB.desc(), rp.data_ptr(),
                                         torch.cuda.current_stream().cuda_stream)
     assert e.value.code == -1
-    # and the next valid call is not affected by the flag left behind
+    # a column index of A outside [0, k): flagged on the device and skipped, never read past
+    Abad = synth.random_sparse(20, 20, 0.2, 1)
+    Abad.col = Abad.col.copy()
+    Abad.col[3] = 25
+    Bok = synth.random_sparse(20, 20, 0.2, 2)
+    dAb, dBo = sg.DeviceCSR.from_host(Abad), sg.DeviceCSR.from_host(Bok)
+    rp = torch.empty(Abad.rows + 1, dtype=torch.int64, device="cuda")
+    with pytest.raises(sg.SpgemmError) as e:
+        binding.spgemm_symbolic_noalloc(20, 20, 20, dAb.desc(), dBo.desc(), rp.data_ptr(),
+                                        torch.cuda.current_stream().cuda_stream)
+    assert e.value.code == -1 and "out of range" in sg.spgemm_last_error()
+    # and the next valid call is not affected by the flags left behind
     C = synth.config(1)
     dC, _, (ref_rp, ref_nnz) = _symbolic_reference(C, C)
     rp = torch.empty(C.rows + 1, dtype=torch.int64, device="cuda")
     nnz = binding.spgemm_symbolic_noalloc(C.rows, C.cols, C.cols, dC.desc(), dC.desc(), rp.data_ptr(),
                                           torch.cuda.current_stream().cuda_stream)
     assert nnz == ref_nnz and np.array_equal(rp.cpu().numpy(), ref_rp)
+
+
+def test_noalloc_takes_no_device_memory_after_warm_up():
+    """The point of the entry point: once a warm-up call has loaded its code on the device,
+    further calls take no device memory -- the device's free memory and the caching allocator's
+    counters stay exactly where they were."""
+    import torch
+    import sparse_gemm_irregular_gb300 as sg
+    from sparse_gemm_irregular_gb300 import binding
+    A = synth.config(1)
+    dA, _, (ref_rp, ref_nnz) = _symbolic_reference(A, A)
+    da = dA.desc()
+    stream = torch.cuda.current_stream().cuda_stream
+    rp = torch.empty(A.rows + 1, dtype=torch.int64, device="cuda")
+    # warm-up: an empty product (m = 0) loads the kernels and looks up the static array
+    empty = sg.DeviceCSR.from_host(synth.CSR(0, A.cols, np.zeros(1, np.int64), np.zeros(0, np.int32),
+                                             np.zeros(0)))
+    rp0 = torch.empty(1, dtype=torch.int64, device="cuda")
+    assert binding.spgemm_symbolic_noalloc(0, A.cols, A.cols, empty.desc(), da, rp0.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    stats0 = torch.cuda.memory_stats()
+    keys = ("allocation.all.allocated", "segment.all.allocated", "reserved_bytes.all.current")
+    for _ in range(3):
+        nnz = binding.spgemm_symbolic_noalloc(A.rows, A.cols, A.cols, da, da, rp.data_ptr(), stream)
+        assert nnz == ref_nnz
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    stats1 = torch.cuda.memory_stats()
+    for k in keys:
+        assert stats1.get(k, 0) == stats0.get(k, 0), k
+    assert np.array_equal(rp.cpu().numpy(), ref_rp)
