@@ -1,11 +1,19 @@
-"""Benchmark of the SpGEMM library: C = A * A on a seeded R-MAT matrix (scale 18, edge factor
-16, Graph500 quadrant probabilities, fp64 values U[0,1)), one GPU per process.
+"""Benchmark of the SpGEMM library: C = A * A on the seeded synthetic workloads, one GPU per
+process.
+
+Headline workload: R-MAT scale 21, edge factor 32 (Graph500 quadrant probabilities, fp64
+values U[0,1)), the largest of the five.  Its C (about 6e10 entries, 0.7 TB) fits neither the
+device nor the host, so the numeric phase runs in row windows (spgemm_row_windows cuts them
+between heavy batches) into one reused device buffer; every window is computed inside the
+timed step.  The other four workloads (uniform 8 per row, band 7, R-MAT scale 18, the
+Markov-clustering expansion) are measured the same way in the same run and reported under
+"workloads".
 
 One step = one whole product through the library (create: planner, IP count and binning;
-symbolic; caller allocation of C; numeric; destroy), inputs resident in HBM.  The metric is
-GFLOP/s = 2 x intermediate products / time, plus the fraction of the HBM roofline of the
-compulsory bytes (A, the rows of B that are touched, and C).  L2 is flushed between timed steps
-by writing a 512 MiB buffer outside the timed events.
+symbolic; caller allocation of C or reuse of the window buffer; numeric; destroy), inputs
+resident in HBM.  The metric is GFLOP/s = 2 x intermediate products / time, plus the fraction
+of the HBM roofline of the compulsory bytes (A, the rows of B that are touched, and C).  L2 is
+flushed between timed steps by writing a 512 MiB buffer outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 1..5]
 
@@ -18,6 +26,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -32,6 +41,11 @@ import synth  # noqa: E402
 
 METRIC = "SpGEMM GFLOP/s (2 x intermediate products / s), 1 x GB300"
 UNIT = "GFLOP/s"
+# A C larger than this share of the device memory is produced window by window into a reused
+# device buffer; a C larger than HOST_C_BYTES comes back to the host window by window as well
+WINDOWED_SHARE = 0.5
+HOST_C_BYTES = 32e9
+WINDOW_TARGET = 1_000_000_000      # entries of C per numeric window (windows hold whole heavy batches)
 
 
 def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
@@ -89,6 +103,24 @@ def load_peaks():
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu on Arm hosts, /proc/cpuinfo elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 class ClockSampler:
@@ -160,7 +192,7 @@ def sample_rows_by_ip(A, B, ip_budget: float, seed: int = 0):
 def oracle_rate(A, B, seconds: float, threads: int):
     """Time the oracle (as it stands) on a row sample sized to about `seconds` of work."""
     import oracle
-    rows, ipn = sample_rows_by_ip(A, B, 2e6)
+    rows, ipn = sample_rows_by_ip(A, B, 2e6 * threads / 16)
     t0 = time.perf_counter()
     oracle.spgemm_rows(A, B, rows, threads=threads)
     dt = time.perf_counter() - t0
@@ -182,7 +214,6 @@ def run_reference(args, A, cfg_name, rank):
         return
     import oracle
     threads = os.cpu_count() or 1
-    _, _, ipn0, _ = None, None, None, None
     # size each step to about 4 s of oracle work on all cores
     rows, ipn = sample_rows_by_ip(A, A, 2e6)
     t0 = time.perf_counter()
@@ -203,6 +234,7 @@ def run_reference(args, A, cfg_name, rank):
         "data": "synthetic", "config": {"workload": cfg_name, "rows_per_step": len(rows),
                                         "ip_per_step": ipn},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": "%d seeded uniform rows (%d intermediate products) per step"
                                    % (len(rows), ipn)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -210,22 +242,123 @@ def run_reference(args, A, cfg_name, rank):
     print(json.dumps(out), flush=True)
 
 
-# Algorithmic bytes per element of the kernels that can dominate (the speed-of-light volume,
-# gMAGNUS page, section IV-C, Eq. (8) for the histogram).
-def kernel_bytes(name, st, elems_heavy, nnz_c_heavy, final_chunks, heavy_rows):
+def kernel_bytes(name, st):
+    """Algorithmic bytes per product of a kernel that can dominate (the speed-of-light volume of
+    the gMAGNUS page, section IV-C).  When C^_reord is kept from the symbolic to the numeric
+    phase (stats.resident) the heavy rows are expanded once, with values; otherwise the symbolic
+    phase expands columns only and the numeric phase expands again with values."""
+    e = st.ip_heavy
+    res = bool(st.resident)
     if name == "outer_product":
-        return 12 * elems_heavy                       # write C^ (col + val)
-    if name == "histogram":
-        return 4 * elems_heavy + 8 * (heavy_rows + 1) + 8 * final_chunks   # Eq. (8)
+        return 12 * e if res else (4 + 12) * e          # write C^ (col [+ val])
     if name == "multisplit":
-        return 24 * elems_heavy                       # read + write C^ (col + val)
+        return 24 * e if res else (8 + 24) * e          # read + write C^ (col [+ val])
     if name == "chunk_symbolic":
-        return 4 * elems_heavy                        # read C^_reord columns
-    if name == "chunk_numeric":
-        return 12 * elems_heavy + 12 * nnz_c_heavy    # read C^_reord, write the heavy rows of C
+        return 4 * e                                     # read C^_reord columns
     if name == "chunk_dense":
-        return 12 * st.dense_elems + 12 * st.dense_nnz  # its share of the same
+        return 12 * st.dense_elems + 12 * st.dense_nnz  # read its C^_reord elements, write its C entries
     return None
+
+
+class Workload:
+    """One input on the device plus how its C is produced (whole, or window by window)."""
+
+    def __init__(self, name, A, sg, torch):
+        self.name, self.A = name, A
+        self.dA = sg.DeviceCSR.from_host(A)
+        self.sg, self.torch = sg, torch
+        self.col = self.val = None   # reused device window buffers (windowed products)
+        self.windowed = None
+
+    def ensure_buffers(self, n):
+        torch = self.torch
+        if self.col is None or self.col.numel() < n:
+            self.col = self.val = None
+            torch.cuda.empty_cache()
+            self.col = torch.empty(max(n, 1), dtype=torch.int32, device="cuda")
+            self.val = torch.empty(max(n, 1), dtype=torch.float64, device="cuda")
+
+    def step(self, stream, opts=None, dA=None):
+        """One whole product; returns (stats, phase times or None, number of numeric windows)."""
+        sg = self.sg
+        dA = dA if dA is not None else self.dA
+        p = sg.Product(dA, dA, stream=stream, opts=opts)
+        try:
+            _, nnz = p.symbolic()
+            if self.windowed is None:
+                total = self.torch.cuda.get_device_properties(0).total_memory
+                self.windowed = nnz * 12 > WINDOWED_SHARE * total
+            if self.windowed:
+                cuts, wmax = p.row_windows(WINDOW_TARGET)
+                self.ensure_buffers(wmax)
+                p.numeric_windows(self.col, self.val, cuts=cuts)
+                nwin = len(cuts) - 1
+            else:
+                p.numeric()
+                nwin = 1
+            out = (p.stats(), p.phase_times() if opts is not None else None, nwin)
+        finally:
+            p.close()
+        return out
+
+
+def timed_steps(w, stream, flush, steps, warmup, opts_timed, opts_plain, world, clocks=None):
+    """warmup untimed steps, then `steps` timed ones (CUDA events on the product's stream, L2
+    flushed before each outside the events).  Returns (seconds over ranks, stats, phase sums,
+    per-step ms, windows per step, kernel launches in the timed steps)."""
+    import torch
+    sg = w.sg
+    st = None
+    for _ in range(warmup):
+        st, _, _ = w.step(stream, opts_plain)
+    torch.cuda.synchronize()
+    phase_tot = {}
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = sg.spgemm_kernel_launches()
+    nwin = 1
+    ctx = clocks if clocks is not None else _Null()
+    with ctx:
+        for i in range(steps):
+            flush.fill_(float(i))        # L2 flush, outside the step's events
+            ev[i][0].record(stream)
+            st, ph, nwin = w.step(stream, opts_timed)
+            ev[i][1].record(stream)
+            for k_, (ms, n_) in ph.items():
+                a = phase_tot.setdefault(k_, [0.0, 0])
+                a[0] += ms
+                a[1] += n_
+        torch.cuda.synchronize()
+    launches = sg.spgemm_kernel_launches() - launches0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t_total = max_over_ranks(sum(step_ms) / 1e3, world)
+    return t_total, st, phase_tot, step_ms, nwin, launches
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def phase_table(phase_tot, steps):
+    """Device milliseconds per step and phase.  The light rows run on their own stream next to
+    the heavy pipeline, so their numeric region is the wall time of that stream, overlapped."""
+    out = {}
+    for k_, v in phase_tot.items():
+        if not v[1]:
+            continue
+        key = "light_numeric_overlapped_wall" if k_ == "light_numeric" else k_
+        out[key] = v[0] / steps
+    return out
 
 
 def main():
@@ -234,17 +367,19 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--config", type=int, default=4, help="headline workload (1..5); default R-MAT scale 21")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the other four workloads")
     ap.add_argument("--flags", type=int, default=0, help="extra SPGEMM_FLAG_* bits for A/B runs")
     ap.add_argument("--chunk-width", type=int, default=0, help="planner override W (A/B runs)")
     ap.add_argument("--tau", type=int, default=0, help="planner override tau (A/B runs)")
     ap.add_argument("--rmat-scale", type=int, default=0,
                     help="replace the workload by a seeded R-MAT of this scale (small cases for profiling)")
     ap.add_argument("--edge-factor", type=int, default=16)
-    ap.add_argument("--no-variants", action="store_true",
-                    help="skip the variant measurements (direct split, upper-bound and estimated light rows)")
+    ap.add_argument("--variants", action="store_true",
+                    help="also measure the variants (direct split, upper-bound and estimated light rows) "
+                         "on the headline workload")
     ap.add_argument("--workflow", type=int, default=0,
                     help="light-row sizing: 0 exact symbolic, 1 IP upper bound, 2 HyperLogLog, 3 automatic")
     args = ap.parse_args()
@@ -272,53 +407,17 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     sg.load()
-    dA = sg.DeviceCSR.from_host(A)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
-    timing = sg.options(flags=sg.binding.FLAG_TIMING | args.flags, chunk_width=args.chunk_width, tau=args.tau,
-                        workflow=args.workflow)
-    plain = (sg.options(flags=args.flags, chunk_width=args.chunk_width, tau=args.tau, workflow=args.workflow)
-             if (args.flags or args.chunk_width or args.tau or args.workflow) else None)
+    extra = dict(chunk_width=args.chunk_width, tau=args.tau, workflow=args.workflow)
+    timing = sg.options(flags=sg.binding.FLAG_TIMING | args.flags, **extra)
+    plain = sg.options(flags=args.flags, **extra) if (args.flags or args.chunk_width or args.tau or args.workflow) \
+        else None
 
-    def step(opts=None, keep=False):
-        p = sg.Product(dA, dA, stream=stream, opts=opts)
-        rp, nnz = p.symbolic()
-        col, val = p.numeric()
-        out = (p.stats(), p.phase_times() if opts is not None else None)
-        p.close()
-        if keep:
-            return out, (rp, col, val)
-        return out
-
-    for _ in range(args.warmup):
-        (st, _), _c = step(plain, keep=True)
-        del _c
-    torch.cuda.synchronize()
-
-    # timed region
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    phase_tot = {}
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = sg.spgemm_kernel_launches()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(float(i))        # L2 flush, outside the step's events
-            ev[i][0].record(stream)
-            st, ph = step(timing)
-            ev[i][1].record(stream)
-            for k_, (ms, n_) in ph.items():
-                a = phase_tot.setdefault(k_, [0.0, 0])
-                a[0] += ms
-                a[1] += n_
-        torch.cuda.synchronize()
-    launches = sg.spgemm_kernel_launches() - launches0
-    if world > 1:
-        dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    t_total = max_over_ranks(sum(step_ms) / 1e3, world)
+    w = Workload(cfg_name, A, sg, torch)
+    clk = ClockSampler(local)
+    t_total, st, phase_tot, step_ms, nwin, launches = timed_steps(
+        w, stream, flush, args.steps, args.warmup, timing, plain, world, clocks=clk)
 
     ip = st.ip_total
     c_nnz = st.c_nnz
@@ -329,17 +428,18 @@ def main():
     hbm_frac = comp / (t_total / args.steps) / 1e9 / peak
 
     # dominant kernel of the step and its roofline
-    kern = ["outer_product", "histogram", "multisplit", "chunk_symbolic", "chunk_dense"]
+    kern = ["outer_product", "multisplit", "chunk_symbolic", "chunk_dense"]
     dom = max(kern, key=lambda k_: phase_tot.get(k_, [0, 0])[0])
-    dom_ms, dom_n = phase_tot[dom]
+    dom_ms, dom_n = phase_tot.get(dom, [0.0, 0])
     roofline = None
-    byt = kernel_bytes(dom, st, st.ip_heavy, st.c_nnz_heavy, st.final_chunks, st.rows_heavy)
+    byt = kernel_bytes(dom, st)
     if dom_n and byt:
         achieved = byt * args.steps / (dom_ms / 1e3) / 1e9   # algorithmic bytes / device time
         traffic = measured_traffic(KERNEL_OF.get(dom, ""), cfg_name)
         roofline = {"kernel": KERNEL_OF.get(dom, dom), "bound": "hbm", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                    "algorithmic_bytes_per_launch": byt,
+                    "algorithmic_bytes_per_step": byt,
+                    "algorithmic_bytes_per_launch": byt * args.steps / dom_n,
                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)",
                     "timed_regions_per_step": dom_n / args.steps,
                     "ms_per_step": dom_ms / args.steps}
@@ -350,12 +450,14 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg_name, "m": A.rows, "nnz_A": A.nnz, "ip_total": ip, "nnz_C": c_nnz,
                    "rows_heavy": st.rows_heavy, "ip_heavy": st.ip_heavy,
+                   "heavy_batches": st.heavy_batches, "resident": st.resident,
+                   "numeric_windows": nwin,
                    "light_rows": ("exact symbolic", "IP upper bound", "HyperLogLog estimate")[st.workflow],
                    "l2": "512 MiB buffer written between timed steps (outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_roofline": {"compulsory_bytes": comp, "frac": hbm_frac, "peak_gbs": peak,
                          "peak_source": peak_src},
-        "phases_ms_per_step": {k_: v[0] / args.steps for k_, v in phase_tot.items() if v[1]},
+        "phases_ms_per_step": phase_table(phase_tot, args.steps),
         "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -365,62 +467,91 @@ def main():
     # the same product on other paths, measured the same way: the direct split of level 0
     # (SPGEMM_FLAG_DIRECT_SPLIT) and the light rows sized by their IP bound or by HyperLogLog
     # estimates instead of the exact symbolic pass (SPGEMM_WORKFLOW_UPPER_BOUND / _ESTIMATE)
-    if not args.no_variants:
+    if args.variants:
         result["variants"] = {}
         for name, vflags, vwf in (("direct_split", sg.binding.FLAG_DIRECT_SPLIT, args.workflow),
                                   ("upper_bound", 0, sg.binding.WORKFLOW_UPPER_BOUND),
                                   ("estimate", 0, sg.binding.WORKFLOW_ESTIMATE)):
             vopt = sg.options(flags=sg.binding.FLAG_TIMING | vflags | args.flags, chunk_width=args.chunk_width,
                               tau=args.tau, workflow=vwf)
-            for _ in range(2):
-                step(vopt)
-            torch.cuda.synchronize()
-            vms, vph = [], {}
-            for i in range(args.steps):
-                flush.fill_(float(i))
-                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a_.record(stream)
-                _, ph = step(vopt)
-                b_.record(stream)
-                torch.cuda.synchronize()
-                vms.append(a_.elapsed_time(b_))
-                for k_, (ms, n_) in ph.items():
-                    vph[k_] = vph.get(k_, 0.0) + ms
-            vt = max_over_ranks(sum(vms) / 1e3, world)
+            vt, vst, vph, _, _, _ = timed_steps(w, stream, flush, args.steps, 2, vopt, vopt, world)
             result["variants"][name] = {
                 "value": job_rate(ip, args.steps, world, vt), "unit": UNIT,
-                "ms_per_step": vt * 1e3 / args.steps,
-                "phases_ms_per_step": {k_: v / args.steps for k_, v in vph.items() if v > 0}}
+                "ms_per_step": vt * 1e3 / args.steps, "phases_ms_per_step": phase_table(vph, args.steps)}
 
     # end to end through the public API with host buffers
     if not args.no_e2e:
-        result["e2e"] = e2e(args, A, sg, torch, stream, world)
+        result["e2e"] = e2e(args, w, sg, torch, stream, world)
+
+    # the other workloads, measured the same way (device-resident inputs; the L2 flush between
+    # steps; max over ranks), each with its end-to-end figure
+    if not args.no_others and not args.rmat_scale:
+        result["workloads"] = {}
+        for cid in sorted(synth.CONFIGS):
+            if cid == args.config:
+                continue
+            name = synth.CONFIGS[cid][0]
+            Ao = synth.config(cid)
+            wo = Workload(name, Ao, sg, torch)
+            ot, ost, oph, oms, onw, _ = timed_steps(wo, stream, flush, args.steps, args.warmup, timing, plain, world)
+            ocomp = compulsory_bytes(Ao, Ao, ost.c_nnz)
+            entry = {"value": job_rate(ost.ip_total, args.steps, world, ot), "unit": UNIT,
+                     "ms_per_step": ot * 1e3 / args.steps, "steps": args.steps,
+                     "ip_total": ost.ip_total, "nnz_C": ost.c_nnz, "rows_heavy": ost.rows_heavy,
+                     "resident": ost.resident, "numeric_windows": onw,
+                     "hbm_roofline": {"compulsory_bytes": ocomp,
+                                      "frac": ocomp / (ot / args.steps) / 1e9 / peak},
+                     "phases_ms_per_step": phase_table(oph, args.steps)}
+            if not args.no_e2e:
+                entry["e2e"] = e2e(args, wo, sg, torch, stream, world)
+            result["workloads"][name] = entry
+            del wo
+            torch.cuda.synchronize()
+            sg.spgemm_release_memory()
+            torch.cuda.empty_cache()
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        gf, nrows, ipn, dt = oracle_rate(A, A, 12.0, threads)
+        gf, nrows, ipn, dt = oracle_rate(A, A, 10.0, threads)
+        gf1, nrows1, ipn1, dt1 = oracle_rate(A, A, 6.0, 1)
         result["cpu_baseline"] = {"value": gf, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                  "cpu": cpu_model(),
                                   "sample": "%d seeded uniform rows, %d intermediate products, %.1f s"
-                                            % (nrows, ipn, dt)}
+                                            % (nrows, ipn, dt),
+                                  "one_core": {"value": gf1, "unit": UNIT, "cores": 1,
+                                               "sample": "%d seeded uniform rows, %d intermediate products, "
+                                                         "%.1f s" % (nrows1, ipn1, dt1)}}
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
 
 
-def e2e(args, A, sg, torch, stream, world):
-    """Same metric through the public API with host inputs and outputs: every step copies A from
-    pinned host memory, runs the product, and receives C in pinned host memory through
-    spgemm_numeric_host (C is computed in row windows and each finished window is copied out
-    while the next one is computed).  Warm-up steps as for the device-resident metric."""
+def e2e(args, w, sg, torch, stream, world):
+    """Same metric through the public API with host inputs and outputs, over the same number of
+    steps as the device-resident metric: every step copies A from pinned host memory and the
+    product's C comes back to pinned host memory.  A C that fits the host goes through
+    spgemm_numeric_host (row windows computed on the device, each finished window copied out
+    while the next is computed).  A C larger than the host (the R-MAT scale 21 product) is
+    computed window by window with spgemm_numeric_rows into two device buffers, and each window
+    is copied into a reused pinned host buffer on a second stream while the next window is
+    computed: the host receives every entry of C, one window at a time."""
+    A = w.A
+    torch.cuda.synchronize()
+    sg.spgemm_release_memory()
+    torch.cuda.empty_cache()
+    host_windowed = None
     hp = [torch.from_numpy(a).pin_memory() for a in (A.row_ptr, A.col, A.val)]
     dev = [torch.empty_like(x, device="cuda") for x in hp]
     h2d = sum(x.numel() * x.element_size() for x in hp)
-    host_c = None
     times = []
     warm = max(3, args.warmup)
-    steps = max(1, min(args.steps, 3))
+    steps = args.steps
     d2h = 0
     st = None
+    copy_stream = torch.cuda.Stream()
+    host_c = None
+    win = None   # windowed: two device buffers, two pinned host pieces
     for i in range(warm + steps):
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -431,11 +562,50 @@ def e2e(args, A, sg, torch, stream, world):
         dA = sg.DeviceCSR(A.rows, A.cols, dev[0], dev[1], dev[2])
         p = sg.Product(dA, dA, stream=stream)
         _, nnz = p.symbolic()
-        if host_c is None:  # first (warm-up) pass: pin the host arrays of C once
-            host_c = [torch.empty(A.rows + 1, dtype=torch.int64).pin_memory(),
-                      torch.empty(max(nnz, 1), dtype=torch.int32).pin_memory(),
-                      torch.empty(max(nnz, 1), dtype=torch.float64).pin_memory()]
-        p.numeric_host(host_c[1], host_c[2], host_c[0])
+        if host_windowed is None:
+            host_windowed = w.windowed or nnz * 12 > HOST_C_BYTES
+        if not host_windowed:
+            if host_c is None:  # first (warm-up) pass: pin the host arrays of C once
+                host_c = [torch.empty(A.rows + 1, dtype=torch.int64).pin_memory(),
+                          torch.empty(max(nnz, 1), dtype=torch.int32).pin_memory(),
+                          torch.empty(max(nnz, 1), dtype=torch.float64).pin_memory()]
+            p.numeric_host(host_c[1], host_c[2], host_c[0])
+        else:
+            cuts, wmax = p.row_windows(WINDOW_TARGET)
+            if win is None or win["dev"][0][0].numel() < wmax:
+                win = None
+                torch.cuda.empty_cache()
+                piece = 1 << 27  # entries per host copy piece (1.5 GB of col + val)
+                win = {"dev": [(torch.empty(wmax, dtype=torch.int32, device="cuda"),
+                                torch.empty(wmax, dtype=torch.float64, device="cuda")) for _ in range(2)],
+                       "host": [(torch.empty(piece, dtype=torch.int32).pin_memory(),
+                                 torch.empty(piece, dtype=torch.float64).pin_memory()) for _ in range(2)],
+                       "piece": piece, "done": [torch.cuda.Event() for _ in range(2)],
+                       "hdone": [torch.cuda.Event() for _ in range(2)]}
+            rp_host = p.row_ptr.cpu().numpy()
+            hk = 0
+            for wi, (rb, re) in enumerate(zip(cuts[:-1], cuts[1:])):
+                b = wi % 2
+                dcol, dval = win["dev"][b]
+                if wi >= 2:
+                    stream.wait_event(win["done"][b])      # its previous window copied out
+                sg.spgemm_numeric_rows(p.h, rb, re, dcol.data_ptr(), dval.data_ptr())
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                copy_stream.wait_event(ev)
+                n = int(rp_host[re] - rp_host[rb])
+                with torch.cuda.stream(copy_stream):
+                    for o in range(0, n, win["piece"]):
+                        e_ = min(n, o + win["piece"])
+                        hc, hv = win["host"][hk % 2]
+                        if hk >= 2:
+                            win["hdone"][hk % 2].synchronize()
+                        hc[:e_ - o].copy_(dcol[o:e_], non_blocking=True)
+                        hv[:e_ - o].copy_(dval[o:e_], non_blocking=True)
+                        win["hdone"][hk % 2].record(copy_stream)
+                        hk += 1
+                win["done"][b].record(copy_stream)
+            stream.wait_stream(copy_stream)
         t1.record(stream)
         st = p.stats()
         p.close()
@@ -444,8 +614,15 @@ def e2e(args, A, sg, torch, stream, world):
         if i >= warm:
             times.append(t0.elapsed_time(t1) / 1e3)
     t = max_over_ranks(sum(times), world)
-    return {"value": job_rate(st.ip_total, len(times), world, t), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": len(times), "warmup": warm}
+    out = {"value": job_rate(st.ip_total, len(times), world, t), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": len(times), "warmup": warm}
+    if host_windowed:
+        out["host_output"] = "row windows copied into a reused pinned host buffer (C beyond the host budget)"
+    del win, host_c
+    torch.cuda.synchronize()
+    sg.spgemm_release_memory()
+    torch.cuda.empty_cache()
+    return out
 
 
 if __name__ == "__main__":

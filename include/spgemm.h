@@ -216,6 +216,23 @@ int spgemm_numeric_rows(spgemm_handle h, int64_t row_begin, int64_t row_end, int
 int spgemm_numeric_host(spgemm_handle h, int64_t* c_row_ptr, int32_t* c_col_idx, double* c_vals,
                         int64_t window_nnz);
 
+/* Row windows for a numeric phase run window by window (spgemm_numeric_rows into one reused
+ * buffer, for a C larger than the device).  Windows cover [0, m) in order; each holds about
+ * target_nnz entries of C (0: a quarter of C, at least 4 M entries).  When the heavy rows'
+ * expansion is recomputed in the numeric phase (stats.resident == 0 with several heavy
+ * batches), every cut falls between two heavy batches, so each batch is expanded once per
+ * pass over the windows; such windows may hold more than target_nnz entries.
+ *   cuts:           host, cap int64 entries; receives n_windows + 1 row indices, cuts[0] = 0,
+ *                   cuts[n_windows] = m, window w = rows [cuts[w], cuts[w+1]);
+ *   n_windows:      host, receives the number of windows (also when cap is too small);
+ *   max_window_nnz: host (may be NULL), receives the entries of C in the largest window.
+ * Copies C.row_ptr to the host and synchronises the stream.  Errors: BAD_STATE before
+ * spgemm_symbolic; INVALID_ARG for NULL pointers, negative sizes, or cap < n_windows + 1
+ * (n_windows and max_window_nnz are set, so the caller can retry with a longer array).  The
+ * pages have no counterpart: it serves the row-window numeric phase. */
+int spgemm_row_windows(spgemm_handle h, int64_t target_nnz, int64_t* cuts, int64_t cap, int64_t* n_windows,
+                       int64_t* max_window_nnz);
+
 int spgemm_get_stats(spgemm_handle h, spgemm_stats* out);
 int spgemm_get_plan(spgemm_handle h, spgemm_plan* out);
 

@@ -13,8 +13,8 @@ from .binding import (SpgemmError, load, options, spgemm_create, spgemm_destroy,
                       spgemm_hll_estimate, spgemm_mcl_prune_numeric, spgemm_mcl_prune_symbolic,
                       spgemm_numeric_host,
                       spgemm_get_plan, spgemm_get_stats, spgemm_kernel_launches, spgemm_last_error, spgemm_numeric,
-                      spgemm_numeric_rows, spgemm_plan_params, spgemm_release_memory, spgemm_strerror,
-                      spgemm_symbolic)
+                      spgemm_numeric_rows, spgemm_plan_params, spgemm_release_memory, spgemm_row_windows,
+                      spgemm_strerror, spgemm_symbolic)
 
 __all__ = [
     "DeviceCSR", "multiply", "Product", "SpgemmError", "load", "options", "spgemm_create",
@@ -22,7 +22,7 @@ __all__ = [
     "spgemm_mcl_prune_symbolic", "spgemm_mcl_prune_numeric", "mcl_iteration",
     "spgemm_kernel_launches",
     "spgemm_last_error", "spgemm_numeric", "spgemm_numeric_rows", "spgemm_plan_params",
-    "spgemm_release_memory",
+    "spgemm_release_memory", "spgemm_row_windows",
     "spgemm_strerror", "spgemm_symbolic",
 ]
 
@@ -95,6 +95,21 @@ class Product:
 
     def numeric_rows(self, row_begin: int, row_end: int, col, val):
         spgemm_numeric_rows(self.h, row_begin, row_end, col.data_ptr(), val.data_ptr())
+
+    def row_windows(self, target_nnz: int = 0):
+        """(row cuts, entries of C in the largest window) for numeric_rows window by window."""
+        return spgemm_row_windows(self.h, target_nnz)
+
+    def numeric_windows(self, col, val, target_nnz: int = 0, cuts=None):
+        """Numeric phase window by window into the same device arrays col / val (each window at
+        offset 0; they need the largest window's entries).  Returns the cuts used."""
+        if cuts is None:
+            cuts, wmax = self.row_windows(target_nnz)
+            if col.numel() < wmax or val.numel() < wmax:
+                raise ValueError("window buffers shorter than the largest window")
+        for rb, re in zip(cuts[:-1], cuts[1:]):
+            spgemm_numeric_rows(self.h, rb, re, col.data_ptr(), val.data_ptr())
+        return cuts
 
     def numeric_host(self, col, val, row_ptr=None, window_nnz: int = 0):
         """Numeric phase into host (CPU) tensors col (int32, nnz) and val (float64, nnz), and

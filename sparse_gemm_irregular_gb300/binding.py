@@ -77,6 +77,7 @@ EXPORTS = {
     "spgemm_numeric": (ctypes.c_int, [_vp, _vp, _vp]),
     "spgemm_numeric_rows": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
     "spgemm_numeric_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64]),
+    "spgemm_row_windows": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _vp]),
     "spgemm_get_stats": (ctypes.c_int, [_vp, _vp]),
     "spgemm_get_plan": (ctypes.c_int, [_vp, _vp]),
     "spgemm_get_phase_times": (ctypes.c_int, [_vp, _vp, _vp, _i32]),
@@ -163,6 +164,19 @@ def spgemm_numeric_rows(h, row_begin: int, row_end: int, c_col: int, c_val: int)
 def spgemm_numeric_host(h, c_row_ptr: int, c_col: int, c_val: int, window_nnz: int = 0):
     _check(load().spgemm_numeric_host(h, _vp(c_row_ptr) if c_row_ptr else None, _vp(c_col), _vp(c_val),
                                       window_nnz), "spgemm_numeric_host")
+
+
+def spgemm_row_windows(h, target_nnz: int = 0):
+    """Row cuts of a windowed numeric phase and the entries of C in its largest window."""
+    n = _i64(0)
+    wmax = _i64(0)
+    rc = load().spgemm_row_windows(h, target_nnz, None, 0, ctypes.byref(n), ctypes.byref(wmax))
+    if rc != 0 and n.value <= 0:
+        _check(rc, "spgemm_row_windows")
+    cuts = (_i64 * (n.value + 1))()
+    _check(load().spgemm_row_windows(h, target_nnz, cuts, n.value + 1, ctypes.byref(n), ctypes.byref(wmax)),
+           "spgemm_row_windows")
+    return [int(x) for x in cuts], int(wmax.value)
 
 
 def spgemm_get_stats(h) -> spgemm_stats:

@@ -1488,9 +1488,18 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
       // batches of heavy rows whose C^ fits the budget
       int64_t cap = h->opt.heavy_batch_elems;
       if (!cap) {
+        // free device memory plus what the handle's pool holds cached but unused (a previous
+        // product's workspace, reused by this one's allocations)
         size_t fr = 0, tot = 0;
         cudaMemGetInfo(&fr, &tot);
-        cap = static_cast<int64_t>(static_cast<double>(fr) * 0.35 / 24.0);
+        uint64_t reserved = 0, used = 0;
+        if (cudaMemPoolGetAttribute(h->pool, cudaMemPoolAttrReservedMemCurrent, &reserved) != cudaSuccess ||
+            cudaMemPoolGetAttribute(h->pool, cudaMemPoolAttrUsedMemCurrent, &used) != cudaSuccess) {
+          cudaGetLastError();
+          reserved = used = 0;
+        }
+        const double avail = static_cast<double>(fr) + static_cast<double>(reserved > used ? reserved - used : 0);
+        cap = static_cast<int64_t>(avail * 0.35 / 24.0);
       }
       int64_t i = 0, maxb = 0;
       while (i < h->nheavy) {
@@ -1698,6 +1707,34 @@ int spgemm_numeric_host(spgemm_handle h, int64_t* c_row_ptr, int32_t* c_col_idx,
   }
   SG_TRY(check_cuda(cudaStreamSynchronize(h->st_copy), "numeric host copies"));
   return sync_and_check(h, "numeric");
+}
+
+int spgemm_row_windows(spgemm_handle h, int64_t target_nnz, int64_t* cuts, int64_t cap, int64_t* n_windows,
+                       int64_t* max_window_nnz) {
+  g_last_error.clear();
+  if (!h || target_nnz < 0 || cap < 0 || !n_windows || (cap > 0 && !cuts)) return SPGEMM_ERR_INVALID_ARG;
+  if (h->state < 2) {
+    set_last_error("row windows need the symbolic phase");
+    return SPGEMM_ERR_BAD_STATE;
+  }
+  const int64_t m = h->m;
+  std::vector<int64_t> rp(static_cast<size_t>(m + 1));
+  SG_TRY(check_cuda(cudaMemcpyAsync(rp.data(), h->c_row_ptr, sizeof(int64_t) * (m + 1), cudaMemcpyDeviceToHost, h->st),
+                    "copy row_ptr"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "copy row_ptr"));
+  const int64_t target = target_nnz ? target_nnz : std::max<int64_t>(rp[m] / 4, int64_t(1) << 22);
+  const std::vector<int64_t> c = host_windows(h, rp, target);
+  const int64_t nw = static_cast<int64_t>(c.size()) - 1;
+  *n_windows = nw;
+  int64_t wmax = 0;
+  for (int64_t w = 0; w < nw; ++w) wmax = std::max(wmax, rp[c[w + 1]] - rp[c[w]]);
+  if (max_window_nnz) *max_window_nnz = wmax;
+  if (cap < nw + 1) {
+    set_last_error("cuts array too short: it needs n_windows + 1 entries");
+    return SPGEMM_ERR_INVALID_ARG;
+  }
+  std::copy(c.begin(), c.end(), cuts);
+  return SPGEMM_OK;
 }
 
 int spgemm_get_stats(spgemm_handle h, spgemm_stats* out) {
