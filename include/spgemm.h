@@ -71,6 +71,13 @@ extern "C" {
                                          C^_reord (counts from per-B-row chunk histograms), so C^
                                          is never stored and level 0 needs no multisplit pass */
 #define SPGEMM_FLAG_NO_GRAPH 2048    /* never capture or replay the numeric phase as a CUDA graph */
+#define SPGEMM_FLAG_FUSED 8192       /* heavy rows without the intermediate matrix in HBM: the
+                                        rows of B are split once by column chunk, and every
+                                        (heavy row, chunk) accumulator generates its own products
+                                        from A and the split B instead of reading them from
+                                        C^_reord (no outer product, no multisplit pass, no heavy
+                                        batches to recompute); taken when a row has at most 2048
+                                        chunks and B has fewer than 2^31 entries (stats.fused) */
 #define SPGEMM_FLAG_NO_ESC 4096      /* light hash rows with at most 64 intermediate products
                                         use the shared-memory hash table like longer rows, instead
                                         of the default expand-sort-compact accumulator held in one
@@ -157,6 +164,8 @@ typedef struct {
   int64_t rows_overflow;     /* estimated workflow: light rows that exceeded their slot    */
   int32_t workflow;          /* SPGEMM_WORKFLOW_* the symbolic phase ran (after AUTO)      */
   int32_t hll_registers;     /* registers per sketch (estimated workflow), else 0          */
+  int32_t fused;             /* 1: heavy rows generated their products (SPGEMM_FLAG_FUSED)  */
+  int32_t reserved;
 } spgemm_stats;
 
 typedef struct spgemm_ctx* spgemm_handle;

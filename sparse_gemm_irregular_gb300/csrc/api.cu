@@ -666,6 +666,99 @@ bool use_direct(const spgemm_ctx* h) {
   return (h->opt.flags & SPGEMM_FLAG_DIRECT_SPLIT) && h->plan.levels == 1 && h->plan.chunks_required > 1;
 }
 
+// ---- heavy rows without C^ (SPGEMM_FLAG_FUSED) ------------------------------------------------
+FusedSrc fused_src(const spgemm_ctx* h, const HeavyBatch& hb, const int32_t* seg) {
+  FusedSrc f{};
+  f.arp = h->A.row_ptr;
+  f.aval = h->A.vals;
+  f.hrp = hb.f_hrp;
+  f.seg = seg;
+  f.E = hb.entries;
+  f.bcol = h->d_bs_col;
+  f.bval = h->d_bs_val;
+  f.shift = ilog2_i64(h->plan.chunk_width);
+  return f;
+}
+
+// The batch's segment table (built from the current split of B), for one phase's chunk kernels.
+// One buffer on the handle, grown to the largest batch during the symbolic phase, so the numeric
+// phase allocates nothing (and can be captured into a graph).
+int fused_segtable(spgemm_ctx* h, const HeavyBatch& hb, int32_t** seg) {
+  const int64_t v = h->plan.chunks_required;
+  const int64_t need = std::max<int64_t>((v + 1) * hb.entries, 1);
+  if (need > h->seg_cap) {
+    ws_free(h, h->d_seg);
+    h->d_seg = nullptr;
+    h->seg_cap = 0;
+    SG_ALLOC(h->d_seg, int32_t, need);
+    h->seg_cap = need;
+  }
+  *seg = h->d_seg;
+  launch_segtable(h->A, h->d_heavy + hb.h0, hb.h1 - hb.h0, hb.f_hrp, h->B, h->d_bo, v, hb.entries, *seg, h->st);
+  return SPGEMM_OK;
+}
+
+// The column split of B (the multisplit applied to B's rows by the final chunk width): the
+// symbolic phase counts the chunk entries of every row of B that a heavy row uses and splits
+// the columns; the numeric phase splits columns and values again (A and B may have new values).
+int fused_prepare(spgemm_ctx* h, bool vals) {
+  PhaseTimer t(h, 2);
+  const int64_t kc = h->k;
+  const int64_t v = h->plan.chunks_required;
+  const int shift = ilog2_i64(h->plan.chunk_width);
+  if (!h->d_colcnt) {
+    SG_ALLOC(h->d_colcnt, int32_t, std::max<int64_t>(kc, 1));
+    SG_ALLOC(h->d_bh, int32_t, std::max<int64_t>(kc * v, 1));
+    SG_ALLOC(h->d_bo, int32_t, std::max<int64_t>(kc * (v + 1), 1));
+    SG_ALLOC(h->d_bs_col, int32_t, std::max<int64_t>(h->B.nnz, 1));
+    cudaMemsetAsync(h->d_colcnt, 0, sizeof(int32_t) * kc, h->st);
+    cudaMemsetAsync(h->d_bh, 0, sizeof(int32_t) * kc * v, h->st);
+    launch_csc_count(h->A, h->d_heavy, h->nheavy, h->d_colcnt, h->st);
+    launch_b_chunk_hist(h->B, h->d_colcnt, shift, v, h->d_bh, h->d_err, h->st);
+  }
+  if (vals && !h->d_bs_val) SG_ALLOC(h->d_bs_val, double, std::max<int64_t>(h->B.nnz, 1));
+  launch_bsplit(h->B, h->d_colcnt, h->d_bh, shift, v, h->d_bo, h->d_bs_col, vals ? h->d_bs_val : nullptr, h->d_err,
+                h->st);
+  return SPGEMM_OK;
+}
+
+// Final chunks of a batch: the level-0 counts from the per-B-row chunk counts, one final chunk
+// per (row, chunk), chunk-major.  Symbolic phase only; the numeric phase reuses them.
+int heavy_fused(spgemm_ctx* h, HeavyBatch& hb) {
+  const int64_t R = hb.h1 - hb.h0;
+  const int32_t* rows = h->d_heavy + hb.h0;
+  const int64_t v = h->plan.chunks_required;
+  const int64_t W = h->plan.chunk_width;
+  PhaseTimer t(h, 4);
+  int64_t*& hrp = hb.f_hrp;
+  unsigned long long* counts;
+  SG_ALLOC(hrp, int64_t, R + 1);
+  SG_ALLOC(counts, unsigned long long, R * v);
+  launch_heavy_row_len(h->A, rows, R, hrp, h->st);
+  SG_TRY(scan(h, hrp, hrp, R));
+  SG_TRY(check_cuda(cudaMemcpyAsync(&hb.entries, hrp + R, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                    "copy heavy entries"));
+  cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * R * v, h->st);
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "heavy entries"));
+  const int64_t entries = hb.entries;
+  launch_row_chunk_counts(h->A, rows, R, hrp, entries, h->d_bh, v, counts, h->st);
+  hb.lv.clear();
+  LevelInfo li;
+  li.nin = R;
+  li.v = v;
+  li.width = W;
+  hb.lv.push_back(li);
+  hb.nfinal = R * v;
+  hb.bitmap_from = 0;
+  SG_ALLOC(hb.f_start, int64_t, R * v);
+  SG_ALLOC(hb.f_cnt, int64_t, R * v);
+  SG_ALLOC(hb.f_row, int32_t, R * v);
+  SG_ALLOC(hb.f_base, int32_t, R * v);
+  launch_fused_desc(counts, R, v, W, hb.f_cnt, hb.f_row, hb.f_base, hb.f_start, h->st);
+  ws_free(h, counts);
+  return SPGEMM_OK;
+}
+
 // Accumulator bins of the final chunks (stable order), then their symbolic counts and the
 // offsets of every chunk inside its row of C.
 int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
@@ -697,6 +790,8 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     ws_free(h, fcnt);
     ws_free(h, starts);
   }
+  int32_t* seg = nullptr;
+  if (h->fused) SG_TRY(fused_segtable(h, hb, &seg));
   {
     PhaseTimer t(h, 7);
     ChunkSet cs{};
@@ -716,8 +811,13 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
                     h->lad.slots[L], h->lad.tpr[L], false, 0, false, sk, h->d_err, h->st);
     for (int j = 0; j < 4; ++j) {        // last-level chunks: bitmaps of width W
       const int b = h->lad.n + j;
-      launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
-                          h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk, h->d_err, h->d_counter, nullptr, h->st);
+      if (h->fused)
+        launch_fused_chunks(fused_src(h, hb, seg), cs, hb.f_list + hb.f_bin_start[b],
+                            hb.f_bin_start[b + 1] - hb.f_bin_start[b], h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk,
+                            h->d_err, h->d_counter, h->st);
+      else
+        launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+                            h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk, h->d_err, h->d_counter, nullptr, h->st);
     }
   }
   {
@@ -750,6 +850,8 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
 }
 
 int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
+  int32_t* seg = nullptr;
+  if (h->fused) SG_TRY(fused_segtable(h, hb, &seg));
   PhaseTimer t(h, 11);
   ChunkSet cs{};
   cs.start = hb.f_start;
@@ -764,15 +866,20 @@ int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
   for (int L = 0; L < h->lad.n; ++L)
     launch_chunks(cs, hb.f_list + hb.f_bin_start[L], hb.f_bin_start[L + 1] - hb.f_bin_start[L], h->lad.slots[L],
                   h->lad.tpr[L], false, 0, true, sk, h->d_err, h->st);
-  if ((h->opt.flags & SPGEMM_FLAG_DENSE_L2) && !h->d_gacc)
+  if ((h->opt.flags & SPGEMM_FLAG_DENSE_L2) && !h->fused && !h->d_gacc)
     SG_ALLOC(h->d_gacc, double, static_cast<int64_t>(h->sms) * h->plan.chunk_width);
   for (int j = 0; j < 4; ++j) {
     const int b = h->lad.n + j;
     PhaseTimer td(h, 12);  // only the dense bin is counted here (its region nests in slot 11)
     if (j < 3) td.cancel();
-    launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
-                        h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err,
-                        h->d_counter, h->d_gacc, h->st);
+    if (h->fused)
+      launch_fused_chunks(fused_src(h, hb, seg), cs, hb.f_list + hb.f_bin_start[b],
+                          hb.f_bin_start[b + 1] - hb.f_bin_start[b], h->plan.chunk_width, j == 3 ? 2 : 1,
+                          kChunkSlots[j], kChunkTpr[j], sk, h->d_err, h->d_counter, h->st);
+    else
+      launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+                          h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err,
+                          h->d_counter, h->d_gacc, h->st);
   }
   return SPGEMM_OK;
 }
@@ -1159,9 +1266,14 @@ int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, doubl
       launch_copy_rows(h->d_est_list[b], h->est_count[b], h->d_row_tmp, h->c_row_ptr, rb, re,
                        h->d_tmp_col[b == 2 ? 1 : 0], h->d_tmp_val[b == 2 ? 1 : 0], c_col, c_val, b > 0, h->st);
   }
+  bool split = false;
   for (auto& hb : h->batches) {
     if (hb.row_hi < rb || hb.row_lo >= re) continue;
-    if (!h->resident) {
+    if (h->fused) {
+      if (!split) SG_TRY(fused_prepare(h, true));  // B's current values, split once per call
+      split = true;
+      SG_TRY(heavy_chunk_numeric(h, hb, sk));
+    } else if (!h->resident) {
       SG_TRY(ensure_chat(h, true));
       int64_t* crp;
       SG_ALLOC(crp, int64_t, hb.h1 - hb.h0 + 1);
@@ -1244,7 +1356,7 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
   }
   h->last_graph = false;
   const bool graphable = !h->timing && !(h->opt.flags & SPGEMM_FLAG_NO_GRAPH) &&
-                         (h->batches.empty() || h->resident);
+                         (h->batches.empty() || h->resident || h->fused);
   if (graphable) {
     SG_TRY(numeric_bins(h));  // its one synchronisation stays outside any capture
     const bool same = rb == h->num_rb && re == h->num_re && c_col == h->num_col && c_val == h->num_val;
@@ -1276,12 +1388,12 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
 std::vector<int64_t> host_windows(const spgemm_ctx* h, const std::vector<int64_t>& rp, int64_t target) {
   std::vector<int64_t> cuts{0};
   const int64_t m = h->m;
-  if (!h->resident && h->batches.size() > 1) {
+  if ((!h->resident || h->fused) && h->batches.size() > 1) {
     for (size_t b = 1; b < h->batches.size(); ++b) {
       const int64_t c = h->batches[b].row_lo;  // first heavy row of batch b; rows before it belong to earlier windows
       if (c > cuts.back() && rp[c] - rp[cuts.back()] >= target) cuts.push_back(c);
     }
-  } else if (h->resident || h->batches.empty()) {
+  } else if (h->resident || h->fused || h->batches.empty()) {
     int64_t r = 0;
     while (r < m) {
       // first row whose prefix reaches the next target (binary search on the row pointer)
@@ -1474,6 +1586,9 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
       ws_free(h, tmp);
     }
     if (h->nheavy > 0) {
+      h->fused = (h->opt.flags & SPGEMM_FLAG_FUSED) && h->plan.chunks_required <= kFusedMaxChunks &&
+                 h->B.nnz < (int64_t(1) << 31);
+      h->stats.fused = h->fused ? 1 : 0;
       SG_ALLOC(h->d_heavy_pre, int64_t, h->nheavy + 1);
       launch_gather_ip(h->d_heavy, h->nheavy, h->d_ip, h->d_heavy_pre, h->st);
       SG_TRY(scan(h, h->d_heavy_pre, h->d_heavy_pre, h->nheavy));
@@ -1516,9 +1631,9 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
         i = j;
       }
       h->batch_cap = (maxb + 15) / 16 * 16;  // keeps both halves of the C^ buffer 16-byte aligned
-      h->resident = h->batches.size() == 1 && !(h->opt.flags & SPGEMM_FLAG_RECOMPUTE);
+      h->resident = h->batches.size() == 1 && !(h->opt.flags & SPGEMM_FLAG_RECOMPUTE) && !h->fused;
       h->stats.heavy_batches = static_cast<int64_t>(h->batches.size());
-      h->stats.chat_bytes = maxb * 12;
+      h->stats.chat_bytes = h->fused ? 0 : maxb * 12;
       h->stats.resident = h->resident ? 1 : 0;
     }
     return SPGEMM_OK;
@@ -1556,7 +1671,16 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     light_pass(h, false, sk);
   }
   int64_t levels = 0, finals = 0, dense = 0;
+  if (h->fused && !h->batches.empty()) SG_TRY(fused_prepare(h, false));
   for (auto& hb : h->batches) {
+    if (h->fused) {
+      SG_TRY(heavy_fused(h, hb));
+      SG_TRY(heavy_chunk_symbolic(h, hb, c_row_ptr));
+      levels = std::max<int64_t>(levels, 1);
+      finals += hb.nfinal;
+      dense += hb.f_bin_start[h->lad.n + 4] - hb.f_bin_start[h->lad.n + 3];
+      continue;
+    }
     const bool vals = h->resident;
     SG_TRY(ensure_chat(h, vals));
     int64_t* crp;

@@ -216,6 +216,35 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
                          int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
                          cudaStream_t s);
 constexpr int kChunkHubSlots = 137;           // hub columns of a dense chunk (k_chunk.cu)
+
+// ---- heavy rows without C^ in HBM (k_fused.cu) ----------------------------------------------
+constexpr int64_t kFusedMaxChunks = 2048;      // chunks per row the column split of B supports
+// Where the generating accumulators read a chunk's products from: row r of A and, for every
+// entry (r, k), the chunk-c part of row k of the column-split B.
+struct FusedSrc {
+  const int64_t* arp;    // A's row pointers and values (the heavy rows' values are read in place)
+  const double* aval;
+  const int64_t* hrp;    // batch: prefix of the heavy rows' lengths (entry e0 of batch-local row p)
+  const int32_t* seg;    // batch: segment table, (v + 1) x E, chunk-major (launch_segtable)
+  int64_t E;             // batch: entries of its heavy rows
+  const int32_t* bcol;   // B with every row's entries grouped by chunk
+  const double* bval;
+  int shift;             // log2 of the chunk width
+};
+// bo and the split entries of the rows of B with colcnt > 0 (bh: their per-chunk counts);
+// bs_val null: columns only
+void launch_bsplit(const spgemm_csr& B, const int32_t* colcnt, const int32_t* bh, int shift, int64_t v,
+                   int32_t* bo, int32_t* bs_col, double* bs_val, uint32_t* err, cudaStream_t s);
+// seg[c * E + e] = B_split position of chunk c of the B row of heavy entry e (c = v: the row's end)
+void launch_segtable(const spgemm_csr& A, const int32_t* rows, int64_t R, const int64_t* hrp, const spgemm_csr& B,
+                     const int32_t* bo, int64_t v, int64_t E, int32_t* seg, cudaStream_t s);
+// final chunks of a batch from its level-0 counts, chunk-major
+void launch_fused_desc(const unsigned long long* counts, int64_t R, int64_t v, int64_t width, int64_t* f_cnt,
+                       int32_t* f_row, int32_t* f_base, int64_t* f_start, cudaStream_t s);
+// mode 0 symbolic, 1 hash numeric, 2 dense numeric (persistent blocks, counter zeroed here)
+void launch_fused_chunks(const FusedSrc& f, const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width,
+                         int mode, int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter,
+                         cudaStream_t s);
 void launch_invert(const int32_t* list, int64_t n, int32_t* xmap, cudaStream_t s);
 void launch_offset_copy(const int64_t* src, int64_t n, int64_t delta, int64_t* dst, cudaStream_t s);
 // out[0] += sum of a[list[i]], out[1] += sum of b[list[i]] for i < n
@@ -258,6 +287,8 @@ struct HeavyBatch {
   int64_t nnz_c = 0;            // entries of C in the batch's rows (read after the symbolic sync)
   int64_t bitmap_from = 0;      // descriptors from here on are last-level chunks (width W)
   int64_t dense_sums[2] = {0, 0};  // elements and nnz of the chunks on the dense accumulator
+  int64_t* f_hrp = nullptr;     // generated products (SPGEMM_FLAG_FUSED): prefix of the rows' lengths
+  int64_t entries = 0;          // and the entries of the batch's heavy rows
 };
 
 struct spgemm_ctx {
@@ -325,6 +356,16 @@ struct spgemm_ctx {
   bool last_graph = false;     // the last numeric call ran from the graph
 
   int esc_levels = 0;           // ladder levels whose light rows take the ESC accumulator
+
+  // heavy rows without C^ (SPGEMM_FLAG_FUSED): the column split of B, kept between the phases
+  bool fused = false;
+  int32_t* d_colcnt = nullptr;  // per row of B: entries of heavy rows of A that use it
+  int32_t* d_bh = nullptr;      // B.rows x v: entries of row k in chunk c
+  int32_t* d_bo = nullptr;      // B.rows x (v + 1): offsets of the chunks inside row k
+  int32_t* d_bs_col = nullptr;  // B's entries grouped by chunk inside every row
+  double* d_bs_val = nullptr;
+  int32_t* d_seg = nullptr;     // segment table of the batch being accumulated (launch_segtable)
+  int64_t seg_cap = 0;
 
   // light rows sized by their IP bound or by HyperLogLog estimates (SPGEMM_WORKFLOW_*)
   int workflow = 0;            // the workflow the symbolic phase ran

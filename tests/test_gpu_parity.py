@@ -56,6 +56,14 @@ FORCED = [
     # short hash rows in the shared hash tables instead of expand-sort-compact
     dict(flags=4096),
     dict(flags=4096 | 2 | 4, tau=4096),
+    # heavy rows generating their products from the column-split B (no C^): one level of 8 chunks,
+    # every row heavy, 16 chunks per row, many batches, one chunk per row, hash chunks in warps only
+    dict(flags=8192, tau=16, chunk_width=32, chunks_max=4),
+    dict(flags=8192 | 1, tau=64, chunk_width=64, chunks_max=8),
+    dict(flags=8192, tau=16, chunk_width=32, chunks_max=16),
+    dict(flags=8192, tau=16, chunk_width=64, chunks_max=4, heavy_batch_elems=700),
+    dict(flags=8192 | 1, tau=32, chunk_width=512),
+    dict(flags=8192 | 1, tau=8, chunk_width=16),
 ]
 
 
@@ -70,6 +78,7 @@ def test_forced_paths(gpu_lib, kw, seed):
         assert st.rows_heavy == int((oracle.row_ip(A, B) > 0).sum())
     if kw.get("chunks_max") == 2:
         assert st.levels_run >= 2
+    assert st.fused == (1 if kw.get("flags", 0) & 8192 and st.rows_heavy > 0 else 0)
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(tau=16, chunk_width=32, chunks_max=4),
@@ -83,13 +92,14 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
     row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
     full (multisplit path, plain shared atomics in the multisplit, dense chunks in L2, direct
     split, bulk-copy staged multisplit, per-product level-0 histogram, short hash rows in
-    shared hash tables instead of expand-sort-compact)."""
+    shared hash tables instead of expand-sort-compact, heavy chunks generated from the
+    column-split B)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
     assert st.rows_heavy > 0 and st.rows_light > 0 and st.dense_elems > 0
@@ -135,12 +145,12 @@ def sample_rows(A, B, n_top=300, n_uniform=3000, seed=0):
     return np.unique(np.concatenate([top, uni]))
 
 
-@pytest.mark.parametrize("flags", [0, 256])
+@pytest.mark.parametrize("flags", [0, 256, 8192])
 def test_config3_full_size_sampled(gpu_lib, flags):
     A = synth.config(3)
     p, rp, col, val = gpu_product_device(A, A, opts(flags=flags) if flags else None)
     st = p.stats()
-    assert st.rows_heavy > 0 and st.resident == 1
+    assert st.rows_heavy > 0 and st.resident == (0 if flags & 8192 else 1)
     rowsum, _ = device_invariants(A, A, rp, col, val)
     compare_sampled_device(A, A, rp, col, val, sample_rows(A, A))
     p.close()
@@ -148,7 +158,7 @@ def test_config3_full_size_sampled(gpu_lib, flags):
     release_device_memory()
 
 
-@pytest.mark.parametrize("flags", [0, 256])
+@pytest.mark.parametrize("flags", [0, 256, 8192])
 def test_config5_full_size_sampled(gpu_lib, flags):
     M = synth.config(5)
     p, rp, col, val = gpu_product_device(M, M, opts(flags=flags) if flags else None)
@@ -207,7 +217,7 @@ def test_validate_flag_rejects_bad_column(gpu_lib):
 
 
 @pytest.mark.parametrize("case,window", [("rmat", 0), ("rmat", 20000), ("recompute", 3000), ("light", 2000),
-                                         ("rmat", 1)])
+                                         ("rmat", 1), ("fused", 3000), ("fused_batches", 3000)])
 def test_numeric_host_windows(gpu_lib, case, window):
     """spgemm_numeric_host: C computed in row windows and streamed into pinned host arrays equals
     the oracle -- one window, many windows (down to one row each), recomputed heavy batches
@@ -216,6 +226,11 @@ def test_numeric_host_windows(gpu_lib, case, window):
     import sparse_gemm_irregular_gb300 as sg
     if case == "rmat":
         A, B, kw = synth.rmat(13, 16, seed=8), None, None
+    elif case == "fused":
+        A, B, kw = synth.rmat(13, 16, seed=8), None, dict(flags=8192, tau=512, chunk_width=256)
+    elif case == "fused_batches":
+        A, B, kw = synth.rmat(13, 16, seed=8), None, dict(flags=8192, tau=512, chunk_width=256,
+                                                          heavy_batch_elems=200000)
     elif case == "recompute":
         A = synth.random_sparse(200, 180, 0.06, 3, duplicates=True, empty_rows=True, sort_rows=False)
         B = synth.random_sparse(180, 500, 0.08, 12, duplicates=True, empty_rows=True, sort_rows=False)
@@ -296,7 +311,7 @@ def test_config4_row_windows(gpu_lib):
         release_device_memory()
 
 
-@pytest.mark.parametrize("case", ["light", "resident", "recompute", "no_graph"])
+@pytest.mark.parametrize("case", ["light", "resident", "recompute", "no_graph", "fused"])
 def test_numeric_repeat_graph(gpu_lib, case):
     """Repeated numeric calls into the same arrays: the second call is captured into a CUDA graph
     and later calls replay it, where the phase has no host synchronisation (no heavy row, or
@@ -310,6 +325,8 @@ def test_numeric_repeat_graph(gpu_lib, case):
         A, kw = synth.rmat(12, 16, seed=8), dict(tau=512, chunk_width=256)
     elif case == "recompute":
         A, kw = synth.rmat(11, 16, seed=9), dict(tau=256, chunk_width=128, heavy_batch_elems=20000, flags=16)
+    elif case == "fused":
+        A, kw = synth.rmat(12, 16, seed=8), dict(tau=512, chunk_width=256, flags=sg.binding.FLAG_FUSED)
     else:
         A, kw = synth.uniform_rows(2048, 8, seed=4), dict(flags=sg.binding.FLAG_NO_GRAPH)
     dA = sg.DeviceCSR.from_host(A)
@@ -321,6 +338,8 @@ def test_numeric_repeat_graph(gpu_lib, case):
             assert st0.resident == 1 and st0.rows_heavy > 0
         if case == "recompute":
             assert st0.resident == 0 and st0.heavy_batches > 1
+        if case == "fused":
+            assert st0.fused == 1 and st0.rows_heavy > 0 and st0.resident == 0
         col = torch.empty(max(nnz, 1), dtype=torch.int32, device="cuda")
         val = torch.empty(max(nnz, 1), dtype=torch.float64, device="cuda")
         graphed, launches = [], []
@@ -335,7 +354,7 @@ def test_numeric_repeat_graph(gpu_lib, case):
             launches.append(sg.spgemm_kernel_launches() - k0)
             graphed.append(p.stats().numeric_graph)
             compare_full(A, A, rp.cpu().numpy(), col.cpu().numpy()[:nnz], val.cpu().numpy()[:nnz])
-        expect = [0, 1, 1, 1] if case in ("light", "resident") else [0, 0, 0, 0]
+        expect = [0, 1, 1, 1] if case in ("light", "resident", "fused") else [0, 0, 0, 0]
         assert graphed == expect, sg.spgemm_last_error()
         # the first call also bins the light rows by their exact size (once per handle); a replay
         # counts the kernels its graph holds
@@ -350,13 +369,16 @@ def test_numeric_repeat_graph(gpu_lib, case):
         p.close()
 
 
-@pytest.mark.parametrize("case", ["rmat_pair", "a_times_r", "a_times_r_heavy", "a_times_at"])
+@pytest.mark.parametrize("case", ["rmat_pair", "a_times_r", "a_times_r_heavy", "a_times_at", "rmat_pair_fused",
+                                  "a_times_at_fused"])
 def test_general_products(gpu_lib, case):
     """Products beyond C = A*A: an R-MAT pair A*B with B != A, a rectangular A*R with a tall
     aggregation operator R, and A*A^T of a rectangular A (heavy path forced on small inputs)."""
     kw = None
-    if case == "rmat_pair":
+    if case.startswith("rmat_pair"):
         A, B = synth.rmat(13, 16, seed=1), synth.rmat(13, 16, seed=2)
+        if case.endswith("fused"):
+            kw = dict(tau=256, chunk_width=512, flags=8192)
     elif case.startswith("a_times_r"):
         A = synth.rmat(13, 16, seed=3)
         B = synth.aggregation(A.cols, 700, seed=4, per_row=2)
@@ -365,7 +387,7 @@ def test_general_products(gpu_lib, case):
     else:
         A = synth.random_sparse(3000, 5000, 0.004, 6, duplicates=True, empty_rows=True, sort_rows=False)
         B = synth.transpose(A)
-        kw = dict(tau=128, chunk_width=256)
+        kw = dict(tau=128, chunk_width=256, flags=8192 if case.endswith("fused") else 0)
     rp, col, val, st = gpu_product(A, B, opts(**kw) if kw else None)
     compare_full(A, B, rp, col, val, threads=16)
     if kw:
