@@ -107,6 +107,13 @@ typedef struct {
   int32_t reserved;
   double hll_coef;           /* estimated workflow: capacity = ceil(coef * estimate) (0: 2.0 with
                                 32 registers, 1.5 with 64) */
+  int64_t workspace_limit;   /* most bytes of device workspace the handle may hold at once (0: no
+                                limit); an allocation past it fails with SPGEMM_ERR_OUT_OF_MEMORY */
+  int32_t debug_hash_slots;  /* tests: cap every light-row hash table at this many slots (0: off), so
+                                that longer rows overflow their table (SPGEMM_ERR_DEVICE) */
+  int32_t debug_wait_spins;  /* tests: polls allowed to the first bulk-copy wait of every block of the
+                                staged multisplit (SPGEMM_FLAG_TMA_SPLIT; 0: the normal limit), so that
+                                a test reaches its timeout path (SPGEMM_ERR_DEVICE) */
 } spgemm_options;
 
 /* Light-row sizing (Ocean page, Table 1 and the estimation-based workflow).  SYMBOLIC counts

@@ -17,6 +17,7 @@ ERRORS = {
     -1: "INVALID_ARG", -2: "INVALID_CSR", -3: "BAD_STATE", -4: "OUT_OF_MEMORY",
     -5: "OVERFLOW", -6: "DEVICE", -7: "CUDA",
 }
+ERRORS_BY_NAME = {v: k for k, v in ERRORS.items()}
 FLAG_ALL_HEAVY = 1
 FLAG_ALL_LIGHT = 2
 FLAG_NO_DENSE_LIGHT = 4
@@ -50,7 +51,8 @@ class spgemm_csr(ctypes.Structure):
 class spgemm_options(ctypes.Structure):
     _fields_ = [("tau", _i64), ("chunk_width", _i64), ("chunks_max", _i64),
                 ("heavy_batch_elems", _i64), ("smem_bytes", _i64), ("flags", _i32),
-                ("workflow", _i32), ("hll_registers", _i32), ("reserved", _i32), ("hll_coef", ctypes.c_double)]
+                ("workflow", _i32), ("hll_registers", _i32), ("reserved", _i32), ("hll_coef", ctypes.c_double),
+                ("workspace_limit", _i64), ("debug_hash_slots", _i32), ("debug_wait_spins", _i32)]
 
 
 class spgemm_plan(ctypes.Structure):

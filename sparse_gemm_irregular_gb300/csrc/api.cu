@@ -75,18 +75,27 @@ void* ws_alloc(spgemm_ctx* h, size_t bytes) {
   void* p = nullptr;
   if (h->capturing) return nullptr;  // a captured phase must not allocate: the capture is dropped
   if (bytes == 0) bytes = 16;
+  if (h->opt.workspace_limit > 0 && h->ws_bytes + bytes > static_cast<size_t>(h->opt.workspace_limit))
+    return nullptr;  // the caller's budget
   if (cudaMallocFromPoolAsync(&p, bytes, h->pool, h->st) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
   h->allocs.push_back(p);
+  h->alloc_bytes.push_back(bytes);
+  h->ws_bytes += bytes;
   return p;
 }
 
 void ws_free(spgemm_ctx* h, void* p) {
   if (!p) return;
   auto it = std::find(h->allocs.begin(), h->allocs.end(), p);
-  if (it != h->allocs.end()) h->allocs.erase(it);
+  if (it != h->allocs.end()) {
+    const size_t i = static_cast<size_t>(it - h->allocs.begin());
+    h->ws_bytes -= h->alloc_bytes[i];
+    h->alloc_bytes.erase(h->alloc_bytes.begin() + static_cast<std::ptrdiff_t>(i));
+    h->allocs.erase(it);
+  }
   cudaFreeAsync(p, h->st);
 }
 
@@ -518,7 +527,7 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
                        launch_multisplit_tma(in_ptr, part, total_in, in_col, in_val, shift, v, P.group_rows, xmap,
                                              cursor, h->d_chat_col + out_half * cap,
                                              vals ? h->d_chat_val + out_half * cap : nullptr, vals, h->sms, h->d_err,
-                                             h->st);
+                                             h->st, static_cast<uint32_t>(std::max(0, h->opt.debug_wait_spins)));
       if (!tma)
         launch_multisplit(in_ptr, part, total_in, in_col, in_val, shift, v, P.group_rows, xmap, cursor,
                           h->d_chat_col + out_half * cap, vals ? h->d_chat_val + out_half * cap : nullptr, vals, match,
@@ -1488,6 +1497,8 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
     return fail(rc);
   }
   h->lad = make_ladder(h->plan.tau);
+  if (h->opt.debug_hash_slots > 0)  // tests: tables too small for the longer rows
+    for (int i = 0; i < h->lad.n; ++i) h->lad.slots[i] = std::min<int64_t>(h->lad.slots[i], h->opt.debug_hash_slots);
   // the largest light bin's hash table must fit one block's shared memory (this also keeps the
   // products of a light row, at most tau, far below 2^31)
   if (light_smem_bytes(h->lad.slots[h->lad.n - 1], h->lad.tpr[h->lad.n - 1], false, true) > static_cast<size_t>(optin)) {
@@ -1962,6 +1973,8 @@ int spgemm_destroy(spgemm_handle h) {
   if (h->st_graph) cudaStreamDestroy(h->st_graph);
   for (void* p : h->allocs) cudaFreeAsync(p, h->st);
   h->allocs.clear();
+  h->alloc_bytes.clear();
+  h->ws_bytes = 0;
   cudaStreamSynchronize(h->st);
   for (int b = 0; b < 2; ++b) {
     if (h->ev_done[b]) cudaEventDestroy(h->ev_done[b]);

@@ -203,7 +203,7 @@ void launch_multisplit(const int64_t* row_ptr, const int2* part, int64_t total, 
 bool launch_multisplit_tma(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
                            const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
                            unsigned long long* cursor, int32_t* out_col, double* out_val, bool with_vals, int sms,
-                           uint32_t* err, cudaStream_t s);
+                           uint32_t* err, cudaStream_t s, uint32_t first_spins = 0);
 void launch_final_desc(const int64_t* reord_ptr, int64_t q0, int64_t q1, int64_t elem_base,
                        const int32_t* row, const int32_t* base, int64_t* f_start, int64_t* f_cnt,
                        int32_t* f_row, int32_t* f_base, cudaStream_t s);
@@ -313,6 +313,8 @@ struct spgemm_ctx {
 
   // workspace (device)
   std::vector<void*> allocs;
+  std::vector<size_t> alloc_bytes;  // sizes of allocs (the workspace budget counts them)
+  size_t ws_bytes = 0;              // live workspace bytes
   uint32_t* d_err = nullptr;
   int* d_counter = nullptr;     // work counter of the persistent dense accumulator
   double* d_gacc = nullptr;     // L2-resident dense accumulators (SPGEMM_FLAG_DENSE_L2)

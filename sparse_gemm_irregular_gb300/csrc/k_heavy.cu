@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
       if (VALS) out_val[dst] = __ldg(&cval[a_first + e]) * bval[src];
       const int64_t ch = static_cast<int64_t>(c) >> shift;
       row = crow[a_first + e];
-      if (ch < v) key = static_cast<int>(e * v + ch);
+      if (c >= 0 && ch < v) key = static_cast<int>(e * v + ch);
       else set_error(err, kErrBounds);
     }
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
@@ -321,7 +321,7 @@ __global__ void k_b_chunk_hist(const int64_t* __restrict__ brp, const int32_t* _
   if (k >= krows || colcnt[k] == 0) return;
   for (int64_t q = brp[k] + lane_id(); q < brp[k + 1]; q += 32) {
     const int64_t c = static_cast<int64_t>(bcol[q]) >> shift;
-    if (c < v) atomicAdd(&bh[k * v + c], 1);
+    if (c >= 0 && c < v) atomicAdd(&bh[k * v + c], 1);
     else set_error(err, kErrBounds);
   }
 }
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
       c = bcol[src];
       if (VALS) val = __ldg(&cval[a_first + e]) * bval[src];
       const int64_t ch = static_cast<int64_t>(c) >> shift;
-      if (ch < v) {
+      if (c >= 0 && ch < v) {
         key = static_cast<int>(e * v + ch);
         const int64_t gid = static_cast<int64_t>(seg_row[e]) * v + ch;
         q = xmap ? xmap[gid] : gid;

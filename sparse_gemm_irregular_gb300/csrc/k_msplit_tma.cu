@@ -7,7 +7,8 @@
 // at (its bin's run start + its rank) with the column shifted into the chunk's local range.
 //
 // Every wait on an mbarrier is bounded: after kMaxSpins failed polls the block records
-// kErrTimeout, drains its own copies in flight (again bounded) and returns.
+// kErrTimeout, drains its own copies in flight (again bounded, on the parity of the copy that
+// was waited for) and returns.  A test lowers the first wait's limit to reach that path.
 #include <algorithm>
 
 #include "internal.h"
@@ -50,8 +51,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait; returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxSpins; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t spins = kMaxSpins) {
+  for (uint32_t i = 0; i < spins; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kMsThreads, 8) k_multisplit_tma(
     const int64_t* __restrict__ rp, const int2* __restrict__ part, int64_t total, int64_t ntiles,
     const int32_t* __restrict__ in_col, const double* __restrict__ in_val, int shift, int64_t v, int64_t gr,
     const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
-    double* __restrict__ out_val, uint32_t* err) {
+    double* __restrict__ out_val, uint32_t* err, uint32_t first_spins) {
   extern __shared__ __align__(128) char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ int s_fail;
@@ -121,22 +122,25 @@ __global__ void __launch_bounds__(kMsThreads, 8) k_multisplit_tma(
   uint32_t phase = 0u;
   uint32_t pending = 1u | (t + gridDim.x < ntiles ? 2u : 0u);
   int s = 0;
+  bool first = true;
   for (; t < ntiles; t += gridDim.x, s ^= 1) {
     const int64_t g0 = t * kT;
     const int64_t g1 = min(total, g0 + kT);
     const int n = static_cast<int>(g1 - g0);
     const int body = n & ~3;
     const int2 pr = part[t];
-    // wait for the stage (bounded)
-    if (!mbar_wait(&bars[s], (phase >> s) & 1u)) {
-      if (threadIdx.x == 0) {
-        set_error(err, kErrTimeout);
-        s_fail = 1;
-      }
+    // wait for the stage (bounded; the first wait's limit can be lowered to test the timeout).
+    // Thread 0 decides for the block: on a timeout it keeps the stage pending and its parity
+    // unflipped, so the drain below waits for that very copy.
+    const bool ok = mbar_wait(&bars[s], (phase >> s) & 1u, first ? first_spins : kMaxSpins);
+    first = false;
+    if (threadIdx.x == 0 && !ok) {
+      set_error(err, kErrTimeout);
+      s_fail = 1;
     } else {
       pending &= ~(1u << s);
+      phase ^= 1u << s;
     }
-    phase ^= 1u << s;
     const Stage cur = stage(s);
     // ragged tail of the last tile: plain loads
     for (int i = body + static_cast<int>(threadIdx.x); i < n; i += blockDim.x) {
@@ -210,7 +214,7 @@ size_t multisplit_tma_smem(int64_t group_rows, int64_t nchunks) {
 bool launch_multisplit_tma(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* in_col,
                            const double* in_val, int shift, int64_t nchunks, int64_t group_rows, const int32_t* xmap,
                            unsigned long long* cursor, int32_t* out_col, double* out_val, bool with_vals, int sms,
-                           uint32_t* err, cudaStream_t s) {
+                           uint32_t* err, cudaStream_t s, uint32_t first_spins) {
   if (total == 0) return true;
   const size_t smem = multisplit_tma_smem(group_rows, nchunks);
   if (smem > 227 * 1024) return false;  // too many bins for this variant
@@ -226,7 +230,8 @@ bool launch_multisplit_tma(const int64_t* row_ptr, const int2* part, int64_t tot
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * per_sm));
   note_launch();
   kern<<<grid, kMsThreads, smem, s>>>(row_ptr, part, total, ntiles, in_col, with_vals ? in_val : nullptr, shift,
-                                      nchunks, group_rows, xmap, cursor, out_col, with_vals ? out_val : nullptr, err);
+                                      nchunks, group_rows, xmap, cursor, out_col, with_vals ? out_val : nullptr, err,
+                                      first_spins ? first_spins : kMaxSpins);
   return true;
 }
 

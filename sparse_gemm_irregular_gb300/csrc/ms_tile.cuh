@@ -53,7 +53,7 @@ __device__ __forceinline__ void ms_bins(const int64_t* rstart, int nr, int64_t p
     int b = -1;
     if (p < g1 && p >= rstart[0] && p < rstart[nr]) {
       const int64_t ch = static_cast<int64_t>(c[j]) >> shift;
-      if (ch < v) b = static_cast<int>(r * v + ch);
+      if (c[j] >= 0 && ch < v) b = static_cast<int>(r * v + ch);
       else set_error(err, kErrBounds);
     }
     bin[j] = b;

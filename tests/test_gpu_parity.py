@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element.
 
-Small and medium inputs are compared in full; the full-size workloads of the benchmark are
-compared on a sample of rows (all the heaviest rows plus a seeded uniform sample) and through
-invariants that hold at any size.  Planner overrides force the rare paths on small inputs:
+Small and medium inputs are compared in full (the full-size workloads are compared in
+test_gpu_fullsize.py); the direct split of level 0 is also checked at full size on a sample of
+rows (all the heaviest rows plus a seeded uniform sample) and through invariants that hold at
+any size.  Planner overrides force the rare paths on small inputs:
 every row heavy, several multisplit levels, light chunks at early levels, recomputation across
 many heavy batches."""
 import numpy as np
@@ -145,12 +146,14 @@ def sample_rows(A, B, n_top=300, n_uniform=3000, seed=0):
     return np.unique(np.concatenate([top, uni]))
 
 
-@pytest.mark.parametrize("flags", [0, 256, 8192])
+# the default and generating paths are compared in full at this size (test_gpu_fullsize.py);
+# here the direct split of level 0, on sampled rows and invariants
+@pytest.mark.parametrize("flags", [256])
 def test_config3_full_size_sampled(gpu_lib, flags):
     A = synth.config(3)
     p, rp, col, val = gpu_product_device(A, A, opts(flags=flags) if flags else None)
     st = p.stats()
-    assert st.rows_heavy > 0 and st.resident == (0 if flags & 8192 else 1)
+    assert st.rows_heavy > 0 and st.resident == 1
     rowsum, _ = device_invariants(A, A, rp, col, val)
     compare_sampled_device(A, A, rp, col, val, sample_rows(A, A))
     p.close()
@@ -158,7 +161,7 @@ def test_config3_full_size_sampled(gpu_lib, flags):
     release_device_memory()
 
 
-@pytest.mark.parametrize("flags", [0, 256, 8192])
+@pytest.mark.parametrize("flags", [256])
 def test_config5_full_size_sampled(gpu_lib, flags):
     M = synth.config(5)
     p, rp, col, val = gpu_product_device(M, M, opts(flags=flags) if flags else None)
@@ -254,61 +257,6 @@ def test_numeric_host_windows(gpu_lib, case, window):
     finally:
         p.close()
     compare_full(A, B, rp.numpy(), col.numpy()[:nnz], val.numpy()[:nnz], threads=16)
-
-
-def test_config4_row_windows(gpu_lib):
-    """R-MAT scale 21, edge factor 32: C (about 6e10 entries) fits neither the device nor the
-    test host.  The symbolic phase runs at full size (heavy batches recomputed, not resident);
-    the numeric phase runs in row windows (spgemm_numeric_rows) -- the heaviest rows, a middle
-    block and the last block.  Every window row is checked against C x = A (B x); every window
-    row with at most 2e6 intermediate products against the oracle."""
-    import torch
-    import sparse_gemm_irregular_gb300 as sg
-    A = synth.config(4)
-    ip = oracle.row_ip(A, A)
-    dA = sg.DeviceCSR.from_host(A)
-    p = sg.Product(dA, dA)
-    try:
-        rp, nnz = p.symbolic()
-        st = p.stats()
-        assert st.rows_heavy > 0 and st.resident == 0
-        rp_h = rp.cpu().numpy()
-        del rp
-        row_nnz = np.diff(rp_h)
-        assert rp_h[0] == 0 and rp_h[-1] == nnz and np.all(row_nnz >= 0) and np.all(row_nnz <= ip)
-        x = synth.uniform(11, synth.STREAM_SAMPLE, 0, A.cols, 0.0, 1.0)
-        brow = np.repeat(np.arange(A.rows), np.diff(A.row_ptr))
-        bx = np.bincount(brow, weights=A.val * x[A.col], minlength=A.rows)  # B x (B = A)
-        m = A.rows
-        checked = 0
-        for rb, re in [(0, 32), (m // 2, m // 2 + 8192), (m - 8192, m)]:
-            cnt = int(rp_h[re] - rp_h[rb])
-            col = torch.empty(max(cnt, 1), dtype=torch.int32, device="cuda")
-            val = torch.empty(max(cnt, 1), dtype=torch.float64, device="cuda")
-            p.numeric_rows(rb, re, col, val)
-            torch.cuda.synchronize()
-            c = col.cpu().numpy()[:cnt]
-            v = val.cpu().numpy()[:cnt]
-            del col, val
-            lrp = rp_h[rb:re + 1] - rp_h[rb]
-            rid = np.repeat(np.arange(re - rb), np.diff(lrp))
-            # sorted, unique columns in every row
-            same_row = rid[1:] == rid[:-1]
-            assert np.all(c[1:][same_row] > c[:-1][same_row])
-            # C x = A (B x), all values nonnegative
-            y = np.bincount(rid, weights=v * x[c], minlength=re - rb)
-            a0, a1 = A.row_ptr[rb], A.row_ptr[re]
-            arid = np.repeat(np.arange(re - rb), np.diff(A.row_ptr[rb:re + 1]))
-            ref = np.bincount(arid, weights=A.val[a0:a1] * bx[A.col[a0:a1]], minlength=re - rb)
-            assert np.all(np.abs(y - ref) <= 1e-11 * ref + 1e-300)
-            rows = np.arange(rb, re)
-            small = rows[ip[rows] <= 2_000_000]
-            compare_rows(A, A, rp_h - rp_h[rb], c, v, small, threads=16)
-            checked += len(small)
-        assert checked > 10000
-    finally:
-        p.close()
-        release_device_memory()
 
 
 @pytest.mark.parametrize("case", ["light", "resident", "recompute", "no_graph", "fused"])
@@ -421,3 +369,99 @@ def test_esc_short_rows(gpu_lib, case):
     for kw in (None, opts(flags=4096)):  # expand-sort-compact (default), and hash tables
         rp, col, val, st = gpu_product(A, B, kw)
         compare_full(A, B, rp, col, val, threads=8)
+
+
+def _csr(rows, cols, entries):
+    """CSR from a list of (row, col, value) in the given order (duplicates kept)."""
+    from synth import CSR
+    entries = sorted(entries, key=lambda t: t[0])  # stable: keeps the order inside each row
+    rp = np.zeros(rows + 1, np.int64)
+    for r, _, _ in entries:
+        rp[r + 1] += 1
+    return CSR(rows, cols, np.cumsum(rp), np.array([c for _, c, _ in entries], np.int32),
+               np.array([v for _, _, v in entries], np.float64))
+
+
+@pytest.mark.parametrize("kw", [None, dict(flags=1, tau=1, chunk_width=64, chunks_max=4),
+                                dict(flags=8192 | 1, tau=1, chunk_width=64, chunks_max=4)])
+def test_exact_cancellation_kept(gpu_lib, kw):
+    """An entry whose products sum to exactly 0.0 stays in C with the value 0.0 (the symbolic
+    phase fixes the structure before any value exists): A = [1 1], B = [2; -2], then a seeded
+    product where every entry of half the rows cancels, on the light path and on both heavy
+    paths."""
+    A = _csr(1, 2, [(0, 0, 1.0), (0, 1, 1.0)])
+    B = _csr(2, 1, [(0, 0, 2.0), (1, 0, -2.0)])
+    rp, col, val, _ = gpu_product(A, B, opts(**kw) if kw else None)
+    assert list(rp) == [0, 1] and list(col) == [0] and val[0] == 0.0
+    # larger: rows 2k and 2k+1 of B are equal up to the sign and own columns 4k .. 4k+3 alone;
+    # row i of A uses both rows of three pairs with the same weight when i is even (every column
+    # then receives exactly +t and -t: zero in any order), different weights when odd
+    vals = synth.uniform(31, 2, 0, 256, 0.5, 2.0)
+    ent = []
+    for k in range(64):
+        for t in range(4):
+            ent.append((2 * k, 4 * k + t, float(vals[4 * k + t])))
+            ent.append((2 * k + 1, 4 * k + t, -float(vals[4 * k + t])))
+    B2 = _csr(128, 300, ent)
+    aent = []
+    for i in range(200):
+        for j in range(3):
+            k = (7 * i + 13 * j) % 64
+            w = 0.5 + j
+            aent.append((i, 2 * k, w))
+            aent.append((i, 2 * k + 1, w if i % 2 == 0 else 2 * w))
+    A2 = _csr(200, 128, aent)
+    rp, col, val, _ = gpu_product(A2, B2, opts(**kw) if kw else None)
+    compare_full(A2, B2, rp, col, val)
+    even = np.concatenate([np.arange(rp[i], rp[i + 1]) for i in range(0, 200, 2)])
+    assert len(even) > 0 and np.all(val[even] == 0.0)  # present, exactly zero
+
+
+def test_rows_at_tau(gpu_lib):
+    """Rows with exactly tau intermediate products stay light, tau + 1 go heavy (gMAGNUS page,
+    Algorithm 3, ThreshPartition: heavy means more than tau)."""
+    tau = 64
+    B = synth.random_sparse(40, 2000, 0.004, 41)            # rows of about 8 entries
+    lens = np.diff(B.row_ptr)
+    rng = np.random.default_rng(5)
+    ent = []
+    want = []
+    for i in range(120):
+        target = tau + (i % 3) - 1                            # tau - 1, tau, tau + 1
+        s, row = 0, []
+        while s < target:
+            k = int(rng.integers(0, 40))
+            if lens[k] == 0 or s + lens[k] > target:
+                k = next((kk for kk in range(40) if 0 < lens[kk] <= target - s), None)
+                if k is None:
+                    break
+            row.append(k)
+            s += lens[k]
+        if s != target:
+            continue
+        want.append(s)
+        ent += [(len(want) - 1, k, 1.0 + 0.1 * j) for j, k in enumerate(row)]
+    A = _csr(len(want), 40, ent)
+    ip = oracle.row_ip(A, B)
+    assert np.array_equal(ip, want) and {tau - 1, tau, tau + 1} <= set(ip.tolist())
+    for flags in (0, 8192):
+        rp, col, val, st = gpu_product(A, B, opts(tau=tau, chunk_width=256, flags=flags))
+        assert st.rows_heavy == int((ip > tau).sum())
+        compare_full(A, B, rp, col, val)
+
+
+@pytest.mark.parametrize("flags", [0, 8192])
+def test_chunks_at_dense_switch(gpu_lib, flags):
+    """Final chunks of exactly 1024 elements take a hash accumulator, 1025 the dense one (the
+    hash/dense switch of the last level); chunk width 2048, one heavy row per case."""
+    W = 2048
+    ent_b = [(0, c, 1.0 + c / 4096) for c in range(1024)]                 # 1024 columns in chunk 0
+    ent_b += [(1, W + c, 0.5 + c / 8192) for c in range(1025)]            # 1025 columns in chunk 1
+    ent_b += [(2, c * 2, 2.0) for c in range(512)]                        # 512 columns in chunk 0
+    B = _csr(3, 2 * W, ent_b)
+    A = _csr(3, 3, [(0, 0, 1.5), (0, 1, -0.5),                            # chunks of 1024 and 1025
+                    (1, 2, 1.0), (1, 2, 3.0), (1, 0, 0.25),               # 1024 + 1024 duplicates-heavy
+                    (2, 1, 2.0)])                                         # one chunk of 1025
+    rp, col, val, st = gpu_product(A, B, opts(tau=1000, chunk_width=W, flags=flags))
+    assert st.rows_heavy == 3 and st.chunks_dense >= 2
+    compare_full(A, B, rp, col, val)
