@@ -377,9 +377,11 @@ def main():
     ap.add_argument("--rmat-scale", type=int, default=0,
                     help="replace the workload by a seeded R-MAT of this scale (small cases for profiling)")
     ap.add_argument("--edge-factor", type=int, default=16)
-    ap.add_argument("--variants", action="store_true",
-                    help="also measure the variants (direct split, upper-bound and estimated light rows) "
-                         "on the headline workload")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the variants of the headline product (the separate level-0 multisplit pass, "
+                         "chunks generated from the column-split B)")
+    ap.add_argument("--all-variants", action="store_true",
+                    help="also the light rows sized by their IP bound or by HyperLogLog estimates")
     ap.add_argument("--workflow", type=int, default=0,
                     help="light-row sizing: 0 exact symbolic, 1 IP upper bound, 2 HyperLogLog, 3 automatic")
     args = ap.parse_args()
@@ -433,10 +435,11 @@ def main():
     dom_ms, dom_n = phase_tot.get(dom, [0.0, 0])
     roofline = None
     byt = kernel_bytes(dom, st)
+    kname = "k_outer_direct" if (dom == "outer_product" and st.direct_split) else KERNEL_OF.get(dom, dom)
     if dom_n and byt:
         achieved = byt * args.steps / (dom_ms / 1e3) / 1e9   # algorithmic bytes / device time
-        traffic = measured_traffic(KERNEL_OF.get(dom, ""), cfg_name)
-        roofline = {"kernel": KERNEL_OF.get(dom, dom), "bound": "hbm", "achieved": achieved, "peak": peak,
+        traffic = measured_traffic(kname, cfg_name)
+        roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                     "algorithmic_bytes_per_step": byt,
                     "algorithmic_bytes_per_launch": byt * args.steps / dom_n,
@@ -451,6 +454,7 @@ def main():
         "config": {"workload": cfg_name, "m": A.rows, "nnz_A": A.nnz, "ip_total": ip, "nnz_C": c_nnz,
                    "rows_heavy": st.rows_heavy, "ip_heavy": st.ip_heavy,
                    "heavy_batches": st.heavy_batches, "resident": st.resident,
+                   "level0_split": "inside the outer product" if st.direct_split else "separate multisplit pass",
                    "numeric_windows": nwin,
                    "light_rows": ("exact symbolic", "IP upper bound", "HyperLogLog estimate")[st.workflow],
                    "l2": "512 MiB buffer written between timed steps (outside the step events)",
@@ -464,20 +468,25 @@ def main():
         "step_ms": step_ms,
     }
 
-    # the same product on other paths, measured the same way: the direct split of level 0
-    # (SPGEMM_FLAG_DIRECT_SPLIT) and the light rows sized by their IP bound or by HyperLogLog
-    # estimates instead of the exact symbolic pass (SPGEMM_WORKFLOW_UPPER_BOUND / _ESTIMATE)
-    if args.variants:
+    # the same product on other paths, measured the same way (fewer steps): the paper's flow of
+    # a separate outer product and level-0 multisplit pass (SPGEMM_FLAG_EXPAND_SPLIT), the heavy
+    # chunks generated from the column-split B (SPGEMM_FLAG_FUSED), and on request the light rows
+    # sized by their IP bound or by HyperLogLog estimates (SPGEMM_WORKFLOW_UPPER_BOUND / _ESTIMATE)
+    if not args.no_variants:
         result["variants"] = {}
-        for name, vflags, vwf in (("direct_split", sg.binding.FLAG_DIRECT_SPLIT, args.workflow),
-                                  ("upper_bound", 0, sg.binding.WORKFLOW_UPPER_BOUND),
-                                  ("estimate", 0, sg.binding.WORKFLOW_ESTIMATE)):
+        todo = [("expanded_multisplit", sg.binding.FLAG_EXPAND_SPLIT, args.workflow),
+                ("generated_chunks", sg.binding.FLAG_FUSED, args.workflow)]
+        if args.all_variants:
+            todo += [("upper_bound", 0, sg.binding.WORKFLOW_UPPER_BOUND),
+                     ("estimate", 0, sg.binding.WORKFLOW_ESTIMATE)]
+        vsteps = min(args.steps, 5)
+        for name, vflags, vwf in todo:
             vopt = sg.options(flags=sg.binding.FLAG_TIMING | vflags | args.flags, chunk_width=args.chunk_width,
                               tau=args.tau, workflow=vwf)
-            vt, vst, vph, _, _, _ = timed_steps(w, stream, flush, args.steps, 2, vopt, vopt, world)
+            vt, vst, vph, _, _, _ = timed_steps(w, stream, flush, vsteps, 2, vopt, vopt, world)
             result["variants"][name] = {
-                "value": job_rate(ip, args.steps, world, vt), "unit": UNIT,
-                "ms_per_step": vt * 1e3 / args.steps, "phases_ms_per_step": phase_table(vph, args.steps)}
+                "value": job_rate(ip, vsteps, world, vt), "unit": UNIT, "steps": vsteps,
+                "ms_per_step": vt * 1e3 / vsteps, "phases_ms_per_step": phase_table(vph, vsteps)}
 
     # end to end through the public API with host buffers
     if not args.no_e2e:
@@ -534,8 +543,8 @@ def e2e(args, w, sg, torch, stream, world):
     spgemm_numeric_host (row windows computed on the device, each finished window copied out
     while the next is computed).  A C larger than the host (the R-MAT scale 21 product) is
     computed window by window with spgemm_numeric_rows into two device buffers, and each window
-    is copied into a reused pinned host buffer on a second stream while the next window is
-    computed: the host receives every entry of C, one window at a time."""
+    is copied, piece by piece, into a reused pinned host buffer on a second stream while the next
+    window is computed: every entry of C crosses to the host, one piece at a time."""
     A = w.A
     torch.cuda.synchronize()
     sg.spgemm_release_memory()
@@ -578,12 +587,10 @@ def e2e(args, w, sg, torch, stream, world):
                 piece = 1 << 27  # entries per host copy piece (1.5 GB of col + val)
                 win = {"dev": [(torch.empty(wmax, dtype=torch.int32, device="cuda"),
                                 torch.empty(wmax, dtype=torch.float64, device="cuda")) for _ in range(2)],
-                       "host": [(torch.empty(piece, dtype=torch.int32).pin_memory(),
-                                 torch.empty(piece, dtype=torch.float64).pin_memory()) for _ in range(2)],
-                       "piece": piece, "done": [torch.cuda.Event() for _ in range(2)],
-                       "hdone": [torch.cuda.Event() for _ in range(2)]}
+                       "host": (torch.empty(piece, dtype=torch.int32).pin_memory(),
+                                torch.empty(piece, dtype=torch.float64).pin_memory()),
+                       "piece": piece, "done": [torch.cuda.Event() for _ in range(2)]}
             rp_host = p.row_ptr.cpu().numpy()
-            hk = 0
             for wi, (rb, re) in enumerate(zip(cuts[:-1], cuts[1:])):
                 b = wi % 2
                 dcol, dval = win["dev"][b]
@@ -594,16 +601,14 @@ def e2e(args, w, sg, torch, stream, world):
                 ev.record(stream)
                 copy_stream.wait_event(ev)
                 n = int(rp_host[re] - rp_host[rb])
+                # the window goes to the host piece by piece, in stream order on the copy stream
+                # (each piece lands before the next overwrites it), while the next window computes
                 with torch.cuda.stream(copy_stream):
+                    hc, hv = win["host"]
                     for o in range(0, n, win["piece"]):
                         e_ = min(n, o + win["piece"])
-                        hc, hv = win["host"][hk % 2]
-                        if hk >= 2:
-                            win["hdone"][hk % 2].synchronize()
                         hc[:e_ - o].copy_(dcol[o:e_], non_blocking=True)
                         hv[:e_ - o].copy_(dval[o:e_], non_blocking=True)
-                        win["hdone"][hk % 2].record(copy_stream)
-                        hk += 1
                 win["done"][b].record(copy_stream)
             stream.wait_stream(copy_stream)
         t1.record(stream)

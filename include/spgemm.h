@@ -69,7 +69,12 @@ extern "C" {
                                          per-B-row chunk counts summed over the rows of A */
 #define SPGEMM_FLAG_DIRECT_SPLIT 256  /* one-level plans: the outer product writes straight into
                                          C^_reord (counts from per-B-row chunk histograms), so C^
-                                         is never stored and level 0 needs no multisplit pass */
+                                         is never stored and level 0 needs no multisplit pass.
+                                         The default since it measured faster; kept for callers
+                                         that set it */
+#define SPGEMM_FLAG_EXPAND_SPLIT 16384 /* one-level plans too: the outer product writes C^ and a
+                                         separate multisplit pass builds C^_reord (the paper's
+                                         flow; also taken with NO_MATCH, TMA_SPLIT or FUSED_HIST) */
 #define SPGEMM_FLAG_NO_GRAPH 2048    /* never capture or replay the numeric phase as a CUDA graph */
 #define SPGEMM_FLAG_FUSED 8192       /* heavy rows without the intermediate matrix in HBM: the
                                         rows of B are split once by column chunk, and every
@@ -172,7 +177,7 @@ typedef struct {
   int32_t workflow;          /* SPGEMM_WORKFLOW_* the symbolic phase ran (after AUTO)      */
   int32_t hll_registers;     /* registers per sketch (estimated workflow), else 0          */
   int32_t fused;             /* 1: heavy rows generated their products (SPGEMM_FLAG_FUSED)  */
-  int32_t reserved;
+  int32_t direct_split;      /* 1: level 0 split inside the outer product (one-level plans)  */
 } spgemm_stats;
 
 typedef struct spgemm_ctx* spgemm_handle;

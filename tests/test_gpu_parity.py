@@ -65,6 +65,9 @@ FORCED = [
     dict(flags=8192, tau=16, chunk_width=64, chunks_max=4, heavy_batch_elems=700),
     dict(flags=8192 | 1, tau=32, chunk_width=512),
     dict(flags=8192 | 1, tau=8, chunk_width=16),
+    # one-level plans through the separate outer product and multisplit pass
+    dict(flags=16384 | 1, tau=64, chunk_width=64, chunks_max=8),
+    dict(flags=16384, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
 ]
 
 
@@ -93,14 +96,14 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192, 16384])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
     row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
     full (multisplit path, plain shared atomics in the multisplit, dense chunks in L2, direct
     split, bulk-copy staged multisplit, per-product level-0 histogram, short hash rows in
     shared hash tables instead of expand-sort-compact, heavy chunks generated from the
-    column-split B)."""
+    column-split B, the separate multisplit pass of a one-level plan)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
     assert st.rows_heavy > 0 and st.rows_light > 0 and st.dense_elems > 0
@@ -146,9 +149,10 @@ def sample_rows(A, B, n_top=300, n_uniform=3000, seed=0):
     return np.unique(np.concatenate([top, uni]))
 
 
-# the default and generating paths are compared in full at this size (test_gpu_fullsize.py);
-# here the direct split of level 0, on sampled rows and invariants
-@pytest.mark.parametrize("flags", [256])
+# the default (level 0 split inside the outer product) and generating paths are compared in full
+# at this size (test_gpu_fullsize.py); here the separate multisplit pass, on sampled rows and
+# invariants
+@pytest.mark.parametrize("flags", [16384])
 def test_config3_full_size_sampled(gpu_lib, flags):
     A = synth.config(3)
     p, rp, col, val = gpu_product_device(A, A, opts(flags=flags) if flags else None)
@@ -161,7 +165,7 @@ def test_config3_full_size_sampled(gpu_lib, flags):
     release_device_memory()
 
 
-@pytest.mark.parametrize("flags", [256])
+@pytest.mark.parametrize("flags", [16384])
 def test_config5_full_size_sampled(gpu_lib, flags):
     M = synth.config(5)
     p, rp, col, val = gpu_product_device(M, M, opts(flags=flags) if flags else None)
