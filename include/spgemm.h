@@ -83,6 +83,12 @@ extern "C" {
                                         C^_reord (no outer product, no multisplit pass, no heavy
                                         batches to recompute); taken when a row has at most 2048
                                         chunks and B has fewer than 2^31 entries (stats.fused) */
+#define SPGEMM_FLAG_LONG_ROWS 32768  /* heavy rows by a long-row hash accumulator instead of the
+                                        outer product + multisplit + chunk accumulators: one block
+                                        per row, a shared-memory table that spills into a global
+                                        table of the row, output ordered by a bitmap of the row's
+                                        columns (after the Ocean page's hybrid accumulator for
+                                        long rows; stats.long_rows) */
 #define SPGEMM_FLAG_NO_ESC 4096      /* light hash rows with at most 64 intermediate products
                                         use the shared-memory hash table like longer rows, instead
                                         of the default expand-sort-compact accumulator held in one
@@ -178,6 +184,8 @@ typedef struct {
   int32_t hll_registers;     /* registers per sketch (estimated workflow), else 0          */
   int32_t fused;             /* 1: heavy rows generated their products (SPGEMM_FLAG_FUSED)  */
   int32_t direct_split;      /* 1: level 0 split inside the outer product (one-level plans)  */
+  int32_t long_rows;         /* 1: heavy rows by the long-row hash (SPGEMM_FLAG_LONG_ROWS)   */
+  int32_t reserved;
 } spgemm_stats;
 
 typedef struct spgemm_ctx* spgemm_handle;

@@ -578,6 +578,22 @@ int heavy_levels(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record, const in
   return SPGEMM_OK;
 }
 
+// Chunk histogram of the rows of B that some heavy row uses (final chunk width): bh[k * v + c]
+// = entries of row k in chunk c.  Computed once per handle and shared by every batch and both
+// phases (the direct split of level 0 and the generated chunks read it).
+int ensure_bh(spgemm_ctx* h) {
+  if (h->d_bh) return SPGEMM_OK;
+  const int64_t kc = h->k;
+  const int64_t v = h->plan.chunks_required;
+  SG_ALLOC(h->d_colcnt, int32_t, std::max<int64_t>(kc, 1));
+  SG_ALLOC(h->d_bh, int32_t, std::max<int64_t>(kc * v, 1));
+  cudaMemsetAsync(h->d_colcnt, 0, sizeof(int32_t) * kc, h->st);
+  cudaMemsetAsync(h->d_bh, 0, sizeof(int32_t) * kc * v, h->st);
+  launch_csc_count(h->A, h->d_heavy, h->nheavy, h->d_colcnt, h->st);
+  launch_b_chunk_hist(h->B, h->d_colcnt, ilog2_i64(h->plan.chunk_width), v, h->d_bh, h->d_err, h->st);
+  return SPGEMM_OK;
+}
+
 // Heavy batch, direct split (SPGEMM_FLAG_DIRECT_SPLIT, one-level plans): the per-(row, chunk)
 // counts come from per-B-row chunk histograms, and the outer product writes every element straight
 // into its C^_reord row, so C^ never reaches global memory and level 0 needs no multisplit pass.
@@ -618,16 +634,15 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   int64_t* rptr;
   int32_t *out_row, *out_base;
   const int64_t nout = R * v;
-  SG_ALLOC(bh, int32_t, kc * v);
+  SG_TRY(ensure_bh(h));
+  bh = h->d_bh;
   SG_ALLOC(counts, unsigned long long, nout);
   SG_ALLOC(rptr, int64_t, nout + 1);
   SG_ALLOC(out_row, int32_t, nout);
   SG_ALLOC(out_base, int32_t, nout);
   int64_t* hrp;
   SG_ALLOC(hrp, int64_t, R + 1);
-  cudaMemsetAsync(bh, 0, sizeof(int32_t) * kc * v, h->st);
   cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
-  launch_b_chunk_hist(h->B, colcnt, shift, v, bh, h->d_err, h->st);
   launch_heavy_row_len(h->A, rows, R, hrp, h->st);
   SG_TRY(scan(h, hrp, hrp, R));
   launch_row_chunk_counts(h->A, rows, R, hrp, nnzh, bh, v, counts, h->st);
@@ -665,7 +680,7 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   }
   for (void* p : {static_cast<void*>(colcnt), static_cast<void*>(colptr), static_cast<void*>(slice_off),
                   static_cast<void*>(csc_row), static_cast<void*>(csc_val), static_cast<void*>(cursor),
-                  static_cast<void*>(bh), static_cast<void*>(counts), static_cast<void*>(rptr),
+                  static_cast<void*>(counts), static_cast<void*>(rptr),
                   static_cast<void*>(out_row), static_cast<void*>(out_base), static_cast<void*>(part)})
     ws_free(h, p);
   return SPGEMM_OK;
@@ -721,15 +736,10 @@ int fused_prepare(spgemm_ctx* h, bool vals) {
   const int64_t kc = h->k;
   const int64_t v = h->plan.chunks_required;
   const int shift = ilog2_i64(h->plan.chunk_width);
-  if (!h->d_colcnt) {
-    SG_ALLOC(h->d_colcnt, int32_t, std::max<int64_t>(kc, 1));
-    SG_ALLOC(h->d_bh, int32_t, std::max<int64_t>(kc * v, 1));
+  SG_TRY(ensure_bh(h));
+  if (!h->d_bo) {
     SG_ALLOC(h->d_bo, int32_t, std::max<int64_t>(kc * (v + 1), 1));
     SG_ALLOC(h->d_bs_col, int32_t, std::max<int64_t>(h->B.nnz, 1));
-    cudaMemsetAsync(h->d_colcnt, 0, sizeof(int32_t) * kc, h->st);
-    cudaMemsetAsync(h->d_bh, 0, sizeof(int32_t) * kc * v, h->st);
-    launch_csc_count(h->A, h->d_heavy, h->nheavy, h->d_colcnt, h->st);
-    launch_b_chunk_hist(h->B, h->d_colcnt, shift, v, h->d_bh, h->d_err, h->st);
   }
   if (vals && !h->d_bs_val) SG_ALLOC(h->d_bs_val, double, std::max<int64_t>(h->B.nnz, 1));
   launch_bsplit(h->B, h->d_colcnt, h->d_bh, shift, v, h->d_bo, h->d_bs_col, vals ? h->d_bs_val : nullptr, h->d_err,
@@ -999,6 +1009,51 @@ void light_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
       launch_light(h->A, h->B, h->d_span_lo, job, numeric, sk, h->d_err, h->st_light);
     }
   }
+}
+
+// ---- heavy rows by the long-row hash (SPGEMM_FLAG_LONG_ROWS) -----------------------------------
+// The heavy rows in groups whose global tables fit a budget (a quarter of the free memory, at most
+// 8 GB): table slots per row from its IP (symbolic) or its nnz (numeric), a bitmap of C's columns
+// per block for the ordered write.  Numeric rows outside [sk.row_begin, sk.row_end) are skipped.
+int long_pass(spgemm_ctx* h, bool numeric, const Sink& sk) {
+  const int64_t R = h->nheavy;
+  if (R == 0) return SPGEMM_OK;
+  PhaseTimer t(h, numeric ? 11 : 7);
+  int64_t* cap;
+  SG_ALLOC(cap, int64_t, R + 1);
+  launch_long_caps(h->d_heavy, R, h->d_ip, numeric ? h->c_row_ptr : nullptr, cap, h->st);
+  SG_TRY(scan(h, cap, cap, R));
+  std::vector<int64_t> pre(static_cast<size_t>(R + 1));
+  SG_TRY(check_cuda(cudaMemcpyAsync(pre.data(), cap, sizeof(int64_t) * (R + 1), cudaMemcpyDeviceToHost, h->st),
+                    "copy long-row tables"));
+  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "long-row tables"));
+  size_t fr = 0, tot = 0;
+  cudaMemGetInfo(&fr, &tot);
+  const int64_t slot_bytes = numeric ? 12 : 4;
+  const int64_t budget = std::max<int64_t>(std::min<int64_t>(int64_t(8) << 30, static_cast<int64_t>(fr / 4)),
+                                           (pre[1] - pre[0]) * slot_bytes);
+  const int blocks = long_blocks(h->sms);
+  const int64_t nwords = (h->n + 31) / 32;
+  uint32_t* bits = nullptr;
+  if (numeric) SG_ALLOC(bits, uint32_t, std::max<int64_t>(2 * nwords * blocks, 1));
+  int64_t j0 = 0;
+  while (j0 < R) {
+    int64_t j1 = j0 + 1;  // at least one row, then as many as fit the budget
+    while (j1 < R && (pre[j1 + 1] - pre[j0]) * slot_bytes <= budget) ++j1;
+    const int64_t slots = pre[j1] - pre[j0];
+    int32_t* gkeys;
+    double* gvals = nullptr;
+    SG_ALLOC(gkeys, int32_t, slots);
+    if (numeric) SG_ALLOC(gvals, double, slots);
+    launch_long(h->A, h->B, h->d_heavy + j0, j1 - j0, cap + j0, pre[j0], gkeys, gvals, bits, nwords, numeric, sk,
+                blocks, h->d_err, h->st);
+    ws_free(h, gkeys);
+    if (gvals) ws_free(h, gvals);
+    j0 = j1;
+  }
+  if (bits) ws_free(h, bits);
+  ws_free(h, cap);
+  return SPGEMM_OK;
 }
 
 // ---- estimated light-row sizing (Ocean page: Table 1, the estimation-based workflow) -------
@@ -1281,6 +1336,7 @@ int numeric_enqueue(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, doubl
       launch_copy_rows(h->d_est_list[b], h->est_count[b], h->d_row_tmp, h->c_row_ptr, rb, re,
                        h->d_tmp_col[b == 2 ? 1 : 0], h->d_tmp_val[b == 2 ? 1 : 0], c_col, c_val, b > 0, h->st);
   }
+  if (h->long_rows) SG_TRY(long_pass(h, true, sk));
   bool split = false;
   for (auto& hb : h->batches) {
     if (hb.row_hi < rb || hb.row_lo >= re) continue;
@@ -1370,7 +1426,7 @@ int numeric_window(spgemm_ctx* h, int64_t rb, int64_t re, int32_t* c_col, double
     return SPGEMM_ERR_BAD_STATE;
   }
   h->last_graph = false;
-  const bool graphable = !h->timing && !(h->opt.flags & SPGEMM_FLAG_NO_GRAPH) &&
+  const bool graphable = !h->timing && !(h->opt.flags & SPGEMM_FLAG_NO_GRAPH) && !h->long_rows &&
                          (h->batches.empty() || h->resident || h->fused);
   if (graphable) {
     SG_TRY(numeric_bins(h));  // its one synchronisation stays outside any capture
@@ -1602,7 +1658,19 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
       SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "ip total"));
       ws_free(h, tmp);
     }
-    if (h->nheavy > 0) {
+    if (h->nheavy > 0 && (h->opt.flags & SPGEMM_FLAG_LONG_ROWS) && h->n <= 0x7fffffffLL) {
+      // heavy rows by the long-row hash: no expansion, no batches
+      h->long_rows = true;
+      h->stats.long_rows = 1;
+      std::vector<int64_t> hp(h->nheavy + 1);
+      SG_ALLOC(h->d_heavy_pre, int64_t, h->nheavy + 1);
+      launch_gather_ip(h->d_heavy, h->nheavy, h->d_ip, h->d_heavy_pre, h->st);
+      SG_TRY(scan(h, h->d_heavy_pre, h->d_heavy_pre, h->nheavy));
+      SG_TRY(check_cuda(cudaMemcpyAsync(hp.data(), h->d_heavy_pre + h->nheavy, sizeof(int64_t), cudaMemcpyDeviceToHost,
+                                        h->st), "copy heavy IP"));
+      SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "heavy IP"));
+      h->stats.ip_heavy = hp[0];
+    } else if (h->nheavy > 0) {
       h->fused = (h->opt.flags & SPGEMM_FLAG_FUSED) && h->plan.chunks_required <= kFusedMaxChunks &&
                  h->B.nnz < (int64_t(1) << 31);
       h->stats.fused = h->fused ? 1 : 0;
@@ -1688,6 +1756,7 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
     light_pass(h, false, sk);
   }
   int64_t levels = 0, finals = 0, dense = 0;
+  if (h->long_rows) SG_TRY(long_pass(h, false, sk));
   if (h->fused && !h->batches.empty()) SG_TRY(fused_prepare(h, false));
   for (auto& hb : h->batches) {
     if (h->fused) {

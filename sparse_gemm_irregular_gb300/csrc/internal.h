@@ -151,6 +151,18 @@ void launch_copy_rows(const int32_t* rows, int64_t n, const int64_t* row_tmp, co
                       int64_t row_begin, int64_t row_end, const int32_t* tcol, const double* tval, int32_t* ccol,
                       double* cval, bool wide, cudaStream_t s);
 
+// ---- long rows by a shared + global hash (k_long.cu) -------------------------------------------
+size_t long_smem_bytes(bool numeric);
+int long_blocks(int sms);
+// rows[0..nrows) of a group, global table of row j at slots [goff[j] - gbase, goff[j+1] - gbase) of
+// gkeys / gvals; gbits: 2 * nwords words per block (numeric); symbolic writes sink.row_nnz
+void launch_long(const spgemm_csr& A, const spgemm_csr& B, const int32_t* rows, int64_t nrows, const int64_t* goff,
+                 int64_t gbase, int32_t* gkeys, double* gvals, uint32_t* gbits, int64_t nwords, bool numeric,
+                 const Sink& sink, int blocks, uint32_t* err, cudaStream_t s);
+// cap[j] = global table slots of rows[j]: the power of two >= 2 x (ip[row], or its nnz from row_ptr)
+void launch_long_caps(const int32_t* rows, int64_t n, const int64_t* ip, const int64_t* row_ptr, int64_t* cap,
+                      cudaStream_t s);
+
 // ---- Markov-clustering step (k_mcl.cu) -----------------------------------------------------
 void launch_col_sums(const spgemm_csr& C, double* sums, cudaStream_t s);  // sums zeroed by the caller
 void launch_keep_count(const spgemm_csr& C, const double* sums, double thr, int64_t* counts, cudaStream_t s);
@@ -366,6 +378,7 @@ struct spgemm_ctx {
   int32_t* d_bo = nullptr;      // B.rows x (v + 1): offsets of the chunks inside row k
   int32_t* d_bs_col = nullptr;  // B's entries grouped by chunk inside every row
   double* d_bs_val = nullptr;
+  bool long_rows = false;       // heavy rows by the shared + global hash (SPGEMM_FLAG_LONG_ROWS)
   int32_t* d_seg = nullptr;     // segment table of the batch being accumulated (launch_segtable)
   int64_t seg_cap = 0;
 

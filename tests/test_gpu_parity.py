@@ -65,6 +65,10 @@ FORCED = [
     dict(flags=8192, tau=16, chunk_width=64, chunks_max=4, heavy_batch_elems=700),
     dict(flags=8192 | 1, tau=32, chunk_width=512),
     dict(flags=8192 | 1, tau=8, chunk_width=16),
+    # heavy rows by the long-row hash (shared table spilling to a global one): small shared tables
+    # would not spill on these sizes, so every row is heavy and long enough
+    dict(flags=32768 | 1, tau=16),
+    dict(flags=32768, tau=64, heavy_batch_elems=700),
     # one-level plans through the separate outer product and multisplit pass
     dict(flags=16384 | 1, tau=64, chunk_width=64, chunks_max=8),
     dict(flags=16384, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
@@ -96,17 +100,20 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192, 16384])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192, 16384, 32768])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
     row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
     full (multisplit path, plain shared atomics in the multisplit, dense chunks in L2, direct
     split, bulk-copy staged multisplit, per-product level-0 histogram, short hash rows in
     shared hash tables instead of expand-sort-compact, heavy chunks generated from the
-    column-split B, the separate multisplit pass of a one-level plan)."""
+    column-split B, the separate multisplit pass of a one-level plan, heavy rows by the long-row
+    hash)."""
     A = synth.rmat(14, 16, seed=5)
     rp, col, val, st = gpu_product(A, A, opts(flags=flags) if flags else None)
-    assert st.rows_heavy > 0 and st.rows_light > 0 and st.dense_elems > 0
+    assert st.rows_heavy > 0 and st.rows_light > 0
+    assert st.dense_elems > 0 or flags & 32768
+    assert st.long_rows == (1 if flags & 32768 else 0)
     compare_full(A, A, rp, col, val, threads=16)
 
 
@@ -224,7 +231,7 @@ def test_validate_flag_rejects_bad_column(gpu_lib):
 
 
 @pytest.mark.parametrize("case,window", [("rmat", 0), ("rmat", 20000), ("recompute", 3000), ("light", 2000),
-                                         ("rmat", 1), ("fused", 3000), ("fused_batches", 3000)])
+                                         ("rmat", 1), ("fused", 3000), ("fused_batches", 3000), ("long", 3000)])
 def test_numeric_host_windows(gpu_lib, case, window):
     """spgemm_numeric_host: C computed in row windows and streamed into pinned host arrays equals
     the oracle -- one window, many windows (down to one row each), recomputed heavy batches
@@ -235,6 +242,8 @@ def test_numeric_host_windows(gpu_lib, case, window):
         A, B, kw = synth.rmat(13, 16, seed=8), None, None
     elif case == "fused":
         A, B, kw = synth.rmat(13, 16, seed=8), None, dict(flags=8192, tau=512, chunk_width=256)
+    elif case == "long":
+        A, B, kw = synth.rmat(13, 16, seed=8), None, dict(flags=32768, tau=512)
     elif case == "fused_batches":
         A, B, kw = synth.rmat(13, 16, seed=8), None, dict(flags=8192, tau=512, chunk_width=256,
                                                           heavy_batch_elems=200000)
