@@ -89,6 +89,11 @@ extern "C" {
                                         table of the row, output ordered by a bitmap of the row's
                                         columns (after the Ocean page's hybrid accumulator for
                                         long rows; stats.long_rows) */
+#define SPGEMM_FLAG_NO_GEN_SYMBOLIC 65536 /* products whose heavy expansion is recomputed in the
+                                        numeric phase (stats.resident == 0) count their heavy
+                                        chunks in the symbolic phase from products generated out of
+                                        the column-split B, not from an expansion of the columns;
+                                        this flag keeps the column expansion (stats.gen_symbolic) */
 #define SPGEMM_FLAG_NO_ESC 4096      /* light hash rows with at most 64 intermediate products
                                         use the shared-memory hash table like longer rows, instead
                                         of the default expand-sort-compact accumulator held in one
@@ -185,7 +190,7 @@ typedef struct {
   int32_t fused;             /* 1: heavy rows generated their products (SPGEMM_FLAG_FUSED)  */
   int32_t direct_split;      /* 1: level 0 split inside the outer product (one-level plans)  */
   int32_t long_rows;         /* 1: heavy rows by the long-row hash (SPGEMM_FLAG_LONG_ROWS)   */
-  int32_t reserved;
+  int32_t gen_symbolic;      /* 1: heavy chunks counted from generated products in symbolic */
 } spgemm_stats;
 
 typedef struct spgemm_ctx* spgemm_handle;

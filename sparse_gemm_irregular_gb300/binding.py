@@ -34,6 +34,7 @@ FLAG_NO_ESC = 4096
 FLAG_FUSED = 8192
 FLAG_EXPAND_SPLIT = 16384
 FLAG_LONG_ROWS = 32768
+FLAG_NO_GEN_SYMBOLIC = 65536
 WORKFLOW_SYMBOLIC, WORKFLOW_UPPER_BOUND, WORKFLOW_ESTIMATE, WORKFLOW_AUTO = 0, 1, 2, 3
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",
@@ -72,7 +73,7 @@ class spgemm_stats(ctypes.Structure):
                 ("chat_bytes", _i64), ("c_nnz_heavy", _i64), ("dense_elems", _i64), ("dense_nnz", _i64),
                 ("resident", _i32), ("numeric_graph", _i32), ("rows_overflow", _i64), ("workflow", _i32),
                 ("hll_registers", _i32), ("fused", _i32), ("direct_split", _i32), ("long_rows", _i32),
-                ("reserved", _i32)]
+                ("gen_symbolic", _i32)]
 
 
 EXPORTS = {

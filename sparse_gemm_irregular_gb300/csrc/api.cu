@@ -650,6 +650,8 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   launch_reord_meta(counts, R, v, nullptr, nullptr, nullptr, width, rptr, out_row, out_base, h->st);
   SG_TRY(scan(h, rptr, rptr, nout));
   launch_copy_i64(rptr, cursor, nout, h->st);
+  // descriptors counted from generated products (chunk-major): onto this expansion's C^_reord rows
+  if (h->gen_symbolic && !record) launch_fused_starts(rptr, hb.f_row, hb.f_base, hb.nfinal, v, shift, hb.f_start, h->st);
   int2* part;
   SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(hb.elems, kOpTile)));
   launch_partition(slice_off, kc, hb.elems, kOpTile, part, h->st);
@@ -723,8 +725,16 @@ int fused_segtable(spgemm_ctx* h, const HeavyBatch& hb, int32_t** seg) {
     SG_ALLOC(h->d_seg, int32_t, need);
     h->seg_cap = need;
   }
+  if (hb.entries > h->ecol_cap) {
+    ws_free(h, h->d_ecol);
+    h->d_ecol = nullptr;
+    h->ecol_cap = 0;
+    SG_ALLOC(h->d_ecol, int32_t, std::max<int64_t>(hb.entries, 1));
+    h->ecol_cap = hb.entries;
+  }
   *seg = h->d_seg;
-  launch_segtable(h->A, h->d_heavy + hb.h0, hb.h1 - hb.h0, hb.f_hrp, h->B, h->d_bo, v, hb.entries, *seg, h->st);
+  launch_segtable(h->A, h->d_heavy + hb.h0, hb.h1 - hb.h0, hb.f_hrp, h->B, h->d_bo, v, hb.entries, h->d_ecol, *seg,
+                  h->st);
   return SPGEMM_OK;
 }
 
@@ -816,9 +826,10 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     ws_free(h, starts);
   }
   int32_t* seg = nullptr;
-  if (h->fused) SG_TRY(fused_segtable(h, hb, &seg));
+  const bool gen = h->fused || h->gen_symbolic;  // the chunks' products are generated
   {
     PhaseTimer t(h, 7);
+    if (gen) SG_TRY(fused_segtable(h, hb, &seg));
     ChunkSet cs{};
     cs.start = hb.f_start;
     cs.cnt = hb.f_cnt;
@@ -836,7 +847,7 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
                     h->lad.slots[L], h->lad.tpr[L], false, 0, false, sk, h->d_err, h->st);
     for (int j = 0; j < 4; ++j) {        // last-level chunks: bitmaps of width W
       const int b = h->lad.n + j;
-      if (h->fused)
+      if (gen)
         launch_fused_chunks(fused_src(h, hb, seg), cs, hb.f_list + hb.f_bin_start[b],
                             hb.f_bin_start[b + 1] - hb.f_bin_start[b], h->plan.chunk_width, 0, 0, kChunkSymTpr[j], sk,
                             h->d_err, h->d_counter, h->st);
@@ -875,9 +886,9 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
 }
 
 int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
+  PhaseTimer t(h, 11);
   int32_t* seg = nullptr;
   if (h->fused) SG_TRY(fused_segtable(h, hb, &seg));
-  PhaseTimer t(h, 11);
   ChunkSet cs{};
   cs.start = hb.f_start;
   cs.cnt = hb.f_cnt;
@@ -1717,6 +1728,11 @@ int spgemm_create_ex(spgemm_handle* out, int64_t m, int64_t k, int64_t n, const 
       }
       h->batch_cap = (maxb + 15) / 16 * 16;  // keeps both halves of the C^ buffer 16-byte aligned
       h->resident = h->batches.size() == 1 && !(h->opt.flags & SPGEMM_FLAG_RECOMPUTE) && !h->fused;
+      // a recomputed expansion need not run in the symbolic phase: its chunks are counted from
+      // generated products (the column split of B), the numeric phase expands once, with values
+      h->gen_symbolic = !h->fused && !h->resident && use_direct(h) && !(h->opt.flags & SPGEMM_FLAG_NO_GEN_SYMBOLIC) &&
+                        h->plan.chunks_required <= kFusedMaxChunks && h->B.nnz < (int64_t(1) << 31);
+      h->stats.gen_symbolic = h->gen_symbolic ? 1 : 0;
       h->stats.heavy_batches = static_cast<int64_t>(h->batches.size());
       h->stats.chat_bytes = h->fused ? 0 : maxb * 12;
       h->stats.resident = h->resident ? 1 : 0;
@@ -1757,9 +1773,9 @@ int spgemm_symbolic(spgemm_handle h, int64_t* c_row_ptr, int64_t* c_nnz) {
   }
   int64_t levels = 0, finals = 0, dense = 0;
   if (h->long_rows) SG_TRY(long_pass(h, false, sk));
-  if (h->fused && !h->batches.empty()) SG_TRY(fused_prepare(h, false));
+  if ((h->fused || h->gen_symbolic) && !h->batches.empty()) SG_TRY(fused_prepare(h, false));
   for (auto& hb : h->batches) {
-    if (h->fused) {
+    if (h->fused || h->gen_symbolic) {
       SG_TRY(heavy_fused(h, hb));
       SG_TRY(heavy_chunk_symbolic(h, hb, c_row_ptr));
       levels = std::max<int64_t>(levels, 1);

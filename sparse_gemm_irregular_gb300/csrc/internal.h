@@ -248,8 +248,13 @@ struct FusedSrc {
 void launch_bsplit(const spgemm_csr& B, const int32_t* colcnt, const int32_t* bh, int shift, int64_t v,
                    int32_t* bo, int32_t* bs_col, double* bs_val, uint32_t* err, cudaStream_t s);
 // seg[c * E + e] = B_split position of chunk c of the B row of heavy entry e (c = v: the row's end)
+// (ecol: E int32 scratch, the A column of every entry)
 void launch_segtable(const spgemm_csr& A, const int32_t* rows, int64_t R, const int64_t* hrp, const spgemm_csr& B,
-                     const int32_t* bo, int64_t v, int64_t E, int32_t* seg, cudaStream_t s);
+                     const int32_t* bo, int64_t v, int64_t E, int32_t* ecol, int32_t* seg, cudaStream_t s);
+// f_start[q] = rptr[f_row[q] * v + (f_base[q] >> shift)]: generated-symbolic descriptors onto the
+// C^_reord rows of the direct split
+void launch_fused_starts(const int64_t* rptr, const int32_t* f_row, const int32_t* f_base, int64_t n, int64_t v,
+                         int shift, int64_t* f_start, cudaStream_t s);
 // final chunks of a batch from its level-0 counts, chunk-major
 void launch_fused_desc(const unsigned long long* counts, int64_t R, int64_t v, int64_t width, int64_t* f_cnt,
                        int32_t* f_row, int32_t* f_base, int64_t* f_start, cudaStream_t s);
@@ -379,8 +384,11 @@ struct spgemm_ctx {
   int32_t* d_bs_col = nullptr;  // B's entries grouped by chunk inside every row
   double* d_bs_val = nullptr;
   bool long_rows = false;       // heavy rows by the shared + global hash (SPGEMM_FLAG_LONG_ROWS)
+  bool gen_symbolic = false;    // symbolic by generated products, numeric by the direct split
   int32_t* d_seg = nullptr;     // segment table of the batch being accumulated (launch_segtable)
   int64_t seg_cap = 0;
+  int32_t* d_ecol = nullptr;    // the A column of each of its entries
+  int64_t ecol_cap = 0;
 
   // light rows sized by their IP bound or by HyperLogLog estimates (SPGEMM_WORKFLOW_*)
   int workflow = 0;            // the workflow the symbolic phase ran

@@ -123,32 +123,57 @@ void launch_fused_desc(const unsigned long long* counts, int64_t R, int64_t v, i
 // starts (c = v: where that row ends), for the E entries of a batch's heavy rows in row order
 // (hrp: prefix of the rows' lengths).  Chunk-major, so the chunk tasks of one chunk read their
 // entries' ranges coalesced and without a chain of dependent lookups (A column, then B row
-// offset, then chunk offset).  One warp per heavy row; lanes take consecutive entries, so
-// every store of a chunk's row of the table is coalesced.
-__global__ void k_segtable(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
-                           const int32_t* __restrict__ rows, int64_t R, const int64_t* __restrict__ hrp,
-                           const int64_t* __restrict__ brp, const int32_t* __restrict__ bo, int64_t v, int64_t E,
-                           int32_t* __restrict__ seg) {
+// offset, then chunk offset).  Two launches: the A column of every entry (a warp per heavy row,
+// one store per entry), then one thread per (entry, group of 32 chunks), consecutive threads on
+// consecutive entries, so every store is coalesced and no long row serialises a warp.
+__global__ void k_entry_cols(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
+                             const int32_t* __restrict__ rows, int64_t R, const int64_t* __restrict__ hrp,
+                             int32_t* __restrict__ ecol) {
   const int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (p >= R) return;
   const int64_t a0 = arp[rows[p]];
   const int64_t e0 = hrp[p];
   const int64_t L = hrp[p + 1] - e0;
-  for (int64_t j = lane_id(); j < L; j += 32) {
-    const int32_t k = acol[a0 + j];
-    const int32_t b0 = static_cast<int32_t>(brp[k]);
-    const int32_t* b = bo + static_cast<int64_t>(k) * (v + 1);
-    int32_t* out = seg + e0 + j;
-    for (int64_t c = 0; c <= v; ++c) out[c * E] = b0 + __ldg(&b[c]);
-  }
+  for (int64_t j = lane_id(); j < L; j += 32) ecol[e0 + j] = acol[a0 + j];
+}
+
+constexpr int kSegChunks = 32;  // chunks per thread of the segment table
+
+__global__ void k_segtable(const int32_t* __restrict__ ecol, int64_t E, const int64_t* __restrict__ brp,
+                           const int32_t* __restrict__ bo, int64_t v, int32_t* __restrict__ seg) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int32_t k = ecol[e];
+  const int32_t b0 = static_cast<int32_t>(brp[k]);
+  const int32_t* b = bo + static_cast<int64_t>(k) * (v + 1);
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kSegChunks;
+  const int64_t c1 = min(v + 1, c0 + kSegChunks);
+  for (int64_t c = c0; c < c1; ++c) seg[c * E + e] = b0 + __ldg(&b[c]);
 }
 
 void launch_segtable(const spgemm_csr& A, const int32_t* rows, int64_t R, const int64_t* hrp, const spgemm_csr& B,
-                     const int32_t* bo, int64_t v, int64_t E, int32_t* seg, cudaStream_t s) {
+                     const int32_t* bo, int64_t v, int64_t E, int32_t* ecol, int32_t* seg, cudaStream_t s) {
   if (R == 0 || E == 0) return;
   note_launch();
-  k_segtable<<<static_cast<unsigned>(ceil_div(R * 32, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows, R, hrp,
-                                                                         B.row_ptr, bo, v, E, seg);
+  k_entry_cols<<<static_cast<unsigned>(ceil_div(R * 32, 256)), 256, 0, s>>>(A.row_ptr, A.col_idx, rows, R, hrp, ecol);
+  note_launch();
+  const dim3 grid(static_cast<unsigned>(ceil_div(E, 256)), static_cast<unsigned>(ceil_div(v + 1, kSegChunks)));
+  k_segtable<<<grid, 256, 0, s>>>(ecol, E, B.row_ptr, bo, v, seg);
+}
+
+// Descriptors of generated-symbolic batches (chunk-major, see k_fused_desc) pointed at the C^_reord
+// rows that the direct split of level 0 builds in the numeric phase (row-major, rptr[p * v + c]).
+__global__ void k_fused_starts(const int64_t* __restrict__ rptr, const int32_t* __restrict__ frow,
+                               const int32_t* __restrict__ fbase, int64_t n, int64_t v, int shift,
+                               int64_t* __restrict__ fstart) {
+  const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (q < n) fstart[q] = rptr[static_cast<int64_t>(frow[q]) * v + (fbase[q] >> shift)];
+}
+void launch_fused_starts(const int64_t* rptr, const int32_t* f_row, const int32_t* f_base, int64_t n, int64_t v,
+                         int shift, int64_t* f_start, cudaStream_t s) {
+  if (n == 0) return;
+  note_launch();
+  k_fused_starts<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(rptr, f_row, f_base, n, v, shift, f_start);
 }
 
 // ---- product generator -----------------------------------------------------------------------
@@ -162,7 +187,9 @@ constexpr int32_t kLongSeg = 16;  // segments of at least this many products are
 // spread evenly over the block even when its row has a single window (the median heavy row of
 // R-MAT scale 18 has 28 entries).  Every lane of the warp must call it.  The next window's loads
 // are issued before the current window's products, so they are in flight together.
-template <bool VALS, typename Visit>
+// ROUNDS false: the calling warp takes the windows rfirst, rfirst + rstep, ... and every round of
+// them (the symbolic block kernels, whose bitmap updates are cheap next to the loads).
+template <bool VALS, bool ROUNDS, typename Visit>
 __device__ __forceinline__ void fused_products(const FusedSrc& f, int64_t e0, int64_t e1, int64_t abase, int64_t c,
                                                int32_t base, int rfirst, int rstep, Visit&& visit) {
   const int lane = static_cast<int>(lane_id());
@@ -182,12 +209,14 @@ __device__ __forceinline__ void fused_products(const FusedSrc& f, int64_t e0, in
     }
   };
   int round = 0;  // the same in every warp of the group
-  fetch(e0);
-  for (int64_t w = e0; w < e1; w += 32) {
+  const int64_t w_first = ROUNDS ? e0 : e0 + static_cast<int64_t>(rfirst) * 32;
+  const int64_t w_step = ROUNDS ? 32 : static_cast<int64_t>(rstep) * 32;
+  fetch(w_first);
+  for (int64_t w = w_first; w < e1; w += w_step) {
     int32_t len = nhi - nlo;
     int32_t qd = nlo;
     const double a = na;
-    fetch(w + 32);
+    fetch(w + w_step);
     // long segments (most products of power-law inputs: the long rows of B): consecutive lanes
     // sweep consecutive entries of one segment, no search
     uint32_t longs = __ballot_sync(0xffffffffu, len >= kLongSeg);
@@ -198,7 +227,7 @@ __device__ __forceinline__ void fused_products(const FusedSrc& f, int64_t e0, in
       const int32_t n = __shfl_sync(0xffffffffu, len, l);
       const double al = VALS ? __shfl_sync(0xffffffffu, a, l) : 0.0;
       for (int32_t i0 = 0; i0 < n; i0 += 32 * U, ++round) {
-        if (round % rstep != rfirst) continue;
+        if (ROUNDS && round % rstep != rfirst) continue;
         int32_t col[U];
         double bv[U];
 #pragma unroll
@@ -221,7 +250,7 @@ __device__ __forceinline__ void fused_products(const FusedSrc& f, int64_t e0, in
     const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
     qd -= incl - len;  // product fi of this lane's entry sits at B_split position qd + fi
     for (int32_t f0 = 0; f0 < total; f0 += 32 * U, ++round) {
-      if (round % rstep != rfirst) continue;
+      if (ROUNDS && round % rstep != rfirst) continue;
       int32_t col[U];
       double bv[U], av[U];
       int32_t qq[U];
@@ -302,7 +331,7 @@ __global__ void __launch_bounds__(WARP ? 32 * kCkWarpsPerBlock : 512) k_fchunk(C
   const int rfirst = WARP ? 0 : static_cast<int>(threadIdx.x >> 5);
   const int rstep = WARP ? 1 : static_cast<int>(blockDim.x >> 5);
   uint32_t* err = p.err;
-  fused_products<MODE == 1>(f, e0, e1, abase, chunk, base, rfirst, rstep, [&](int32_t lc, double v) {
+  fused_products<MODE == 1, MODE == 1>(f, e0, e1, abase, chunk, base, rfirst, rstep, [&](int32_t lc, double v) {
     if (static_cast<uint32_t>(lc) >= width) {
       set_error(err, kErrBounds);
       return;
@@ -395,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 768 / THREADS > 0 ? 768 / THREADS : 1
       }
     } else if (job.state == 1) {
       const int64_t chunk = static_cast<int64_t>(job.base) >> f.shift;
-      fused_products<true>(f, job.e0, job.e1, job.abase, chunk, job.base, warp - 1, nwork,
+      fused_products<true, true>(f, job.e0, job.e1, job.abase, chunk, job.base, warp - 1, nwork,
                            [&](int32_t lc, double v) {
         if (static_cast<uint32_t>(lc) >= width) {
           set_error(err, kErrBounds);

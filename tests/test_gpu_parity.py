@@ -69,6 +69,9 @@ FORCED = [
     # would not spill on these sizes, so every row is heavy and long enough
     dict(flags=32768 | 1, tau=16),
     dict(flags=32768, tau=64, heavy_batch_elems=700),
+    # recomputed one-level plans count their chunks from generated products by default; this
+    # keeps the column expansion in the symbolic phase
+    dict(flags=65536 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
     # one-level plans through the separate outer product and multisplit pass
     dict(flags=16384 | 1, tau=64, chunk_width=64, chunks_max=8),
     dict(flags=16384, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
