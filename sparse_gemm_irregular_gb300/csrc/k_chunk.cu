@@ -15,8 +15,9 @@
 namespace sg {
 
 // mode 0: symbolic, 1: hash numeric (the dense numeric accumulator is k_chunk_dense below)
+// Warp groups launch 8 warps per block, block groups at most 512 threads (kChunkTpr).
 template <bool WARP, int MODE>
-__global__ void __launch_bounds__(1024) k_chunk(CkParams p) {
+__global__ void __launch_bounds__(WARP ? 32 * kCkWarpsPerBlock : 512) k_chunk(CkParams p) {
   extern __shared__ __align__(16) char smem_raw[];
   CkGroup<WARP> g;
   int64_t item;
@@ -171,8 +172,11 @@ __device__ __forceinline__ void dense_fetch(const CkParams& p, int* next, DenseJ
   j->state = 1;
 }
 
-template <bool L2>
-__global__ void __launch_bounds__(1024, 1) k_chunk_dense(CkParams p, int* next, double* gacc_all) {
+// One instantiation per block size, with the register budget of three blocks per SM (the default
+// W = 8192 fits three value arrays per SM) or of one 1024-thread block.
+template <bool L2, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == 256 ? 3 : (THREADS == 512 ? 2 : 1))
+    k_chunk_dense(CkParams p, int* next, double* gacc_all) {
   extern __shared__ __align__(16) char smem_raw[];
   __shared__ DenseJob jobs[3];  // current, next, and the one the helper is fetching
   CkGroup<false> g;
@@ -329,20 +333,24 @@ void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count,
     if (gacc) {  // L2-resident accumulators (one per SM): the shared array is not needed
       const int64_t blocks = std::min<int64_t>(count, sms);
       const size_t smem = chunk_smem_bytes(width, 0, 3, false);
-      cudaFuncSetAttribute(k_chunk_dense<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      k_chunk_dense<true><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, gacc);
+      cudaFuncSetAttribute(k_chunk_dense<true, 1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+      k_chunk_dense<true, 1024><<<static_cast<unsigned>(blocks), 1024, smem, s>>>(p, counter, gacc);
     } else {
       // as many blocks per SM as the value arrays allow; the block shrinks with them (three
       // 256-thread blocks of W = 8192 beat two of 512 threads and one of 1024 at W = 16384)
       const size_t smem = chunk_smem_bytes(width, 0, 2, false);
       const int fit = static_cast<int>(smem_sm / (smem + 1024));
+      // (384-thread blocks at three per SM measured slower: 15.3 against 14.6 ms on R-MAT s18)
       const int threads = fit >= 3 ? 256 : (fit == 2 ? 512 : 1024);
-      cudaFuncSetAttribute(k_chunk_dense<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      auto kern = threads == 256 ? k_chunk_dense<false, 256>
+                                 : (threads == 512 ? k_chunk_dense<false, 512> : k_chunk_dense<false, 1024>);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       int per_sm = 1;
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_chunk_dense<false>, threads, smem);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
       if (per_sm < 1) per_sm = 1;
       const int64_t blocks = std::min<int64_t>(count, static_cast<int64_t>(sms) * per_sm);
-      k_chunk_dense<false><<<static_cast<unsigned>(blocks), threads, smem, s>>>(p, counter, nullptr);
+      kern<<<static_cast<unsigned>(blocks), threads, smem, s>>>(p, counter, nullptr);
     }
   }
 }
