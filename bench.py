@@ -246,11 +246,14 @@ def kernel_bytes(name, st):
     """Algorithmic bytes per product of a kernel that can dominate (the speed-of-light volume of
     the gMAGNUS page, section IV-C).  When C^_reord is kept from the symbolic to the numeric
     phase (stats.resident) the heavy rows are expanded once, with values; otherwise the symbolic
-    phase expands columns only and the numeric phase expands again with values."""
+    phase expands columns only and the numeric phase expands again with values -- unless the
+    symbolic phase counted the heavy chunks from generated products (stats.gen_symbolic), which
+    leaves one expansion, in the numeric phase."""
     e = st.ip_heavy
     res = bool(st.resident)
+    once = res or bool(st.gen_symbolic)   # one expansion per product, with values
     if name == "outer_product":
-        return 12 * e if res else (4 + 12) * e          # write C^ (col [+ val])
+        return 12 * e if once else (4 + 12) * e         # write C^ / C^_reord (col [+ val])
     if name == "multisplit":
         return 24 * e if res else (8 + 24) * e          # read + write C^ (col [+ val])
     if name == "chunk_symbolic":
@@ -454,6 +457,7 @@ def main():
         "config": {"workload": cfg_name, "m": A.rows, "nnz_A": A.nnz, "ip_total": ip, "nnz_C": c_nnz,
                    "rows_heavy": st.rows_heavy, "ip_heavy": st.ip_heavy,
                    "heavy_batches": st.heavy_batches, "resident": st.resident,
+                   "symbolic_heavy": "generated products" if st.gen_symbolic else "expansion",
                    "level0_split": "inside the outer product" if st.direct_split else "separate multisplit pass",
                    "numeric_windows": nwin,
                    "light_rows": ("exact symbolic", "IP upper bound", "HyperLogLog estimate")[st.workflow],
