@@ -227,6 +227,20 @@ size_t chunk_smem_bytes(int64_t width, int64_t slots, int mode, bool warp);
 void launch_chunk_bitmap(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, int mode,
                          int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter, double* gacc,
                          cudaStream_t s);
+// One chunk of the smallest hash bin, resolved against the numeric sink (cnt < 0: skipped).
+struct ChunkDesc {
+  int64_t start;     // element offset in the C^ buffers
+  int64_t out;       // first output index (relative to the sink's row window)
+  int32_t cnt;       // elements
+  int32_t expected;  // entries of C (symbolic count)
+  int32_t base;      // first column covered
+  int32_t pad;
+};
+constexpr int64_t kWarpChunkMax = 256;        // elements of the largest chunk in the smallest hash bin
+// Numeric hash accumulation of the smallest bin (chunks of at most kWarpChunkMax elements) by
+// persistent warps; desc: count scratch descriptors.
+void launch_chunk_warps(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, const Sink& sink,
+                        ChunkDesc* desc, uint32_t* err, cudaStream_t s);
 constexpr int kChunkHubSlots = 137;           // hub columns of a dense chunk (k_chunk.cu)
 
 // ---- heavy rows without C^ in HBM (k_fused.cu) ----------------------------------------------
@@ -385,6 +399,8 @@ struct spgemm_ctx {
   double* d_bs_val = nullptr;
   bool long_rows = false;       // heavy rows by the shared + global hash (SPGEMM_FLAG_LONG_ROWS)
   bool gen_symbolic = false;    // symbolic by generated products, numeric by the direct split
+  sg::ChunkDesc* d_cdesc = nullptr;  // descriptors of the smallest numeric hash bin (largest batch)
+  int64_t cdesc_cap = 0;
   int32_t* d_seg = nullptr;     // segment table of the batch being accumulated (launch_segtable)
   int64_t seg_cap = 0;
   int32_t* d_ecol = nullptr;    // the A column of each of its entries

@@ -290,6 +290,167 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 3 : (THREADS == 512 
   }
 }
 
+// ---- the smallest hash bin as persistent warps ----------------------------------------------
+// Chunks of at most kWarpChunkMax elements are the most numerous (R-MAT scale 21: 1.2e8 of them,
+// 68 elements on average), so the work that does not scale with the elements decides their cost.
+// A warp keeps its shared table across chunks and takes chunk i, i + (warps of the grid), ...:
+//   - the chunk's descriptor comes from a prepass (one 32-byte load, issued a chunk ahead);
+//   - the hash table is the smallest power of two >= 2 x elements (at least 64 slots), so the
+//     final sweep is proportional to the chunk;
+//   - the bitmap prefix is one warp scan: lane l sums its run of consecutive words;
+//   - the final sweep writes every occupied slot at its rank and empties the slots it visits,
+//     and each lane zeroes its own bitmap words, so no chunk clears the whole table.
+constexpr int kWhWarps = 8;                          // warps per block
+constexpr int kWhSlots = 2 * static_cast<int>(kWarpChunkMax);
+
+__global__ void k_chunk_desc(ChunkSet cs, const int32_t* __restrict__ list, int64_t count, Sink sink,
+                             ChunkDesc* __restrict__ desc, uint32_t* err) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const int64_t q = list[i];
+  const int64_t grow = cs.heavy_rows[cs.row[q]];
+  ChunkDesc d{};
+  d.cnt = -1;
+  const int64_t cnt = cs.cnt[q];
+  if (grow >= sink.row_begin && grow < sink.row_end) {
+    if (cnt > kWarpChunkMax) {
+      set_error(err, kErrBounds);
+    } else {
+      d.start = cs.start[q];
+      d.out = sink.row_ptr[grow] + cs.out[q] - sink.row_ptr[sink.row_begin];
+      d.cnt = static_cast<int32_t>(cnt);
+      d.expected = static_cast<int32_t>(cs.nnz[q]);
+      d.base = cs.base[q];
+    }
+  }
+  desc[i] = d;
+}
+
+__host__ __device__ inline int64_t wh_words_per_lane(int64_t width) { return ((width + 31) / 32 + 31) / 32; }
+
+__host__ __device__ inline size_t wh_group_bytes(int64_t width) {
+  const int64_t words = 32 * wh_words_per_lane(width);  // bitmap and prefix, padded to whole lane runs
+  return ck_align(words * 4) * 2 + ck_align(kWhSlots * 4) + ck_align(kWhSlots * 8);
+}
+
+__global__ void __launch_bounds__(32 * kWhWarps) k_chunk_warps(ChunkSet cs, const ChunkDesc* __restrict__ desc,
+                                                            int64_t count, int64_t width, Sink sink, uint32_t* err) {
+  extern __shared__ __align__(16) char smem_raw[];
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int P = static_cast<int>(wh_words_per_lane(width));
+  const int nwords = 32 * P;
+  char* region = smem_raw + wh_group_bytes(width) * w;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(region);
+  int32_t* pre = reinterpret_cast<int32_t*>(region + ck_align(nwords * 4));
+  int32_t* keys = reinterpret_cast<int32_t*>(region + 2 * ck_align(nwords * 4));
+  double* vals = reinterpret_cast<double*>(region + 2 * ck_align(nwords * 4) + ck_align(kWhSlots * 4));
+  for (int j = lane; j < nwords; j += 32) bits[j] = 0u;
+  for (int j = lane; j < kWhSlots; j += 32) {
+    keys[j] = kEmptyKey;
+    vals[j] = 0.0;
+  }
+  __syncwarp();
+  CkSmem s{};
+  s.bits = bits;
+  s.pre = pre;
+  s.keys = keys;
+  s.vals = vals;
+  const uint32_t uw = static_cast<uint32_t>(width);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWhWarps;
+  int64_t item = static_cast<int64_t>(blockIdx.x) * kWhWarps + w;
+  ChunkDesc d{};
+  d.cnt = -1;
+  if (item < count) d = desc[item];
+  while (item < count) {
+    const int64_t nitem = item + stride;
+    ChunkDesc nd{};
+    nd.cnt = -1;
+    if (nitem < count) nd = desc[nitem];  // in flight while this chunk is summed
+    const int n = d.cnt;
+    if (n > 0) {
+      uint32_t S = 64;
+      while (S < 2u * static_cast<uint32_t>(n) && S < static_cast<uint32_t>(kWhSlots)) S <<= 1;
+      const int32_t* col = cs.col + d.start;
+      const double* val = cs.val + d.start;
+      constexpr int U = static_cast<int>(kWarpChunkMax / 32);
+      int32_t cr[U];
+      double vr[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int f = j * 32 + lane;
+        cr[j] = -1;
+        vr[j] = 0.0;
+        if (f < n) {
+          cr[j] = __ldcs(col + f);
+          vr[j] = __ldcs(val + f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int32_t c = cr[j];
+        if (c < 0) continue;
+        if (static_cast<uint32_t>(c) >= uw) {
+          set_error(err, kErrBounds);
+          continue;
+        }
+        hash_insert(s, S, c, vr[j], err);
+      }
+      __syncwarp();
+      // rank of every word: lane l owns words [l P, l P + P)
+      int32_t run = 0;
+      for (int j = 0; j < P; ++j) run += __popc(bits[lane * P + j]);
+      const int32_t incl = warp_incl_scan(run);
+      const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      int32_t acc = incl - run;
+      for (int j = 0; j < P; ++j) {
+        pre[lane * P + j] = acc;
+        acc += __popc(bits[lane * P + j]);
+      }
+      __syncwarp();
+      const bool ok = total == d.expected;
+      if (!ok && lane == 0) set_error(err, kErrRowOverflow);
+      int32_t* c_col = sink.c_col + d.out;
+      double* c_val = sink.c_val + d.out;
+      for (uint32_t j = lane; j < S; j += 32) {
+        const int32_t k = keys[j];
+        if (k != kEmptyKey) {
+          if (ok) {
+            const int32_t r = ck_rank(s, k);
+            c_col[r] = k + d.base;
+            c_val[r] = vals[j];
+          }
+          keys[j] = kEmptyKey;
+          vals[j] = 0.0;
+        }
+      }
+      __syncwarp();
+      for (int j = 0; j < P; ++j) bits[lane * P + j] = 0u;
+      __syncwarp();
+    }
+    d = nd;
+    item = nitem;
+  }
+}
+
+void launch_chunk_warps(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, const Sink& sink,
+                        ChunkDesc* desc, uint32_t* err, cudaStream_t s) {
+  if (count == 0) return;
+  note_launch();
+  k_chunk_desc<<<static_cast<unsigned>(ceil_div(count, 256)), 256, 0, s>>>(cs, list, count, sink, desc, err);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t smem = wh_group_bytes(width) * kWhWarps;
+  cudaFuncSetAttribute(k_chunk_warps, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_chunk_warps, 32 * kWhWarps, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t blocks = std::min<int64_t>(ceil_div(count, kWhWarps), static_cast<int64_t>(sms) * per_sm);
+  note_launch();
+  k_chunk_warps<<<static_cast<unsigned>(blocks), 32 * kWhWarps, smem, s>>>(cs, desc, count, width, sink, err);
+}
+
 size_t chunk_smem_bytes(int64_t width, int64_t slots, int mode, bool warp) {
   const size_t gb = ck_group_bytes(width, slots, mode);
   return warp ? gb * kCkWarpsPerBlock : gb;

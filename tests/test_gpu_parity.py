@@ -72,6 +72,9 @@ FORCED = [
     # recomputed one-level plans count their chunks from generated products by default; this
     # keeps the column expansion in the symbolic phase
     dict(flags=65536 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
+    # the smallest numeric hash bin by one warp per chunk instead of persistent warps
+    dict(flags=131072, tau=16, chunk_width=64, chunks_max=16),
+    dict(flags=131072 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
     # one-level plans through the separate outer product and multisplit pass
     dict(flags=16384 | 1, tau=64, chunk_width=64, chunks_max=8),
     dict(flags=16384, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
@@ -103,7 +106,7 @@ def test_integer_values_exact(gpu_lib, kw):
     assert np.array_equal(val, oval)  # exact integers: any summation order gives the same bits
 
 
-@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192, 16384, 32768])
+@pytest.mark.parametrize("flags", [0, 64, 128, 256, 512, 1024, 4096, 8192, 16384, 32768, 131072])
 def test_rmat_small_full(gpu_lib, flags):
     """R-MAT scale 14, edge factor 16: heavy rows above the default tau, several chunks per
     row (dense chunks among them), thousands of light rows in every ladder bin -- compared in
