@@ -94,10 +94,11 @@ extern "C" {
                                         chunks in the symbolic phase from products generated out of
                                         the column-split B, not from an expansion of the columns;
                                         this flag keeps the column expansion (stats.gen_symbolic) */
-#define SPGEMM_FLAG_CHUNK_PER_WARP 131072 /* numeric heavy chunks of at most 256 elements: one warp
-                                        per chunk that clears and sweeps its whole 512-slot table,
-                                        instead of the default persistent warps whose tables are
-                                        sized to each chunk and emptied by the final sweep */
+#define SPGEMM_FLAG_HASH_PER_CHUNK 131072 /* numeric heavy chunks of at most 1024 elements: a warp
+                                        (at most 256 elements) or a block per chunk that clears its
+                                        table and bitmap first, instead of the default persistent
+                                        warps and blocks whose tables are sized to each chunk and
+                                        emptied by their final sweep */
 #define SPGEMM_FLAG_NO_ESC 4096      /* light hash rows with at most 64 intermediate products
                                         use the shared-memory hash table like longer rows, instead
                                         of the default expand-sort-compact accumulator held in one

@@ -35,7 +35,7 @@ FLAG_FUSED = 8192
 FLAG_EXPAND_SPLIT = 16384
 FLAG_LONG_ROWS = 32768
 FLAG_NO_GEN_SYMBOLIC = 65536
-FLAG_CHUNK_PER_WARP = 131072
+FLAG_HASH_PER_CHUNK = 131072
 WORKFLOW_SYMBOLIC, WORKFLOW_UPPER_BOUND, WORKFLOW_ESTIMATE, WORKFLOW_AUTO = 0, 1, 2, 3
 PHASES = ["setup", "light_symbolic", "masked_csc", "outer_product", "histogram", "multisplit",
           "multisplit_bookkeeping", "chunk_symbolic", "chunk_offsets", "rowptr_scan",

@@ -825,11 +825,11 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     ws_free(h, fcnt);
     ws_free(h, starts);
   }
-  if (!h->fused && !(h->opt.flags & SPGEMM_FLAG_CHUNK_PER_WARP)) {
+  if (!h->fused && !(h->opt.flags & SPGEMM_FLAG_HASH_PER_CHUNK)) {
     // descriptors of the smallest numeric hash bin: one buffer sized by the largest batch, so
     // the numeric phase allocates nothing
     const int b0 = h->lad.n;
-    const int64_t need = hb.f_bin_start[b0 + 1] - hb.f_bin_start[b0];
+    const int64_t need = hb.f_bin_start[b0 + 2] - hb.f_bin_start[b0];  // the two hash bins
     if (need > h->cdesc_cap) {
       ws_free(h, h->d_cdesc);
       h->d_cdesc = nullptr;
@@ -925,9 +925,10 @@ int heavy_chunk_numeric(spgemm_ctx* h, HeavyBatch& hb, const Sink& sk) {
       launch_fused_chunks(fused_src(h, hb, seg), cs, hb.f_list + hb.f_bin_start[b],
                           hb.f_bin_start[b + 1] - hb.f_bin_start[b], h->plan.chunk_width, j == 3 ? 2 : 1,
                           kChunkSlots[j], kChunkTpr[j], sk, h->d_err, h->d_counter, h->st);
-    else if (j == 0 && !(h->opt.flags & SPGEMM_FLAG_CHUNK_PER_WARP))
-      launch_chunk_warps(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
-                         h->plan.chunk_width, sk, h->d_cdesc, h->d_err, h->st);
+    else if (j < 2 && !(h->opt.flags & SPGEMM_FLAG_HASH_PER_CHUNK))
+      launch_chunk_groups(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
+                          h->plan.chunk_width, j == 0, sk,
+                          h->d_cdesc + (j == 0 ? 0 : hb.f_bin_start[b] - hb.f_bin_start[b - 1]), h->d_err, h->st);
     else
       launch_chunk_bitmap(cs, hb.f_list + hb.f_bin_start[b], hb.f_bin_start[b + 1] - hb.f_bin_start[b],
                           h->plan.chunk_width, j == 3 ? 2 : 1, kChunkSlots[j], kChunkTpr[j], sk, h->d_err,

@@ -237,10 +237,12 @@ struct ChunkDesc {
   int32_t pad;
 };
 constexpr int64_t kWarpChunkMax = 256;        // elements of the largest chunk in the smallest hash bin
-// Numeric hash accumulation of the smallest bin (chunks of at most kWarpChunkMax elements) by
-// persistent warps; desc: count scratch descriptors.
-void launch_chunk_warps(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, const Sink& sink,
-                        ChunkDesc* desc, uint32_t* err, cudaStream_t s);
+constexpr int64_t kBlockChunkMax = 1024;      // and in the next one
+// Numeric hash accumulation of a hash bin by persistent groups: warps for the smallest bin (chunks
+// of at most kWarpChunkMax elements), 128-thread blocks for the next (at most kBlockChunkMax);
+// desc: count scratch descriptors.
+void launch_chunk_groups(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, bool warps,
+                         const Sink& sink, ChunkDesc* desc, uint32_t* err, cudaStream_t s);
 constexpr int kChunkHubSlots = 137;           // hub columns of a dense chunk (k_chunk.cu)
 
 // ---- heavy rows without C^ in HBM (k_fused.cu) ----------------------------------------------

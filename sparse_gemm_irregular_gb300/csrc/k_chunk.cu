@@ -290,20 +290,28 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 3 : (THREADS == 512 
   }
 }
 
-// ---- the smallest hash bin as persistent warps ----------------------------------------------
-// Chunks of at most kWarpChunkMax elements are the most numerous (R-MAT scale 21: 1.2e8 of them,
-// 68 elements on average), so the work that does not scale with the elements decides their cost.
-// A warp keeps its shared table across chunks and takes chunk i, i + (warps of the grid), ...:
+// ---- the hash bins as persistent groups ---------------------------------------------------
+// Chunks of at most 1024 elements are the most numerous (R-MAT scale 21: 1.6e8 of them, 68 and
+// 522 elements on average in the two bins), so the work that does not scale with the elements
+// decides their cost.  A group (a warp for chunks of at most kWarpChunkMax elements, a 128-thread
+// block for the rest) keeps its shared table across chunks and takes chunk i, i + (groups of the
+// grid), ...:
 //   - the chunk's descriptor comes from a prepass (one 32-byte load, issued a chunk ahead);
 //   - the hash table is the smallest power of two >= 2 x elements (at least 64 slots), so the
 //     final sweep is proportional to the chunk;
 //   - the bitmap prefix is one warp scan: lane l sums its run of consecutive words;
 //   - the final sweep writes every occupied slot at its rank and empties the slots it visits,
-//     and each lane zeroes its own bitmap words, so no chunk clears the whole table.
-constexpr int kWhWarps = 8;                          // warps per block
-constexpr int kWhSlots = 2 * static_cast<int>(kWarpChunkMax);
+//     and the group zeroes the bitmap words, so no chunk clears the whole table.
+template <int T>
+struct GroupCfg {
+  static constexpr int kMax = T == 32 ? static_cast<int>(kWarpChunkMax) : static_cast<int>(kBlockChunkMax);
+  static constexpr int kSlots = 2 * kMax;
+  static constexpr int kBlock = T == 32 ? 256 : T;   // eight warp groups per block, or one block group
+  static constexpr int kGroups = kBlock / T;
+  static constexpr int kPerThread = kMax / T;        // elements per thread of the largest chunk
+};
 
-__global__ void k_chunk_desc(ChunkSet cs, const int32_t* __restrict__ list, int64_t count, Sink sink,
+__global__ void k_chunk_desc(ChunkSet cs, const int32_t* __restrict__ list, int64_t count, int64_t max_cnt, Sink sink,
                              ChunkDesc* __restrict__ desc, uint32_t* err) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= count) return;
@@ -313,7 +321,7 @@ __global__ void k_chunk_desc(ChunkSet cs, const int32_t* __restrict__ list, int6
   d.cnt = -1;
   const int64_t cnt = cs.cnt[q];
   if (grow >= sink.row_begin && grow < sink.row_end) {
-    if (cnt > kWarpChunkMax) {
+    if (cnt > max_cnt) {
       set_error(err, kErrBounds);
     } else {
       d.start = cs.start[q];
@@ -326,39 +334,55 @@ __global__ void k_chunk_desc(ChunkSet cs, const int32_t* __restrict__ list, int6
   desc[i] = d;
 }
 
-__host__ __device__ inline int64_t wh_words_per_lane(int64_t width) { return ((width + 31) / 32 + 31) / 32; }
-
-__host__ __device__ inline size_t wh_group_bytes(int64_t width) {
-  const int64_t words = 32 * wh_words_per_lane(width);  // bitmap and prefix, padded to whole lane runs
-  return ck_align(words * 4) * 2 + ck_align(kWhSlots * 4) + ck_align(kWhSlots * 8);
+// bitmap words per lane of the prefix warp (a multiple of 4, so that a lane's run is whole uint4s)
+__host__ __device__ inline int64_t grp_words_per_lane(int64_t width) {
+  const int64_t p = ((width + 31) / 32 + 31) / 32;
+  return (p + 3) & ~int64_t(3);
 }
 
-__global__ void __launch_bounds__(32 * kWhWarps) k_chunk_warps(ChunkSet cs, const ChunkDesc* __restrict__ desc,
-                                                            int64_t count, int64_t width, Sink sink, uint32_t* err) {
+template <int T>
+__host__ __device__ inline size_t grp_bytes(int64_t width) {
+  const int64_t words = 32 * grp_words_per_lane(width);  // bitmap and prefix, padded to whole lane runs
+  return ck_align(words * 4) * 2 + ck_align(GroupCfg<T>::kSlots * 4) + ck_align(GroupCfg<T>::kSlots * 8) + 16;
+}
+
+template <int T>
+__device__ __forceinline__ void grp_sync() {
+  if (T == 32) __syncwarp(); else __syncthreads();
+}
+
+template <int T>
+__global__ void __launch_bounds__(GroupCfg<T>::kBlock) k_chunk_groups(ChunkSet cs, const ChunkDesc* __restrict__ desc,
+                                                                    int64_t count, int64_t width, Sink sink,
+                                                                    uint32_t* err) {
+  using C = GroupCfg<T>;
   extern __shared__ __align__(16) char smem_raw[];
-  const int w = threadIdx.x >> 5;
+  const int gi = threadIdx.x / T;
+  const int t = threadIdx.x % T;
   const int lane = threadIdx.x & 31;
-  const int P = static_cast<int>(wh_words_per_lane(width));
+  const int P = static_cast<int>(grp_words_per_lane(width));
   const int nwords = 32 * P;
-  char* region = smem_raw + wh_group_bytes(width) * w;
+  char* region = smem_raw + grp_bytes<T>(width) * gi;
   uint32_t* bits = reinterpret_cast<uint32_t*>(region);
   int32_t* pre = reinterpret_cast<int32_t*>(region + ck_align(nwords * 4));
   int32_t* keys = reinterpret_cast<int32_t*>(region + 2 * ck_align(nwords * 4));
-  double* vals = reinterpret_cast<double*>(region + 2 * ck_align(nwords * 4) + ck_align(kWhSlots * 4));
-  for (int j = lane; j < nwords; j += 32) bits[j] = 0u;
-  for (int j = lane; j < kWhSlots; j += 32) {
+  double* vals = reinterpret_cast<double*>(region + 2 * ck_align(nwords * 4) + ck_align(C::kSlots * 4));
+  int32_t* tot = reinterpret_cast<int32_t*>(region + 2 * ck_align(nwords * 4) + ck_align(C::kSlots * 4) +
+                                            ck_align(C::kSlots * 8));
+  for (int j = t; j < nwords; j += T) bits[j] = 0u;
+  for (int j = t; j < C::kSlots; j += T) {
     keys[j] = kEmptyKey;
     vals[j] = 0.0;
   }
-  __syncwarp();
+  grp_sync<T>();
   CkSmem s{};
   s.bits = bits;
   s.pre = pre;
   s.keys = keys;
   s.vals = vals;
   const uint32_t uw = static_cast<uint32_t>(width);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWhWarps;
-  int64_t item = static_cast<int64_t>(blockIdx.x) * kWhWarps + w;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * C::kGroups;
+  int64_t item = static_cast<int64_t>(blockIdx.x) * C::kGroups + gi;
   ChunkDesc d{};
   d.cnt = -1;
   if (item < count) d = desc[item];
@@ -370,15 +394,14 @@ __global__ void __launch_bounds__(32 * kWhWarps) k_chunk_warps(ChunkSet cs, cons
     const int n = d.cnt;
     if (n > 0) {
       uint32_t S = 64;
-      while (S < 2u * static_cast<uint32_t>(n) && S < static_cast<uint32_t>(kWhSlots)) S <<= 1;
+      while (S < 2u * static_cast<uint32_t>(n) && S < static_cast<uint32_t>(C::kSlots)) S <<= 1;
       const int32_t* col = cs.col + d.start;
       const double* val = cs.val + d.start;
-      constexpr int U = static_cast<int>(kWarpChunkMax / 32);
-      int32_t cr[U];
-      double vr[U];
+      int32_t cr[C::kPerThread];
+      double vr[C::kPerThread];
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int f = j * 32 + lane;
+      for (int j = 0; j < C::kPerThread; ++j) {
+        const int f = j * T + t;
         cr[j] = -1;
         vr[j] = 0.0;
         if (f < n) {
@@ -387,7 +410,7 @@ __global__ void __launch_bounds__(32 * kWhWarps) k_chunk_warps(ChunkSet cs, cons
         }
       }
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
+      for (int j = 0; j < C::kPerThread; ++j) {
         const int32_t c = cr[j];
         if (c < 0) continue;
         if (static_cast<uint32_t>(c) >= uw) {
@@ -396,23 +419,36 @@ __global__ void __launch_bounds__(32 * kWhWarps) k_chunk_warps(ChunkSet cs, cons
         }
         hash_insert(s, S, c, vr[j], err);
       }
-      __syncwarp();
-      // rank of every word: lane l owns words [l P, l P + P)
-      int32_t run = 0;
-      for (int j = 0; j < P; ++j) run += __popc(bits[lane * P + j]);
-      const int32_t incl = warp_incl_scan(run);
-      const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
-      int32_t acc = incl - run;
-      for (int j = 0; j < P; ++j) {
-        pre[lane * P + j] = acc;
-        acc += __popc(bits[lane * P + j]);
+      grp_sync<T>();
+      // rank of every bitmap word, by the group's first warp: lane l owns words [l P, l P + P)
+      if (t < 32) {
+        const uint4* b4 = reinterpret_cast<const uint4*>(bits + lane * P);
+        int32_t run = 0;
+        for (int j = 0; j < P / 4; ++j) {
+          const uint4 x = b4[j];
+          run += __popc(x.x) + __popc(x.y) + __popc(x.z) + __popc(x.w);
+        }
+        const int32_t incl = warp_incl_scan(run);
+        int32_t acc = incl - run;
+        int4* p4 = reinterpret_cast<int4*>(pre + lane * P);
+        for (int j = 0; j < P / 4; ++j) {
+          const uint4 x = b4[j];
+          int4 o;
+          o.x = acc;
+          o.y = o.x + __popc(x.x);
+          o.z = o.y + __popc(x.y);
+          o.w = o.z + __popc(x.z);
+          acc = o.w + __popc(x.w);
+          p4[j] = o;
+        }
+        if (lane == 31) *tot = incl;
       }
-      __syncwarp();
-      const bool ok = total == d.expected;
-      if (!ok && lane == 0) set_error(err, kErrRowOverflow);
+      grp_sync<T>();
+      const bool ok = *tot == d.expected;
+      if (!ok && t == 0) set_error(err, kErrRowOverflow);
       int32_t* c_col = sink.c_col + d.out;
       double* c_val = sink.c_val + d.out;
-      for (uint32_t j = lane; j < S; j += 32) {
+      for (uint32_t j = t; j < S; j += T) {
         const int32_t k = keys[j];
         if (k != kEmptyKey) {
           if (ok) {
@@ -424,31 +460,41 @@ __global__ void __launch_bounds__(32 * kWhWarps) k_chunk_warps(ChunkSet cs, cons
           vals[j] = 0.0;
         }
       }
-      __syncwarp();
-      for (int j = 0; j < P; ++j) bits[lane * P + j] = 0u;
-      __syncwarp();
+      grp_sync<T>();
+      uint4* z4 = reinterpret_cast<uint4*>(bits);
+      for (int j = t; j < nwords / 4; j += T) z4[j] = make_uint4(0u, 0u, 0u, 0u);
+      grp_sync<T>();
     }
     d = nd;
     item = nitem;
   }
 }
 
-void launch_chunk_warps(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, const Sink& sink,
-                        ChunkDesc* desc, uint32_t* err, cudaStream_t s) {
+template <int T>
+static void groups_launch(const ChunkSet& cs, const ChunkDesc* desc, int64_t count, int64_t width, const Sink& sink,
+                          uint32_t* err, int sms, cudaStream_t s) {
+  using C = GroupCfg<T>;
+  const size_t smem = grp_bytes<T>(width) * C::kGroups;
+  cudaFuncSetAttribute(k_chunk_groups<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_chunk_groups<T>, C::kBlock, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t blocks = std::min<int64_t>(ceil_div(count, C::kGroups), static_cast<int64_t>(sms) * per_sm);
+  note_launch();
+  k_chunk_groups<T><<<static_cast<unsigned>(blocks), C::kBlock, smem, s>>>(cs, desc, count, width, sink, err);
+}
+
+void launch_chunk_groups(const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width, bool warps,
+                         const Sink& sink, ChunkDesc* desc, uint32_t* err, cudaStream_t s) {
   if (count == 0) return;
   note_launch();
-  k_chunk_desc<<<static_cast<unsigned>(ceil_div(count, 256)), 256, 0, s>>>(cs, list, count, sink, desc, err);
+  k_chunk_desc<<<static_cast<unsigned>(ceil_div(count, 256)), 256, 0, s>>>(
+      cs, list, count, warps ? kWarpChunkMax : kBlockChunkMax, sink, desc, err);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t smem = wh_group_bytes(width) * kWhWarps;
-  cudaFuncSetAttribute(k_chunk_warps, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_chunk_warps, 32 * kWhWarps, smem);
-  if (per_sm < 1) per_sm = 1;
-  const int64_t blocks = std::min<int64_t>(ceil_div(count, kWhWarps), static_cast<int64_t>(sms) * per_sm);
-  note_launch();
-  k_chunk_warps<<<static_cast<unsigned>(blocks), 32 * kWhWarps, smem, s>>>(cs, desc, count, width, sink, err);
+  if (warps) groups_launch<32>(cs, desc, count, width, sink, err, sms, s);
+  else groups_launch<128>(cs, desc, count, width, sink, err, sms, s);
 }
 
 size_t chunk_smem_bytes(int64_t width, int64_t slots, int mode, bool warp) {

@@ -773,7 +773,7 @@ __global__ void k_chunk_classify(const int64_t* __restrict__ fc, int64_t n, int6
   if (c == 0) {
     b = kBinEmpty;
   } else if (i >= bitmap_from) {
-    b = static_cast<uint8_t>(r.n + (c <= kWarpChunkMax ? 0 : (c <= 1024 ? 1 : (c <= kChunkDenseMin ? 2 : 3))));
+    b = static_cast<uint8_t>(r.n + (c <= kWarpChunkMax ? 0 : (c <= kBlockChunkMax ? 1 : (c <= kChunkDenseMin ? 2 : 3))));
   } else {
     int L = 0;
     while (L < r.n - 1 && c > r.upper[L]) ++L;

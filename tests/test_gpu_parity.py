@@ -72,7 +72,7 @@ FORCED = [
     # recomputed one-level plans count their chunks from generated products by default; this
     # keeps the column expansion in the symbolic phase
     dict(flags=65536 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
-    # the smallest numeric hash bin by one warp per chunk instead of persistent warps
+    # the two numeric hash bins by a warp or block per chunk instead of persistent groups
     dict(flags=131072, tau=16, chunk_width=64, chunks_max=16),
     dict(flags=131072 | 16, tau=16, chunk_width=64, chunks_max=16, heavy_batch_elems=700),
     # one-level plans through the separate outer product and multisplit pass
