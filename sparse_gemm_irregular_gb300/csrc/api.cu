@@ -347,14 +347,15 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr, un
   SG_TRY(check_cuda(cudaMemcpyAsync(&nnzh, colptr + kc, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
                     "copy masked nnz"));
   SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "masked csc"));
-  int32_t* csc_row;
+  int32_t *csc_row, *csc_col;
   double* csc_val;
   int64_t* cursor;
   SG_ALLOC(csc_row, int32_t, nnzh);
   SG_ALLOC(csc_val, double, nnzh);
+  SG_ALLOC(csc_col, int32_t, nnzh);
   SG_ALLOC(cursor, int64_t, std::max<int64_t>(kc, R));
   launch_copy_i64(colptr, cursor, kc, h->st);
-  launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, h->st);
+  launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, csc_col, h->st);
   // C^ row pointers: heavy IP prefix of the batch; the cursor starts at each row's first slot
   launch_offset_copy(h->d_heavy_pre + hb.h0, R + 1, h->heavy_pre[hb.h0], c_rowptr, h->st);
   launch_copy_i64(c_rowptr, cursor, R, h->st);
@@ -388,7 +389,7 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr, un
   }
   {
     PhaseTimer t(h, 3);
-    launch_outer_product(colptr, csc_row, csc_val, slice_off, part, hb.elems, h->B, cursor, h->d_chat_col,
+    launch_outer_product(colptr, csc_row, csc_val, csc_col, slice_off, part, hb.elems, h->B, cursor, h->d_chat_col,
                          vals ? h->d_chat_val : nullptr, vals, op_counts, shift0, v0, h->d_err, h->st);
   }
   ws_free(h, part);
@@ -397,6 +398,7 @@ int heavy_expand(spgemm_ctx* h, HeavyBatch& hb, bool vals, int64_t* c_rowptr, un
   ws_free(h, slice_off);
   ws_free(h, csc_row);
   ws_free(h, csc_val);
+  ws_free(h, csc_col);
   ws_free(h, cursor);
   return SPGEMM_OK;
 }
@@ -620,14 +622,15 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   SG_TRY(check_cuda(cudaMemcpyAsync(&nnzh, colptr + kc, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
                     "copy masked nnz"));
   SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "masked csc"));
-  int32_t* csc_row;
+  int32_t *csc_row, *csc_col;
   double* csc_val;
   int64_t* cursor;
   SG_ALLOC(csc_row, int32_t, nnzh);
   SG_ALLOC(csc_val, double, nnzh);
+  SG_ALLOC(csc_col, int32_t, nnzh);
   SG_ALLOC(cursor, int64_t, std::max<int64_t>(kc, R * v));
   launch_copy_i64(colptr, cursor, kc, h->st);
-  launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, h->st);
+  launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, csc_col, h->st);
   // level-0 histogram from the chunk histograms of the rows of B
   int32_t* bh;
   unsigned long long* counts;
@@ -652,13 +655,13 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   launch_copy_i64(rptr, cursor, nout, h->st);
   // descriptors counted from generated products (chunk-major): onto this expansion's C^_reord rows
   if (h->gen_symbolic && !record) launch_fused_starts(rptr, hb.f_row, hb.f_base, hb.nfinal, v, shift, hb.f_start, h->st);
-  int2* part;
-  SG_ALLOC(part, int2, std::max<int64_t>(1, ceil_div(hb.elems, kOpTile)));
-  launch_partition(slice_off, kc, hb.elems, kOpTile, part, h->st);
+  OdTile* part;
+  SG_ALLOC(part, OdTile, std::max<int64_t>(1, ceil_div(hb.elems, kOdTile)));
+  launch_od_partition(slice_off, kc, hb.elems, colptr, h->B, part, h->st);
   tcsc.reset();
   {
     PhaseTimer t(h, 3);
-    launch_outer_direct(colptr, csc_row, csc_val, slice_off, part, hb.elems, h->B, nullptr,
+    launch_outer_direct(colptr, csc_row, csc_val, csc_col, slice_off, part, hb.elems, h->B,
                         reinterpret_cast<unsigned long long*>(cursor), h->d_chat_col,
                         vals ? h->d_chat_val : nullptr, vals, shift, v, h->d_err, h->st);
   }
@@ -681,7 +684,8 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
     launch_final_desc(rptr, 0, nout, 0, out_row, out_base, hb.f_start, hb.f_cnt, hb.f_row, hb.f_base, h->st);
   }
   for (void* p : {static_cast<void*>(colcnt), static_cast<void*>(colptr), static_cast<void*>(slice_off),
-                  static_cast<void*>(csc_row), static_cast<void*>(csc_val), static_cast<void*>(cursor),
+                  static_cast<void*>(csc_row), static_cast<void*>(csc_val), static_cast<void*>(csc_col),
+                  static_cast<void*>(cursor),
                   static_cast<void*>(counts), static_cast<void*>(rptr),
                   static_cast<void*>(out_row), static_cast<void*>(out_base), static_cast<void*>(part)})
     ws_free(h, p);

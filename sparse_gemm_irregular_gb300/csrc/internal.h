@@ -19,6 +19,8 @@ constexpr int64_t kMsSmemBudget = 65536;   // bytes of shared memory per multisp
 constexpr int64_t kMsMaxBins = 2048;       // group_rows * chunks bins held by one block
 constexpr int64_t kOpTile = 1024;          // elements per outer-product block
 constexpr int kOpThreads = 128;            // (small blocks: 2048/256 measured 0.4 ms slower on R-MAT s18)
+constexpr int64_t kOdTile = 4096;          // products per block of the direct split
+constexpr int kOdWin = 256;                // entries of a direct-split tile staged at a time
 constexpr int kSmemReserve = 7168;         // bytes kept back from s_LM for per-block staging
 constexpr int kMaxLadder = 16;             // light bin ladder levels
 constexpr int kScanTile = 4096;            // elements per scan block (512 threads x 8)
@@ -176,8 +178,9 @@ void launch_csc_count(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nr
                       int32_t* colcnt, cudaStream_t s);
 void launch_slice_sizes(const int32_t* colcnt, const spgemm_csr& B, int64_t kcols,
                         int64_t* colptr_sizes, int64_t* slice_sizes, cudaStream_t s);
+// csc_col: the column of every CSC entry (the outer product's slice of it)
 void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows,
-                        int64_t* cursor, int32_t* csc_row, double* csc_val, cudaStream_t s);
+                        int64_t* cursor, int32_t* csc_row, double* csc_val, int32_t* csc_col, cudaStream_t s);
 void launch_copy_i64(const int64_t* src, int64_t* dst, int64_t n, cudaStream_t s);
 void launch_gather_rows(const int32_t* src, int32_t* io, int64_t n, cudaStream_t s);
 void launch_partition(const int64_t* off, int64_t nseg, int64_t total, int64_t tile, int2* part, cudaStream_t s);
@@ -190,12 +193,21 @@ void launch_row_chunk_counts(const spgemm_csr& A, const int32_t* rows, int64_t n
                              int64_t entries, const int32_t* bh, int64_t v, unsigned long long* counts,
                              cudaStream_t s);
 void launch_heavy_row_len(const spgemm_csr& A, const int32_t* rows, int64_t nrows, int64_t* len, cudaStream_t s);
+// Direct split of level 0: tiles of kOdTile products, each with its first entry of A~_CSC and
+// entry count (launch_od_partition), then the outer product writing into C^_reord.
+struct OdTile {
+  int64_t a_first;
+  int64_t nent;
+  int32_t s0, s1;  // slices of the tile's first and last product
+};
+void launch_od_partition(const int64_t* slice_off, int64_t nseg, int64_t total, const int64_t* colptr,
+                         const spgemm_csr& B, OdTile* tiles, cudaStream_t s);
 void launch_outer_direct(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
-                         const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
-                         const int32_t* xmap, unsigned long long* cursor, int32_t* out_col, double* out_val,
+                         const int32_t* csc_col, const int64_t* slice_off, const OdTile* tiles, int64_t total,
+                         const spgemm_csr& B, unsigned long long* cursor, int32_t* out_col, double* out_val,
                          bool with_vals, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s);
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
-                          const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
+                          const int32_t* csc_col, const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
                           int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
                           unsigned long long* counts, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s);
 void launch_histogram(const int64_t* row_ptr, const int2* part, int64_t total, const int32_t* col, int shift,

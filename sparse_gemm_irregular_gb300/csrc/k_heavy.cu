@@ -121,23 +121,39 @@ void launch_slice_sizes(const int32_t* colcnt, const spgemm_csr& B, int64_t kcol
 __global__ void k_csc_scatter(const int64_t* __restrict__ arp, const int32_t* __restrict__ acol,
                               const double* __restrict__ aval, const int32_t* __restrict__ rows,
                               int64_t nrows, unsigned long long* __restrict__ cursor,
-                              int32_t* __restrict__ crow, double* __restrict__ cval) {
+                              int32_t* __restrict__ crow, double* __restrict__ cval, int32_t* __restrict__ ccol) {
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (w >= nrows) return;
   const int64_t r = rows[w];
   for (int64_t e = arp[r] + lane_id(); e < arp[r + 1]; e += 32) {
-    const unsigned long long pos = atomicAdd(&cursor[acol[e]], 1ull);
+    const int32_t k = acol[e];
+    const unsigned long long pos = atomicAdd(&cursor[k], 1ull);
     crow[pos] = static_cast<int32_t>(w);  // batch-local heavy row (x_map)
     cval[pos] = aval[e];
+    ccol[pos] = k;                        // its column: the slice of the outer product
   }
 }
 void launch_csc_scatter(const spgemm_csr& A, const int32_t* heavy_rows, int64_t nrows, int64_t* cursor,
-                        int32_t* csc_row, double* csc_val, cudaStream_t s) {
+                        int32_t* csc_row, double* csc_val, int32_t* csc_col, cudaStream_t s) {
   if (nrows == 0) return;
   note_launch();
   k_csc_scatter<<<static_cast<unsigned>(ceil_div(nrows * 32, 256)), 256, 0, s>>>(
       A.row_ptr, A.col_idx, A.vals, heavy_rows, nrows, reinterpret_cast<unsigned long long*>(cursor),
-      csc_row, csc_val);
+      csc_row, csc_val, csc_col);
+}
+
+// Slice (column of A~_CSC) of entry a of a block whose entries lie in slices [s0, s1]: the column
+// recorded by the scatter, checked against the block's range (a binary search over colptr would
+// be a chain of dependent loads at the start of every block).
+__device__ __forceinline__ int64_t entry_slice(const int32_t* __restrict__ ccol, const int64_t* __restrict__ colptr,
+                                               int64_t s0, int64_t s1, int64_t a, uint32_t* err) {
+  if (s0 == s1) return s0;
+  const int64_t s = ccol[a];
+  if (s < s0 || s > s1 || a < colptr[s] || a >= colptr[s + 1]) {
+    set_error(err, kErrBounds);
+    return upper_bound_minus1(colptr, s0, s1 + 1, a);
+  }
+  return s;
 }
 
 // ---- static partition of a flattened index space (GroupRange + Search, Algorithms 4 and 5) -----
@@ -173,7 +189,8 @@ struct OpSmem {
 template <bool VALS, bool HIST>
 __global__ void __launch_bounds__(kOpThreads) k_outer_product(
     const int64_t* __restrict__ colptr, const int32_t* __restrict__ crow, const double* __restrict__ cval,
-    const int64_t* __restrict__ slice_off, const int2* __restrict__ part, int64_t total,
+    const int32_t* __restrict__ ccol, const int64_t* __restrict__ slice_off, const int2* __restrict__ part,
+    int64_t total,
     const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol, const double* __restrict__ bval,
     unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col, double* __restrict__ out_val,
     unsigned long long* __restrict__ counts, int shift, int64_t v, uint32_t* err) {
@@ -206,7 +223,7 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
   // partial B rows at both ends of the block's range).
   for (int64_t e = threadIdx.x; e < nent; e += blockDim.x) {
     const int64_t a = a_first + e;
-    const int64_t s = (s0 == s1) ? s0 : upper_bound_minus1(colptr, s0, s1 + 1, a);
+    const int64_t s = entry_slice(ccol, colptr, s0, s1, a, err);
     const int64_t b0 = brp[s];
     const int64_t len = brp[s + 1] - b0;
     const int64_t F = slice_off[s] + (a - colptr[s]) * len;
@@ -287,7 +304,8 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_product(
 }
 
 void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
-                          const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
+                          const int32_t* csc_col, const int64_t* slice_off, const int2* part, int64_t total,
+                         const spgemm_csr& B,
                           int64_t* row_cursor, int32_t* chat_col, double* chat_val, bool with_vals,
                           unsigned long long* counts, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s) {
   if (total == 0) return;
@@ -299,7 +317,8 @@ void launch_outer_product(const int64_t* colptr, const int32_t* csc_row, const d
     cudaFuncSetAttribute(k_outer_product<V, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
                          static_cast<int>(smem));                                                           \
     note_launch();                                                                                          \
-    k_outer_product<V, H><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,  \
+    k_outer_product<V, H><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, csc_col, slice_off, part, \
+                                                         total,                                             \
                                                          B.row_ptr, B.col_idx, B.vals, ull, chat_col,        \
                                                          V ? chat_val : nullptr, counts, shift, nchunks, err); \
   } while (0)
@@ -388,117 +407,158 @@ void launch_heavy_row_len(const spgemm_csr& A, const int32_t* rows, int64_t nrow
   k_heavy_row_len<<<static_cast<unsigned>(ceil_div(nrows, 256)), 256, 0, s>>>(A.row_ptr, rows, nrows, len);
 }
 
-// Outer product writing straight into C^_reord: the same static partition as Algorithm 4, but each
-// run of consecutive elements that belong to one (entry, chunk) reserves its space with one
-// atomic on that C^_reord row's cursor (warp runs found with __match_any_sync) and is written
-// with the column shifted into the chunk's range.
+// Outer product writing straight into C^_reord: the static partition of Algorithm 4 (tiles of
+// kOdTile products over the slices of A~_CSC x B), but each run of consecutive elements that
+// belong to one (entry, chunk) reserves its space with one atomic on that C^_reord row's cursor
+// (warp runs found with __match_any_sync) and is written with the column shifted into the
+// chunk's range.  A tile's first entry and entry count come from the partition kernel (GetAEntry,
+// Eq. 3, with its divisions), so a block starts without a serial chain; its entries are staged
+// in shared memory kOdWin at a time (position of their first product in the tile, source offset
+// in B, row, A value), so any number of entries fits and the shared footprint stays small enough
+// for a full SM of blocks.
+__global__ void k_od_partition(const int64_t* __restrict__ slice_off, int64_t nseg, int64_t total,
+                               const int64_t* __restrict__ colptr, const int64_t* __restrict__ brp, int64_t ntiles,
+                               OdTile* __restrict__ tiles) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b >= ntiles) return;
+  const int64_t g0 = b * kOdTile;
+  const int64_t g1 = min(total, g0 + kOdTile);
+  // last slice starting at or before the tile's ends: never an empty slice (an empty slice
+  // shares its offset with the next one)
+  const int64_t s0 = upper_bound_minus1(slice_off, 0, nseg + 1, g0);
+  const int64_t s1 = upper_bound_minus1(slice_off, s0, nseg + 1, g1 - 1);
+  const int64_t len0 = brp[s0 + 1] - brp[s0];
+  const int64_t len1 = brp[s1 + 1] - brp[s1];
+  OdTile t;
+  t.s0 = static_cast<int32_t>(s0);
+  t.s1 = static_cast<int32_t>(s1);
+  if (len0 <= 0 || len1 <= 0) {  // inconsistent offsets
+    t.a_first = 0;
+    t.nent = 0;
+  } else {
+    t.a_first = colptr[s0] + (g0 - slice_off[s0]) / len0;
+    t.nent = colptr[s1] + (g1 - 1 - slice_off[s1]) / len1 - t.a_first + 1;
+  }
+  tiles[b] = t;
+}
+
+void launch_od_partition(const int64_t* slice_off, int64_t nseg, int64_t total, const int64_t* colptr,
+                         const spgemm_csr& B, OdTile* tiles, cudaStream_t s) {
+  const int64_t ntiles = ceil_div(total, kOdTile);
+  if (ntiles == 0) return;
+  note_launch();
+  k_od_partition<<<static_cast<unsigned>(ceil_div(ntiles, 256)), 256, 0, s>>>(slice_off, nseg, total, colptr,
+                                                                              B.row_ptr, ntiles, tiles);
+}
+
 template <bool VALS>
 __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
     const int64_t* __restrict__ colptr, const int32_t* __restrict__ crow, const double* __restrict__ cval,
-    const int64_t* __restrict__ slice_off, const int2* __restrict__ part, int64_t total,
-    const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol, const double* __restrict__ bval,
-    const int32_t* __restrict__ xmap, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
+    const int32_t* __restrict__ ccol, const int64_t* __restrict__ slice_off, const OdTile* __restrict__ tiles,
+    int64_t total, const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol,
+    const double* __restrict__ bval, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
     double* __restrict__ out_val, int shift, int64_t v, uint32_t* err) {
-  extern __shared__ __align__(16) char smem_raw[];
-  __shared__ int64_t hdr[2];
-  int64_t* src_delta = reinterpret_cast<int64_t*>(smem_raw);
-  int32_t* seg_start = reinterpret_cast<int32_t*>(src_delta + kOpTile);
-  int32_t* seg_row = seg_start + kOpTile;
-  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kOpTile;
-  const int64_t g1 = min(total, g0 + kOpTile);
-  const int2 sp = part[blockIdx.x];
-  const int64_t s0 = sp.x, s1 = sp.y;
-  if (threadIdx.x == 0) {
-    const int64_t len0 = brp[s0 + 1] - brp[s0];
-    const int64_t len1 = brp[s1 + 1] - brp[s1];
-    const int64_t a_first = colptr[s0] + (g0 - slice_off[s0]) / len0;
-    const int64_t a_last = colptr[s1] + (g1 - 1 - slice_off[s1]) / len1;
-    hdr[0] = a_first;
-    hdr[1] = a_last - a_first + 1;
-  }
-  __syncthreads();
-  const int64_t a_first = hdr[0], nent = hdr[1];
-  if (nent > kOpTile || nent <= 0) {
+  __shared__ int32_t seg_start[kOdWin + 1];
+  __shared__ int64_t src_delta[kOdWin];
+  __shared__ int32_t seg_row[kOdWin];
+  __shared__ double seg_a[kOdWin];
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kOdTile;
+  const int64_t g1 = min(total, g0 + kOdTile);
+  const OdTile tl = tiles[blockIdx.x];
+  const int64_t s0 = tl.s0, s1 = tl.s1, a_first = tl.a_first, nent = tl.nent;
+  if (nent <= 0) {
     if (threadIdx.x == 0) set_error(err, kErrBounds);
     return;
   }
-  for (int64_t e = threadIdx.x; e < nent; e += blockDim.x) {
-    const int64_t a = a_first + e;
-    const int64_t s = (s0 == s1) ? s0 : upper_bound_minus1(colptr, s0, s1 + 1, a);
-    const int64_t b0 = brp[s];
-    const int64_t len = brp[s + 1] - b0;
-    const int64_t F = slice_off[s] + (a - colptr[s]) * len;
-    const int64_t lo = max(F, g0);
-    const int64_t clo = lo < g1 ? lo : g1;
-    seg_start[e] = static_cast<int32_t>(clo - g0);
-    src_delta[e] = b0 + (clo - F) - (clo - g0);
-    seg_row[e] = crow[a];
-  }
-  __syncthreads();
   const int32_t n = static_cast<int32_t>(g1 - g0);
   const int64_t wmask = (int64_t(1) << shift) - 1;
-  int32_t e = 0;
-  if (static_cast<int32_t>(threadIdx.x) < n) {
-    int32_t lo = 0, hi = static_cast<int32_t>(nent) - 1;
-    while (lo < hi) {
-      const int32_t mid = (lo + hi + 1) >> 1;
-      if (seg_start[mid] <= static_cast<int32_t>(threadIdx.x)) lo = mid; else hi = mid - 1;
-    }
-    e = lo;
-  }
-  for (int32_t p0 = 0; p0 < n; p0 += blockDim.x) {
-    const int32_t p = p0 + static_cast<int32_t>(threadIdx.x);
-    int key = -1;
-    int32_t c = 0;
-    double val = 0.0;
-    int64_t q = 0;
-    if (p < n) {
-      while (e + 1 < nent && seg_start[e + 1] <= p) ++e;
-      const int64_t src = src_delta[e] + p;
-      c = bcol[src];
-      if (VALS) val = __ldg(&cval[a_first + e]) * bval[src];
-      const int64_t ch = static_cast<int64_t>(c) >> shift;
-      if (c >= 0 && ch < v) {
-        key = static_cast<int>(e * v + ch);
-        const int64_t gid = static_cast<int64_t>(seg_row[e]) * v + ch;
-        q = xmap ? xmap[gid] : gid;
+  const int32_t tid = static_cast<int32_t>(threadIdx.x);
+  for (int64_t w0 = 0; w0 < nent; w0 += kOdWin) {
+    const int32_t wn = static_cast<int32_t>(min(static_cast<int64_t>(kOdWin), nent - w0));
+    // the window's entries, and one more: the start of the next window (or the tile's end)
+    for (int32_t j = tid; j <= wn; j += static_cast<int32_t>(blockDim.x)) {
+      const int64_t e = w0 + j;
+      if (e < nent) {
+        const int64_t a = a_first + e;
+        const int64_t sl = entry_slice(ccol, colptr, s0, s1, a, err);
+        const int64_t b0 = brp[sl];
+        const int64_t len = brp[sl + 1] - b0;
+        const int64_t F = slice_off[sl] + (a - colptr[sl]) * len;
+        const int64_t lo = max(F, g0);
+        const int64_t clo = lo < g1 ? lo : g1;
+        seg_start[j] = static_cast<int32_t>(clo - g0);
+        if (j < wn) {
+          src_delta[j] = b0 + (clo - F) - (clo - g0);
+          seg_row[j] = crow[a];
+          seg_a[j] = VALS ? cval[a] : 0.0;
+        }
       } else {
-        set_error(err, kErrBounds);
+        seg_start[j] = n;
       }
     }
-    const uint32_t peers = __match_any_sync(0xffffffffu, key);
-    const int leader = __ffs(peers) - 1;
-    unsigned long long base = 0;
-    if (key >= 0 && static_cast<int>(lane_id()) == leader)
-      base = atomicAdd(&cursor[q], static_cast<unsigned long long>(__popc(peers)));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (key >= 0) {
-      const int64_t dst = static_cast<int64_t>(base) + __popc(peers & lanemask_lt());
-      out_col[dst] = static_cast<int32_t>(c & wmask);
-      if (VALS) out_val[dst] = val;
+    __syncthreads();
+    const int32_t plo = seg_start[0], phi = seg_start[wn];
+    // this thread's first product: last entry of the window starting at or before it
+    int32_t e = 0;
+    {
+      const int32_t p = plo + tid;
+      int32_t lo = 0, hi = wn - 1;
+      while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (seg_start[mid] <= p) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
     }
+    for (int32_t p0 = plo; p0 < phi; p0 += static_cast<int32_t>(blockDim.x)) {
+      const int32_t p = p0 + tid;
+      int key = -1;
+      int32_t c = 0;
+      double val = 0.0;
+      int64_t q = 0;
+      if (p < phi) {
+        while (e + 1 < wn && seg_start[e + 1] <= p) ++e;
+        const int64_t src = src_delta[e] + p;
+        c = bcol[src];
+        if (VALS) val = seg_a[e] * bval[src];
+        const int64_t ch = static_cast<int64_t>(c) >> shift;
+        if (c >= 0 && ch < v) {
+          key = static_cast<int>(e * v + ch);  // window-local entry: unique within the warp's round
+          q = static_cast<int64_t>(seg_row[e]) * v + ch;
+        } else {
+          set_error(err, kErrBounds);
+        }
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      const int leader = __ffs(peers) - 1;
+      unsigned long long base = 0;
+      if (key >= 0 && static_cast<int>(lane_id()) == leader)
+        base = atomicAdd(&cursor[q], static_cast<unsigned long long>(__popc(peers)));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (key >= 0) {
+        const int64_t dst = static_cast<int64_t>(base) + __popc(peers & lanemask_lt());
+        out_col[dst] = static_cast<int32_t>(c & wmask);
+        if (VALS) out_val[dst] = val;
+      }
+    }
+    __syncthreads();
   }
 }
 
 void launch_outer_direct(const int64_t* colptr, const int32_t* csc_row, const double* csc_val,
-                         const int64_t* slice_off, const int2* part, int64_t total, const spgemm_csr& B,
-                         const int32_t* xmap, unsigned long long* cursor, int32_t* out_col, double* out_val,
+                         const int32_t* csc_col, const int64_t* slice_off, const OdTile* tiles, int64_t total,
+                         const spgemm_csr& B, unsigned long long* cursor, int32_t* out_col, double* out_val,
                          bool with_vals, int shift, int64_t nchunks, uint32_t* err, cudaStream_t s) {
   if (total == 0) return;
-  const size_t smem = kOpTile * (8 + 4 + 4);
-  const unsigned grid = static_cast<unsigned>(ceil_div(total, kOpTile));
+  const unsigned grid = static_cast<unsigned>(ceil_div(total, kOdTile));
   note_launch();
-  if (with_vals) {
-    cudaFuncSetAttribute(k_outer_direct<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k_outer_direct<true><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total, B.row_ptr,
-                                                        B.col_idx, B.vals, xmap, cursor, out_col, out_val, shift,
-                                                        nchunks, err);
-  } else {
-    cudaFuncSetAttribute(k_outer_direct<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k_outer_direct<false><<<grid, kOpThreads, smem, s>>>(colptr, csc_row, csc_val, slice_off, part, total,
-                                                         B.row_ptr, B.col_idx, B.vals, xmap, cursor, out_col, nullptr,
-                                                         shift, nchunks, err);
-  }
+  if (with_vals)
+    k_outer_direct<true><<<grid, kOpThreads, 0, s>>>(colptr, csc_row, csc_val, csc_col, slice_off, tiles, total,
+                                                     B.row_ptr, B.col_idx, B.vals, cursor, out_col, out_val, shift,
+                                                     nchunks, err);
+  else
+    k_outer_direct<false><<<grid, kOpThreads, 0, s>>>(colptr, csc_row, csc_val, csc_col, slice_off, tiles, total,
+                                                      B.row_ptr, B.col_idx, B.vals, cursor, out_col, nullptr, shift,
+                                                      nchunks, err);
 }
 
 // ---- histogram and multisplit (Algorithm 5) -----------------------------------------------------
