@@ -618,10 +618,18 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   launch_slice_sizes(colcnt, h->B, kc, colptr, slice_off, h->st);
   SG_TRY(scan(h, colptr, colptr, kc));
   SG_TRY(scan(h, slice_off, slice_off, kc));
+  // A batch whose chunks the symbolic phase counted from generated products (the numeric
+  // expansion of a recomputed batch) already knows its entries and, in its descriptors, where
+  // every (row, chunk) run of C^_reord starts: no synchronisation and no second count.
+  const bool from_symbolic = h->gen_symbolic && !record;
   int64_t nnzh = 0;
-  SG_TRY(check_cuda(cudaMemcpyAsync(&nnzh, colptr + kc, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
-                    "copy masked nnz"));
-  SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "masked csc"));
+  if (from_symbolic) {
+    nnzh = hb.entries;
+  } else {
+    SG_TRY(check_cuda(cudaMemcpyAsync(&nnzh, colptr + kc, sizeof(int64_t), cudaMemcpyDeviceToHost, h->st),
+                      "copy masked nnz"));
+    SG_TRY(check_cuda(cudaStreamSynchronize(h->st), "masked csc"));
+  }
   int32_t *csc_row, *csc_col;
   double* csc_val;
   int64_t* cursor;
@@ -631,30 +639,32 @@ int heavy_direct(spgemm_ctx* h, HeavyBatch& hb, bool vals, bool record) {
   SG_ALLOC(cursor, int64_t, std::max<int64_t>(kc, R * v));
   launch_copy_i64(colptr, cursor, kc, h->st);
   launch_csc_scatter(h->A, rows, R, cursor, csc_row, csc_val, csc_col, h->st);
-  // level-0 histogram from the chunk histograms of the rows of B
-  int32_t* bh;
-  unsigned long long* counts;
-  int64_t* rptr;
-  int32_t *out_row, *out_base;
+  unsigned long long* counts = nullptr;
+  int64_t* rptr = nullptr;
+  int32_t *out_row = nullptr, *out_base = nullptr;
   const int64_t nout = R * v;
-  SG_TRY(ensure_bh(h));
-  bh = h->d_bh;
-  SG_ALLOC(counts, unsigned long long, nout);
-  SG_ALLOC(rptr, int64_t, nout + 1);
-  SG_ALLOC(out_row, int32_t, nout);
-  SG_ALLOC(out_base, int32_t, nout);
-  int64_t* hrp;
-  SG_ALLOC(hrp, int64_t, R + 1);
-  cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
-  launch_heavy_row_len(h->A, rows, R, hrp, h->st);
-  SG_TRY(scan(h, hrp, hrp, R));
-  launch_row_chunk_counts(h->A, rows, R, hrp, nnzh, bh, v, counts, h->st);
-  ws_free(h, hrp);
-  launch_reord_meta(counts, R, v, nullptr, nullptr, nullptr, width, rptr, out_row, out_base, h->st);
-  SG_TRY(scan(h, rptr, rptr, nout));
-  launch_copy_i64(rptr, cursor, nout, h->st);
-  // descriptors counted from generated products (chunk-major): onto this expansion's C^_reord rows
-  if (h->gen_symbolic && !record) launch_fused_starts(rptr, hb.f_row, hb.f_base, hb.nfinal, v, shift, hb.f_start, h->st);
+  if (from_symbolic) {
+    launch_cursor_from_desc(hb.f_start, hb.f_row, hb.f_base, hb.nfinal, v, shift, cursor, h->st);
+  } else {
+    // level-0 histogram from the chunk histograms of the rows of B
+    int32_t* bh;
+    SG_TRY(ensure_bh(h));
+    bh = h->d_bh;
+    SG_ALLOC(counts, unsigned long long, nout);
+    SG_ALLOC(rptr, int64_t, nout + 1);
+    SG_ALLOC(out_row, int32_t, nout);
+    SG_ALLOC(out_base, int32_t, nout);
+    int64_t* hrp;
+    SG_ALLOC(hrp, int64_t, R + 1);
+    cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * nout, h->st);
+    launch_heavy_row_len(h->A, rows, R, hrp, h->st);
+    SG_TRY(scan(h, hrp, hrp, R));
+    launch_row_chunk_counts(h->A, rows, R, hrp, nnzh, bh, v, counts, h->st);
+    ws_free(h, hrp);
+    launch_reord_meta(counts, R, v, nullptr, nullptr, nullptr, width, rptr, out_row, out_base, h->st);
+    SG_TRY(scan(h, rptr, rptr, nout));
+    launch_copy_i64(rptr, cursor, nout, h->st);
+  }
   OdTile* part;
   SG_ALLOC(part, OdTile, std::max<int64_t>(1, ceil_div(hb.elems, kOdTile)));
   launch_od_partition(slice_off, kc, hb.elems, colptr, h->B, part, h->st);
@@ -793,8 +803,14 @@ int heavy_fused(spgemm_ctx* h, HeavyBatch& hb) {
   SG_ALLOC(hb.f_cnt, int64_t, R * v);
   SG_ALLOC(hb.f_row, int32_t, R * v);
   SG_ALLOC(hb.f_base, int32_t, R * v);
-  launch_fused_desc(counts, R, v, W, hb.f_cnt, hb.f_row, hb.f_base, hb.f_start, h->st);
+  int64_t* rptr = nullptr;
+  if (h->gen_symbolic) {  // where every (row, chunk) run of the numeric expansion starts
+    SG_ALLOC(rptr, int64_t, R * v + 1);
+    SG_TRY(scan(h, reinterpret_cast<const int64_t*>(counts), rptr, R * v));
+  }
+  launch_fused_desc(counts, rptr, R, v, W, hb.f_cnt, hb.f_row, hb.f_base, hb.f_start, h->st);
   ws_free(h, counts);
+  ws_free(h, rptr);
   return SPGEMM_OK;
 }
 

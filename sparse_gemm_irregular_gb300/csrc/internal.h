@@ -279,13 +279,14 @@ void launch_bsplit(const spgemm_csr& B, const int32_t* colcnt, const int32_t* bh
 // (ecol: E int32 scratch, the A column of every entry)
 void launch_segtable(const spgemm_csr& A, const int32_t* rows, int64_t R, const int64_t* hrp, const spgemm_csr& B,
                      const int32_t* bo, int64_t v, int64_t E, int32_t* ecol, int32_t* seg, cudaStream_t s);
-// f_start[q] = rptr[f_row[q] * v + (f_base[q] >> shift)]: generated-symbolic descriptors onto the
-// C^_reord rows of the direct split
-void launch_fused_starts(const int64_t* rptr, const int32_t* f_row, const int32_t* f_base, int64_t n, int64_t v,
-                         int shift, int64_t* f_start, cudaStream_t s);
-// final chunks of a batch from its level-0 counts, chunk-major
-void launch_fused_desc(const unsigned long long* counts, int64_t R, int64_t v, int64_t width, int64_t* f_cnt,
-                       int32_t* f_row, int32_t* f_base, int64_t* f_start, cudaStream_t s);
+// cursor[f_row[q] * v + (f_base[q] >> shift)] = f_start[q]: the direct split's cursors of a batch
+// whose descriptors hold the run starts (generated symbolic)
+void launch_cursor_from_desc(const int64_t* f_start, const int32_t* f_row, const int32_t* f_base, int64_t n,
+                             int64_t v, int shift, int64_t* cursor, cudaStream_t s);
+// final chunks of a batch from its level-0 counts, chunk-major (rptr: the counts' exclusive scan,
+// the run starts of the numeric expansion, or null)
+void launch_fused_desc(const unsigned long long* counts, const int64_t* rptr, int64_t R, int64_t v, int64_t width,
+                       int64_t* f_cnt, int32_t* f_row, int32_t* f_base, int64_t* f_start, cudaStream_t s);
 // mode 0 symbolic, 1 hash numeric, 2 dense numeric (persistent blocks, counter zeroed here)
 void launch_fused_chunks(const FusedSrc& f, const ChunkSet& cs, const int32_t* list, int64_t count, int64_t width,
                          int mode, int64_t slots, int tpr, const Sink& sink, uint32_t* err, int* counter,

@@ -98,23 +98,24 @@ void launch_bsplit(const spgemm_csr& B, const int32_t* colcnt, const int32_t* bh
 
 // Final chunks of a batch straight from the level-0 counts (row-major counts[p * v + c]),
 // enumerated chunk-major (q = c * R + p): the chunks that run together then read the same
-// column block of B_split, which stays in L2.
-__global__ void k_fused_desc(const unsigned long long* __restrict__ counts, int64_t R, int64_t v, int64_t width,
-                             int64_t* __restrict__ fcnt, int32_t* __restrict__ frow, int32_t* __restrict__ fbase,
-                             int64_t* __restrict__ fstart) {
+// column block of B_split, which stays in L2.  rptr (the exclusive scan of the counts, or null):
+// where each chunk's run of C^_reord starts when the numeric phase expands the batch.
+__global__ void k_fused_desc(const unsigned long long* __restrict__ counts, const int64_t* __restrict__ rptr,
+                             int64_t R, int64_t v, int64_t width, int64_t* __restrict__ fcnt,
+                             int32_t* __restrict__ frow, int32_t* __restrict__ fbase, int64_t* __restrict__ fstart) {
   const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (q >= R * v) return;
   const int64_t c = q / R, p = q - c * R;
   fcnt[q] = static_cast<int64_t>(counts[p * v + c]);
   frow[q] = static_cast<int32_t>(p);
   fbase[q] = static_cast<int32_t>(c * width);
-  fstart[q] = 0;  // nothing stored: the products are generated
+  fstart[q] = rptr ? rptr[p * v + c] : 0;  // nothing stored when the products are generated
 }
-void launch_fused_desc(const unsigned long long* counts, int64_t R, int64_t v, int64_t width, int64_t* f_cnt,
-                       int32_t* f_row, int32_t* f_base, int64_t* f_start, cudaStream_t s) {
+void launch_fused_desc(const unsigned long long* counts, const int64_t* rptr, int64_t R, int64_t v, int64_t width,
+                       int64_t* f_cnt, int32_t* f_row, int32_t* f_base, int64_t* f_start, cudaStream_t s) {
   if (R * v == 0) return;
   note_launch();
-  k_fused_desc<<<static_cast<unsigned>(ceil_div(R * v, 256)), 256, 0, s>>>(counts, R, v, width, f_cnt, f_row,
+  k_fused_desc<<<static_cast<unsigned>(ceil_div(R * v, 256)), 256, 0, s>>>(counts, rptr, R, v, width, f_cnt, f_row,
                                                                           f_base, f_start);
 }
 
@@ -161,19 +162,20 @@ void launch_segtable(const spgemm_csr& A, const int32_t* rows, int64_t R, const 
   k_segtable<<<grid, 256, 0, s>>>(ecol, E, B.row_ptr, bo, v, seg);
 }
 
-// Descriptors of generated-symbolic batches (chunk-major, see k_fused_desc) pointed at the C^_reord
-// rows that the direct split of level 0 builds in the numeric phase (row-major, rptr[p * v + c]).
-__global__ void k_fused_starts(const int64_t* __restrict__ rptr, const int32_t* __restrict__ frow,
-                               const int32_t* __restrict__ fbase, int64_t n, int64_t v, int shift,
-                               int64_t* __restrict__ fstart) {
+// The direct split's reservation cursors of a batch whose run starts the symbolic phase kept in
+// its descriptors: cursor[row * v + chunk] = f_start of that (row, chunk).
+__global__ void k_cursor_from_desc(const int64_t* __restrict__ fstart, const int32_t* __restrict__ frow,
+                                   const int32_t* __restrict__ fbase, int64_t n, int64_t v, int shift,
+                                   int64_t* __restrict__ cursor) {
   const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (q < n) fstart[q] = rptr[static_cast<int64_t>(frow[q]) * v + (fbase[q] >> shift)];
+  if (q < n) cursor[static_cast<int64_t>(frow[q]) * v + (fbase[q] >> shift)] = fstart[q];
 }
-void launch_fused_starts(const int64_t* rptr, const int32_t* f_row, const int32_t* f_base, int64_t n, int64_t v,
-                         int shift, int64_t* f_start, cudaStream_t s) {
+void launch_cursor_from_desc(const int64_t* f_start, const int32_t* f_row, const int32_t* f_base, int64_t n,
+                             int64_t v, int shift, int64_t* cursor, cudaStream_t s) {
   if (n == 0) return;
   note_launch();
-  k_fused_starts<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(rptr, f_row, f_base, n, v, shift, f_start);
+  k_cursor_from_desc<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(f_start, f_row, f_base, n, v, shift,
+                                                                             cursor);
 }
 
 // ---- product generator -----------------------------------------------------------------------
