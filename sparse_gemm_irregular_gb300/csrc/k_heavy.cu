@@ -536,8 +536,10 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
       base = __shfl_sync(0xffffffffu, base, leader);
       if (key >= 0) {
         const int64_t dst = static_cast<int64_t>(base) + __popc(peers & lanemask_lt());
-        out_col[dst] = static_cast<int32_t>(c & wmask);
-        if (VALS) out_val[dst] = val;
+        // evict-first: C^_reord is read back only by the next kernel, while the rows of B the
+        // tile reads are reused by the tiles after it
+        __stcs(out_col + dst, static_cast<int32_t>(c & wmask));
+        if (VALS) __stcs(out_val + dst, val);
       }
     }
     __syncthreads();
