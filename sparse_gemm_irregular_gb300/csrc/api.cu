@@ -846,8 +846,8 @@ int heavy_chunk_symbolic(spgemm_ctx* h, HeavyBatch& hb, int64_t* row_nnz) {
     ws_free(h, starts);
   }
   if (!h->fused && !(h->opt.flags & SPGEMM_FLAG_HASH_PER_CHUNK)) {
-    // descriptors of the smallest numeric hash bin: one buffer sized by the largest batch, so
-    // the numeric phase allocates nothing
+    // descriptors of the two numeric hash bins: one buffer sized by the largest batch, so the
+    // numeric phase allocates nothing
     const int b0 = h->lad.n;
     const int64_t need = hb.f_bin_start[b0 + 2] - hb.f_bin_start[b0];  // the two hash bins
     if (need > h->cdesc_cap) {
