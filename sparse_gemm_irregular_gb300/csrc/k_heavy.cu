@@ -458,9 +458,12 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
     int64_t total, const int64_t* __restrict__ brp, const int32_t* __restrict__ bcol,
     const double* __restrict__ bval, unsigned long long* __restrict__ cursor, int32_t* __restrict__ out_col,
     double* __restrict__ out_val, int shift, int64_t v, uint32_t* err) {
+  // per staged entry: where its products start in the tile, B's columns and values of its products
+  // indexed by the tile position, its C^_reord row's cursors, and its A value
   __shared__ int32_t seg_start[kOdWin + 1];
-  __shared__ int64_t src_delta[kOdWin];
-  __shared__ int32_t seg_row[kOdWin];
+  __shared__ const int32_t* seg_bc[kOdWin];
+  __shared__ const double* seg_bv[kOdWin];
+  __shared__ unsigned long long* seg_cur[kOdWin];
   __shared__ double seg_a[kOdWin];
   const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kOdTile;
   const int64_t g1 = min(total, g0 + kOdTile);
@@ -471,7 +474,8 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
     return;
   }
   const int32_t n = static_cast<int32_t>(g1 - g0);
-  const int64_t wmask = (int64_t(1) << shift) - 1;
+  const uint32_t wmask = (1u << shift) - 1u;
+  const uint32_t uv = static_cast<uint32_t>(v);
   const int32_t tid = static_cast<int32_t>(threadIdx.x);
   for (int64_t w0 = 0; w0 < nent; w0 += kOdWin) {
     const int32_t wn = static_cast<int32_t>(min(static_cast<int64_t>(kOdWin), nent - w0));
@@ -488,8 +492,10 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
         const int64_t clo = lo < g1 ? lo : g1;
         seg_start[j] = static_cast<int32_t>(clo - g0);
         if (j < wn) {
-          src_delta[j] = b0 + (clo - F) - (clo - g0);
-          seg_row[j] = crow[a];
+          const int64_t sd = b0 + (clo - F) - (clo - g0);  // B position of tile position 0
+          seg_bc[j] = bcol + sd;
+          seg_bv[j] = VALS ? bval + sd : nullptr;
+          seg_cur[j] = cursor + static_cast<int64_t>(crow[a]) * v;
           seg_a[j] = VALS ? cval[a] : 0.0;
         }
       } else {
@@ -514,16 +520,15 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
       int key = -1;
       int32_t c = 0;
       double val = 0.0;
-      int64_t q = 0;
+      unsigned long long* cur = nullptr;
       if (p < phi) {
         while (e + 1 < wn && seg_start[e + 1] <= p) ++e;
-        const int64_t src = src_delta[e] + p;
-        c = bcol[src];
-        if (VALS) val = seg_a[e] * bval[src];
-        const int64_t ch = static_cast<int64_t>(c) >> shift;
-        if (c >= 0 && ch < v) {
-          key = static_cast<int>(e * v + ch);  // window-local entry: unique within the warp's round
-          q = static_cast<int64_t>(seg_row[e]) * v + ch;
+        c = seg_bc[e][p];
+        if (VALS) val = seg_a[e] * seg_bv[e][p];
+        const uint32_t ch = static_cast<uint32_t>(c) >> shift;  // a negative column lands above v
+        if (ch < uv) {
+          key = e * static_cast<int>(uv) + static_cast<int>(ch);  // window-local entry: unique in the round
+          cur = seg_cur[e] + ch;
         } else {
           set_error(err, kErrBounds);
         }
@@ -532,13 +537,13 @@ __global__ void __launch_bounds__(kOpThreads) k_outer_direct(
       const int leader = __ffs(peers) - 1;
       unsigned long long base = 0;
       if (key >= 0 && static_cast<int>(lane_id()) == leader)
-        base = atomicAdd(&cursor[q], static_cast<unsigned long long>(__popc(peers)));
+        base = atomicAdd(cur, static_cast<unsigned long long>(__popc(peers)));
       base = __shfl_sync(0xffffffffu, base, leader);
       if (key >= 0) {
         const int64_t dst = static_cast<int64_t>(base) + __popc(peers & lanemask_lt());
         // evict-first: C^_reord is read back only by the next kernel, while the rows of B the
         // tile reads are reused by the tiles after it
-        __stcs(out_col + dst, static_cast<int32_t>(c & wmask));
+        __stcs(out_col + dst, static_cast<int32_t>(static_cast<uint32_t>(c) & wmask));
         if (VALS) __stcs(out_val + dst, val);
       }
     }
