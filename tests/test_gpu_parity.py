@@ -469,6 +469,27 @@ def test_rows_at_tau(gpu_lib):
         compare_full(A, B, rp, col, val)
 
 
+@pytest.mark.parametrize("flags", [0, 131072, 8192])
+def test_chunks_at_hash_group_switch(gpu_lib, flags):
+    """Final chunks of 256 elements (the largest on a warp group), 257 (the smallest on a block
+    group), 66 with 33 distinct columns (just past a 64-slot table), 289, 513 and 770 elements
+    (table sizes 1024 and 2048 of the block groups); by the persistent groups (default), one warp
+    or block per chunk, and the generated chunks.  Chunk width 2048, every row heavy."""
+    W = 2048
+    ent_b = [(0, 3 * c, 1.0 + c / 512) for c in range(256)]               # 256 columns in chunk 0
+    ent_b += [(1, W + 2 * c, 0.5 + c / 1024) for c in range(257)]         # 257 columns in chunk 1
+    ent_b += [(2, 5 * c, -1.0 + c / 64) for c in range(33)]               # 33 columns in chunk 0
+    ent_b += [(3, W + 3 * c, 0.25 + c / 2048) for c in range(513)]        # 513 columns in chunk 1
+    B = _csr(4, 2 * W, ent_b)
+    A = _csr(4, 4, [(0, 0, 1.5), (0, 1, -0.5),                # chunks of 256 and 257 elements
+                    (1, 2, 1.0), (1, 2, 3.0), (1, 3, 0.75),   # 66 elements on 33 columns; 513
+                    (2, 0, 2.0), (2, 2, -1.25),               # 289 elements, shared columns
+                    (3, 1, 0.5), (3, 3, 1.5)])                # 770 elements
+    rp, col, val, st = gpu_product(A, B, opts(tau=32, chunk_width=W, flags=flags))
+    assert st.rows_heavy == 4
+    compare_full(A, B, rp, col, val)
+
+
 @pytest.mark.parametrize("flags", [0, 8192])
 def test_chunks_at_dense_switch(gpu_lib, flags):
     """Final chunks of exactly 1024 elements take a hash accumulator, 1025 the dense one (the
